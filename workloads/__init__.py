@@ -1,0 +1,212 @@
+"""Seeded synthetic decode workloads.
+
+One query token per sequence attends over a long KV cache that is split into
+W segments ("Eliminating Multi-GPU Performance Taxes", review page, notation
+table and the Flash Decode global-reduction equation).  The pages measure
+Flash Decode on synthetic shapes only (batch 1, 96 query heads, head dim 128,
+KV length 32K..2M, FP16; Flash Decode setup paragraph), so every workload here
+is synthetic: q, K and V are standard-normal draws from a seeded generator,
+stored in the 16-bit type of the case.
+
+This module is shared by the oracle tests, the GPU parity tests and the
+benchmark.  It only draws numbers and lays them out; it holds none of the
+attention arithmetic (no scores, no softmax, no combine).
+
+Layouts (all C-contiguous):
+  q  [B, Hq, d]
+  k  [N, Hkv, d]   sequence b occupies rows [cu[b], cu[b] + L_b), N = sum L_b
+  v  [N, Hkv, d]
+16-bit storage: ``np.float16`` for f16, ``np.uint16`` holding bf16 bit
+patterns for bf16 (numpy has no bfloat16 type).
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass, field
+
+import numpy as np
+
+F16 = "f16"
+BF16 = "bf16"
+
+# Independent generator streams per tensor (q, K, V, spike positions, lengths).
+_STREAM_Q, _STREAM_K, _STREAM_V, _STREAM_SPIKE, _STREAM_LEN = 1, 2, 3, 4, 5
+
+_CHUNK = 1 << 25  # elements drawn per generator call (bounds fp32 temporaries)
+
+
+@dataclass
+class DecodeProblem:
+    name: str
+    B: int
+    Hq: int
+    Hkv: int
+    d: int
+    seqlens: np.ndarray          # int32 [B]
+    W: np.ndarray                # int32 [B], segments per sequence
+    dtype: str                   # "f16" | "bf16"
+    q: np.ndarray
+    k: np.ndarray
+    v: np.ndarray
+    seed: int
+    literal_w: bool = False      # run exactly W segments per sequence (no sub-chunks)
+    notes: dict = field(default_factory=dict)
+
+    @property
+    def cu_seqlens(self) -> np.ndarray:
+        cu = np.zeros(self.B + 1, dtype=np.int64)
+        np.cumsum(self.seqlens.astype(np.int64), out=cu[1:])
+        return cu
+
+    @property
+    def n_tokens(self) -> int:
+        return int(self.seqlens.astype(np.int64).sum())
+
+    @property
+    def kv_bytes(self) -> int:
+        """Bytes of K and V that one decode must read (2 bytes per element)."""
+        return 2 * self.n_tokens * self.Hkv * self.d * 2
+
+    def describe(self) -> dict:
+        return {
+            "workload": self.name, "B": self.B, "Hq": self.Hq, "Hkv": self.Hkv,
+            "d": self.d, "dtype": self.dtype, "seed": self.seed,
+            "L": (int(self.seqlens[0]) if self.B == 1 else
+                  {"min": int(self.seqlens.min()), "max": int(self.seqlens.max()),
+                   "sum": self.n_tokens}),
+            "W": (int(self.W[0]) if np.all(self.W == self.W[0]) else
+                  {"min": int(self.W.min()), "max": int(self.W.max()),
+                   "sum": int(self.W.sum())}),
+            "literal_w": self.literal_w, **self.notes,
+        }
+
+
+def rng(seed: int, stream: int) -> np.random.Generator:
+    """Independent, reproducible stream ``stream`` of the workload seeded ``seed``."""
+    return np.random.default_rng(np.random.SeedSequence([int(seed), int(stream)]))
+
+
+def f32_to_bf16_bits(x: np.ndarray) -> np.ndarray:
+    """Round float32 to bfloat16 (round to nearest, ties to even); return the bit patterns."""
+    u = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32)
+    rounding = ((u >> 16) & 1) + np.uint32(0x7FFF)
+    return ((u + rounding) >> 16).astype(np.uint16)
+
+
+def bf16_bits_to_f32(bits: np.ndarray) -> np.ndarray:
+    """Exact widening of bfloat16 bit patterns to float32."""
+    return (np.asarray(bits, dtype=np.uint16).astype(np.uint32) << 16).view(np.float32)
+
+
+def to_storage(x32: np.ndarray, dtype: str) -> np.ndarray:
+    if dtype == F16:
+        return x32.astype(np.float16)
+    if dtype == BF16:
+        return f32_to_bf16_bits(x32)
+    raise ValueError(f"unknown dtype {dtype!r}")
+
+
+def storage_to_f32(x: np.ndarray, dtype: str) -> np.ndarray:
+    """Exact widening of the stored 16-bit values to float32."""
+    if dtype == F16:
+        return np.asarray(x, dtype=np.float16).astype(np.float32)
+    if dtype == BF16:
+        return bf16_bits_to_f32(x)
+    raise ValueError(f"unknown dtype {dtype!r}")
+
+
+def normal(gen: np.random.Generator, shape, dtype: str, scale_rows=None) -> np.ndarray:
+    """Standard-normal draw in float32, optionally scaling whole token rows, stored as ``dtype``.
+
+    ``scale_rows`` is ``(row_indices, factor)``: those rows of the leading axis
+    are multiplied by ``factor`` in float32 before the single rounding to 16 bits.
+    """
+    shape = tuple(int(s) for s in shape)
+    total = int(np.prod(shape)) if shape else 1
+    out = np.empty(total, dtype=np.float16 if dtype == F16 else np.uint16)
+    row = int(np.prod(shape[1:])) if len(shape) > 1 else 1
+    rows_hit = None
+    if scale_rows is not None:
+        rows_hit = (np.sort(np.asarray(scale_rows[0], dtype=np.int64)), np.float32(scale_rows[1]))
+    chunk = max(row, (_CHUNK // row) * row)
+    for start in range(0, total, chunk):
+        stop = min(total, start + chunk)
+        x = gen.standard_normal(stop - start, dtype=np.float32)
+        if rows_hit is not None:
+            r0, r1 = start // row, stop // row
+            idx, factor = rows_hit
+            sel = idx[(idx >= r0) & (idx < r1)]
+            for r in sel:
+                a = (int(r) - r0) * row
+                x[a:a + row] *= factor
+        out[start:stop] = to_storage(x, dtype)
+    return out.reshape(shape)
+
+
+def make_problem(name, B, Hq, Hkv, d, seqlens, W, dtype=F16, seed=0, literal_w=False,
+                 k_spike_rows=None, k_spike_factor=20.0, notes=None) -> DecodeProblem:
+    seqlens = np.asarray(seqlens, dtype=np.int32).reshape(B)
+    W = np.broadcast_to(np.asarray(W, dtype=np.int32), (B,)).copy()
+    N = int(seqlens.astype(np.int64).sum())
+    q = normal(rng(seed, _STREAM_Q), (B, Hq, d), dtype)
+    spike = None if k_spike_rows is None else (k_spike_rows, k_spike_factor)
+    k = normal(rng(seed, _STREAM_K), (N, Hkv, d), dtype, scale_rows=spike)
+    v = normal(rng(seed, _STREAM_V), (N, Hkv, d), dtype)
+    return DecodeProblem(name, B, Hq, Hkv, d, seqlens, W, dtype, q, k, v, seed,
+                         literal_w, dict(notes or {}))
+
+
+# ---------------------------------------------------------------------------
+# The five decode cases (one fixed seed each, 1000 + index).
+# ---------------------------------------------------------------------------
+
+def mha8_d64_L4k_W4(seed: int = 1000) -> DecodeProblem:
+    """B=1, Hq=Hkv=8, d=64, L=4096 split into W=4 segments of 1024; fp16 N(0,1)."""
+    return make_problem("mha8_d64_L4k_W4", 1, 8, 8, 64, [4096], 4, F16, seed)
+
+
+def gqa4_d128_L32k_W8(seed: int = 1001) -> DecodeProblem:
+    """B=1 decode, Hq=32 / Hkv=8 (4 query heads per KV head), d=128, L=32768, W=8; fp16 N(0,1)."""
+    return make_problem("gqa4_d128_L32k_W8", 1, 32, 8, 128, [32768], 8, F16, seed)
+
+
+def gqa8_d128_L128k_W8_spiky(seed: int = 1002) -> DecodeProblem:
+    """B=1, Hq=64 / Hkv=8, d=128, L=131072, W=8; fp16 N(0,1) with 0.1% of key rows x20.
+
+    round(0.001 * L) = 131 token positions are drawn without replacement from
+    their own stream; every KV head of K at those positions is multiplied by 20
+    in float32 before rounding once to fp16.  V is untouched.
+    """
+    L = 131072
+    n_spike = int(round(0.001 * L))
+    rows = rng(seed, _STREAM_SPIKE).choice(L, size=n_spike, replace=False)
+    return make_problem("gqa8_d128_L128k_W8_spiky", 1, 64, 8, 128, [L], 8, F16, seed,
+                        k_spike_rows=rows, k_spike_factor=20.0,
+                        notes={"k_spike_rows": n_spike, "k_spike_factor": 20.0})
+
+
+def ragged16_gqa4_d128(seed: int = 1003) -> DecodeProblem:
+    """B=16 ragged batch, Hq=32 / Hkv=8, d=128, L_b uniform in [1024, 65536], W_b = ceil(L_b/4096)."""
+    lens = rng(seed, _STREAM_LEN).integers(1024, 65536, size=16, endpoint=True).astype(np.int32)
+    W = ((lens.astype(np.int64) + 4095) // 4096).astype(np.int32)
+    return make_problem("ragged16_gqa4_d128", 16, 32, 8, 128, lens, W, F16, seed)
+
+
+def batch64_gqa4_d128_L8k_bf16(W: int = 1, seed: int = 1004) -> DecodeProblem:
+    """B=64, Hq=32 / Hkv=8, d=128, L=8192 each, bf16 N(0,1); W in {1,2,4,8,16}, exactly W segments.
+
+    The inputs do not depend on W (same seed), so a W sweep runs on identical data.
+    """
+    p = make_problem(f"batch64_gqa4_d128_L8k_bf16_W{W}", 64, 32, 8, 128, [8192] * 64, W,
+                     BF16, seed, literal_w=True)
+    return p
+
+
+CASES = {
+    "mha8_d64_L4k_W4": mha8_d64_L4k_W4,
+    "gqa4_d128_L32k_W8": gqa4_d128_L32k_W8,
+    "gqa8_d128_L128k_W8_spiky": gqa8_d128_L128k_W8_spiky,
+    "ragged16_gqa4_d128": ragged16_gqa4_d128,
+    "batch64_gqa4_d128_L8k_bf16": batch64_gqa4_d128_L8k_bf16,
+}
+
+W_SWEEP = (1, 2, 4, 8, 16)
