@@ -1,0 +1,514 @@
+#!/usr/bin/env python3
+"""Benchmark of the fused split-KV Flash Decode on GB300.
+
+Prints ONE JSON line on rank 0.  A step is one fused decode (all of the hot
+path: KV streaming, scores, online softmax, P.V, partial write, arrival and the
+last-arriver combine) over one batch of synthetic input.
+
+  value     KV-read GB/s over exactly --steps steps replayed from a CUDA graph,
+            inputs resident in HBM; K/V rotate over enough copies that every
+            step reads from HBM (copies x bytes >= 4 x L2).
+  latency   per-launch device time (CUDA events around every launch).
+  roofline  KV bytes per launch / mean launch time vs the measured HBM peak.
+  e2e       the same metric through fd_decode with pinned HOST buffers: every
+            step copies q, K, V in and out, lse back.
+  cpu_baseline  the fp64 oracle on the host cores (1 thread), bounded sample.
+
+``--impl reference`` times the fp64 oracle instead (rank 0 only).
+Multi-GPU: N independent replicas (the decode has no cross-GPU exchange).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+DEFAULT_WORKLOAD = "gqa4_d128_L32k_W8"
+METRIC = "decode latency (µs) and achieved KV-read HBM GB/s (% of GB300 peak), 1 GPU"
+FALLBACK_HBM_GBS = 6800.0
+
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["fd", "reference"], default="fd")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--W", type=int, default=1, help="segments for the batch64 W-sweep workload")
+    ap.add_argument("--chunks", type=int, default=0, help="chunks per segment (0 = planner)")
+    ap.add_argument("--two-launch", action="store_true", help="split + combine as two kernels")
+    ap.add_argument("--soak-s", type=float, default=1.5, help="untimed load before timing (clocks)")
+    ap.add_argument("--e2e-steps", type=int, default=30)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--ref-budget-s", type=float, default=120.0)
+    ap.add_argument("--no-graph", action="store_true", help="launch each step from Python")
+    ap.add_argument("--cpu-baseline-only", action="store_true", help=argparse.SUPPRESS)
+    return ap.parse_args(argv)
+
+
+def make_problem(args):
+    import workloads
+    if args.workload.startswith("batch64"):
+        return workloads.batch64_gqa4_d128_L8k_bf16(W=args.W)
+    return workloads.CASES[args.workload]()
+
+
+# ---------------------------------------------------------------------------
+# Multi-rank plumbing (replicas only).
+# ---------------------------------------------------------------------------
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def dist_init(world, backend):
+    import torch.distributed as dist
+    if world > 1 and not dist.is_initialized():
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        dist.init_process_group(backend=backend)
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(value: float, world: int, device=None) -> float:
+    """Largest `value` over all ranks (every rank gets it)."""
+    if world <= 1:
+        return float(value)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate_throughput(units_per_rank: float, elapsed_s: float, world: int, device=None) -> dict:
+    """Whole-job throughput: the units all ranks processed / the slowest rank's time."""
+    slowest = max_over_ranks(elapsed_s, world, device)
+    return {"elapsed_s": slowest, "units": units_per_rank * world,
+            "throughput": units_per_rank * world / slowest if slowest > 0 else float("nan")}
+
+
+# ---------------------------------------------------------------------------
+# Clock sampling during the measured window.
+# ---------------------------------------------------------------------------
+
+_REASON_BITS = {
+    0x1: "gpu_idle", 0x2: "applications_clocks_setting", 0x4: "sw_power_cap",
+    0x8: "hw_slowdown", 0x10: "sync_boost", 0x20: "sw_thermal_slowdown",
+    0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown", 0x100: "display_clock_setting",
+}
+
+
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active")
+
+    def __init__(self, gpu_id: str, period_ms: int = 100):
+        self.gpu_id, self.period_ms = gpu_id, period_ms
+        self.lines, self.proc, self.thread = [], None, None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", self.gpu_id, f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", f"-lms={self.period_ms}"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.proc = None
+            return self
+
+        def pump():
+            for line in self.proc.stdout:
+                self.lines.append((time.time(), line.strip()))
+        self.thread = threading.Thread(target=pump, daemon=True)
+        self.thread.start()
+        return self
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        if self.thread is not None:
+            self.thread.join(timeout=5)
+
+    def summary(self, t0: float, t1: float) -> dict:
+        sm, mx, pw, reasons = [], [], [], set()
+        for ts, line in self.lines:
+            if not (t0 <= ts <= t1):
+                continue
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 5:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+                pw.append(float(parts[3]))
+                bits = int(parts[4], 16)
+            except ValueError:
+                continue
+            for bit, name in _REASON_BITS.items():
+                if bits & bit and name != "gpu_idle":
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm), "power_w_max": max(pw)}
+
+
+# ---------------------------------------------------------------------------
+# CPU side: the fp64 oracle (cpu_baseline and the reference arm).
+# ---------------------------------------------------------------------------
+
+def _oracle_sample(problem, n_tokens):
+    """The first n_tokens of every sequence (all heads) as a standalone problem."""
+    import numpy as np
+    cu = problem.cu_seqlens
+    lens = np.minimum(problem.seqlens.astype(np.int64), n_tokens)
+    ks = [problem.k[cu[b]:cu[b] + lens[b]] for b in range(problem.B)]
+    vs = [problem.v[cu[b]:cu[b] + lens[b]] for b in range(problem.B)]
+    k = np.concatenate(ks) if ks else problem.k[:0]
+    v = np.concatenate(vs) if vs else problem.v[:0]
+    return lens, k, v, int(lens.sum()) * problem.Hkv * problem.d * 2 * 2
+
+
+def time_oracle_step(problem, n_tokens):
+    import oracle
+    lens, k, v, nbytes = _oracle_sample(problem, n_tokens)
+    t = time.perf_counter()
+    oracle.decode_reference(problem.q, k, v, lens, problem.dtype)
+    return time.perf_counter() - t, nbytes
+
+
+def cpu_baseline_only(args):
+    """Runs in a 1-thread subprocess: the oracle on a bounded sample for ~cpu_seconds."""
+    prob = make_problem(args)
+    n = int(prob.seqlens.max())
+    # Calibrate on a small prefix, then size the sample to ~cpu_seconds / 3 per call.
+    dt, nb = time_oracle_step(prob, min(n, 2048))
+    per_byte = dt / max(nb, 1)
+    full_bytes = prob.kv_bytes
+    target = args.cpu_seconds / 3.0
+    n_tok = n if per_byte * full_bytes <= target else max(256, int(n * target / (per_byte * full_bytes)))
+    total_t, total_b, calls = 0.0, 0, 0
+    while total_t < args.cpu_seconds and calls < 1000:
+        dt, nb = time_oracle_step(prob, n_tok)
+        total_t += dt
+        total_b += nb
+        calls += 1
+    frac = "all" if n_tok >= n else f"first {n_tok}"
+    return {"value": total_b / total_t / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"{calls} x fp64 oracle decode of {prob.name} ({frac} tokens of every "
+                      f"sequence, all heads), {total_t:.1f} s, 1 thread"}
+
+
+def run_cpu_baseline_subprocess(args):
+    env = dict(os.environ, **_ONE_THREAD)
+    cmd = [sys.executable, os.path.abspath(__file__), "--cpu-baseline-only", "--workload",
+           args.workload, "--W", str(args.W), "--cpu-seconds", str(args.cpu_seconds)]
+    res = subprocess.run(cmd, env=env, capture_output=True, text=True, timeout=600)
+    if res.returncode != 0:
+        return {"value": None, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                "sample": "failed: " + res.stderr.strip().splitlines()[-1] if res.stderr else "failed"}
+    return json.loads(res.stdout.strip().splitlines()[-1])
+
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    prob = make_problem(args)
+    n = int(prob.seqlens.max())
+    steps, warm = max(1, args.steps), max(0, args.warmup)
+    dt, nb = time_oracle_step(prob, min(n, 2048))
+    per_byte = dt / max(nb, 1)
+    per_step = args.ref_budget_s / (steps + warm)
+    n_tok = n if per_byte * prob.kv_bytes <= per_step else max(
+        32, int(n * per_step / (per_byte * prob.kv_bytes)))
+    for _ in range(warm):
+        time_oracle_step(prob, n_tok)
+    total_t, total_b = 0.0, 0
+    for _ in range(steps):
+        dt, nb = time_oracle_step(prob, n_tok)
+        total_t += dt
+        total_b += nb
+    value = total_b / total_t / 1e9
+    frac = "all" if n_tok >= n else f"first {n_tok}"
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s",
+        "n_gpus": args.gpus, "steps": steps, "warmup": warm,
+        "ms_per_step": total_t / steps * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded N(0,1))",
+        "config": {"workload": prob.name, **prob.describe()},
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": f"each step: fp64 oracle decode of {prob.name} ({frac} tokens "
+                                   f"of every sequence, all heads), 1 thread"},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ---------------------------------------------------------------------------
+# GPU arm.
+# ---------------------------------------------------------------------------
+
+def load_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def to_device(x, dtype, device):
+    import numpy as np
+    import torch
+    if dtype == "f16":
+        t = torch.from_numpy(np.ascontiguousarray(x))
+    else:
+        t = torch.from_numpy(np.ascontiguousarray(x).view(np.int16)).view(torch.bfloat16)
+    return t.to(device)
+
+
+def run_fd(args):
+    import torch
+
+    import split_kv_flash_decode_gb300 as fd
+    from split_kv_flash_decode_gb300 import build
+
+    rank, world, local = dist_env()
+    if world > 1:
+        torch.cuda.set_device(local)
+        dist_init(world, "nccl")
+    device = torch.device("cuda", torch.cuda.current_device())
+    build.build()
+    prob = make_problem(args)
+    props = torch.cuda.get_device_properties(device)
+    l2 = int(getattr(props, "L2_cache_size", 126 * 1024 * 1024))
+    kv_bytes = prob.kv_bytes
+    # Rotate K/V copies so consecutive steps never find their K/V in L2.
+    copies = 1 if kv_bytes == 0 else max(1, math.ceil(4 * l2 / kv_bytes))
+    copies = min(copies, max(1, int(40e9 // max(kv_bytes, 1))))
+
+    flags = (fd.FD_PLAN_LITERAL_W if prob.literal_w else 0) | (
+        fd.FD_PLAN_TWO_LAUNCH if args.two_launch else 0)
+    dec = fd.Decoder(prob.Hq, prob.Hkv, prob.d, prob.seqlens, prob.W, prob.dtype, flags=flags,
+                     chunks=args.chunks, device=device)
+    q = to_device(prob.q, prob.dtype, device)
+    k0 = to_device(prob.k, prob.dtype, device)
+    v0 = to_device(prob.v, prob.dtype, device)
+    ks = [k0] + [k0.clone() for _ in range(copies - 1)]
+    vs = [v0] + [v0.clone() for _ in range(copies - 1)]
+    out = torch.empty_like(q)
+    lse = torch.empty((prob.B, prob.Hq), dtype=torch.float32, device=device)
+    stream = torch.cuda.Stream(device)
+    launches_per_step = 2 if args.two_launch else 1
+
+    def step(i):
+        fd.fd_decode(dec.plan, q, ks[i % copies], vs[i % copies], out, lse, dec.workspace, stream)
+
+    K, Wm = max(1, args.steps), max(3, args.warmup)
+    with torch.cuda.stream(stream):
+        for i in range(Wm):
+            step(i)
+    stream.synchronize()
+
+    # Timed region: exactly K steps with an event pair around every launch.
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    ev_all = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+    graph = None
+    if not args.no_graph:
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            ev_all[0].record(stream)
+            for i in range(K):
+                ev[i][0].record(stream)
+                step(i)
+                ev[i][1].record(stream)
+            ev_all[1].record(stream)
+        stream.synchronize()
+
+    def timed_once():
+        if graph is not None:
+            graph.replay()
+        else:
+            with torch.cuda.stream(stream):
+                ev_all[0].record(stream)
+                for i in range(K):
+                    ev[i][0].record(stream)
+                    step(i)
+                    ev[i][1].record(stream)
+                ev_all[1].record(stream)
+
+    gpu_id = getattr(props, "uuid", None)
+    gpu_id = f"GPU-{gpu_id}" if gpu_id is not None and not str(gpu_id).startswith("GPU-") else str(gpu_id or local)
+    sampler = ClockSampler(gpu_id).start()
+    t_soak = time.time()
+    # Soak: the same replay, untimed, so clocks settle and the sampler sees the load.
+    while time.time() - t_soak < args.soak_s:
+        timed_once()
+        stream.synchronize()
+    barrier(world)
+    torch.cuda.synchronize(device)
+    t_start = time.time()
+    timed_once()
+    stream.synchronize()
+    torch.cuda.synchronize(device)
+    t_end = time.time()
+    barrier(world)
+    sampler.stop()
+    clocks = sampler.summary(t_soak, t_end)
+    if dec.status() != fd.FD_OK:
+        raise RuntimeError("device status word reported an error during the timed region")
+
+    total_ms = ev_all[0].elapsed_time(ev_all[1])
+    per_launch = [a.elapsed_time(b) * 1e3 for a, b in ev]  # microseconds
+    agg = aggregate_throughput(kv_bytes * K / 1e9, total_ms / 1e3, world, device)
+    value = agg["throughput"]  # GB/s, whole job
+    mean_us = statistics.fmean(per_launch)
+    qs = sorted(per_launch)
+
+    def pct(p):
+        return qs[min(len(qs) - 1, max(0, int(round(p / 100 * (len(qs) - 1)))))]
+
+    peak, peak_kind = load_peak()
+    achieved = kv_bytes / (mean_us * 1e-6) / 1e9
+
+    # e2e through the public API with pinned host buffers.
+    e2e = e2e_measure(fd, dec, prob, device, args.e2e_steps, stream, kv_resident=False)
+    e2e_res = e2e_measure(fd, dec, prob, device, max(args.e2e_steps, 200), stream, kv_resident=True,
+                          dev_kv=(k0, v0))
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = run_cpu_baseline_subprocess(args)
+
+    if rank == 0:
+        info = dec.info
+        line = {
+            "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": K,
+            "warmup": Wm, "ms_per_step": agg["elapsed_s"] * 1e3 / K, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": prob.dtype,
+            "data": "synthetic (seeded N(0,1) per tensor)",
+            "config": {
+                "workload": prob.name, **prob.describe(), "accumulate": "f32",
+                "chunks_per_segment": info["chunks"], "ctas": info["ctas"],
+                "partials_per_sequence_max": info["max_partials"],
+                "kv_bytes_per_step": kv_bytes, "two_launch": bool(args.two_launch),
+                "l2_policy": f"K/V rotated over {copies} device copies ({copies * kv_bytes / 1e6:.0f} MB"
+                             f" >= 4 x L2 {l2 / 1e6:.0f} MB)" if copies > 1 else
+                             f"K/V {kv_bytes / 1e6:.0f} MB per step > 4 x L2 {l2 / 1e6:.0f} MB",
+                "launch": "CUDA graph replay of the K steps" if graph is not None else "eager",
+                "parallelism": f"replicas x{world}",
+            },
+            "latency_us": {"mean": mean_us, "median": statistics.median(per_launch),
+                           "p10": pct(10), "p90": pct(90), "min": qs[0], "max": qs[-1]},
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                         "frac": achieved / peak, "traffic": None,
+                         "peak_kind": f"{peak_kind} (hbm_gbs copy, burst)",
+                         "kernel": "fd_split_kernel (fused)" if not args.two_launch
+                         else "fd_split_kernel + fd_combine_kernel"},
+            "e2e": e2e, "e2e_resident_kv": e2e_res,
+            "gpu_launches": K * launches_per_step,
+            "clocks": clocks, "cpu_baseline": cpu,
+            "gpu": props.name,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+def e2e_measure(fd, dec, prob, device, steps, stream, kv_resident, dev_kv=None):
+    """KV GB/s through fd_decode with pinned host inputs copied in and results copied out."""
+    import numpy as np
+    import torch
+    def pinned(x):
+        if prob.dtype == "f16":
+            t = torch.from_numpy(np.ascontiguousarray(x))
+        else:
+            t = torch.from_numpy(np.ascontiguousarray(x).view(np.int16)).view(torch.bfloat16)
+        return t.pin_memory()
+    hq = pinned(prob.q)
+    dq = torch.empty(hq.shape, dtype=hq.dtype, device=device)
+    if kv_resident:
+        dk, dv = dev_kv
+    else:
+        hk, hv = pinned(prob.k), pinned(prob.v)
+        dk = torch.empty(hk.shape, dtype=hk.dtype, device=device)
+        dv = torch.empty(hv.shape, dtype=hv.dtype, device=device)
+    dout = torch.empty_like(dq)
+    dlse = torch.empty((prob.B, prob.Hq), dtype=torch.float32, device=device)
+    hout = torch.empty(dout.shape, dtype=dout.dtype).pin_memory()
+    hlse = torch.empty(dlse.shape, dtype=dlse.dtype).pin_memory()
+    h2d = hq.numel() * 2 + (0 if kv_resident else 2 * prob.k.size * 2)
+    d2h = hout.numel() * 2 + hlse.numel() * 4
+
+    def one():
+        dq.copy_(hq, non_blocking=True)
+        if not kv_resident:
+            dk.copy_(hk, non_blocking=True)
+            dv.copy_(hv, non_blocking=True)
+        fd.fd_decode(dec.plan, dq, dk, dv, dout, dlse, dec.workspace, stream)
+        hout.copy_(dout, non_blocking=True)
+        hlse.copy_(dlse, non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            one()
+        stream.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(steps):
+            one()
+        e1.record(stream)
+        stream.synchronize()
+    ms = e0.elapsed_time(e1) / steps
+    return {"value": prob.kv_bytes / (ms * 1e-3) / 1e9, "unit": "GB/s", "ms_per_step": ms,
+            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "steps": steps,
+            "what": ("q copied in, K/V resident in HBM" if kv_resident else
+                     "q, K, V copied in from pinned host memory") + ", out + lse copied back"}
+
+
+_ONE_THREAD = {"OPENBLAS_NUM_THREADS": "1", "OMP_NUM_THREADS": "1", "MKL_NUM_THREADS": "1",
+               "NUMEXPR_NUM_THREADS": "1"}
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    if args.cpu_baseline_only or args.impl == "reference":
+        # The oracle legs report cores = 1: pin BLAS to one thread before numpy loads.
+        os.environ.update(_ONE_THREAD)
+    if args.cpu_baseline_only:
+        print(json.dumps(cpu_baseline_only(args)), flush=True)
+        return 0
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_fd(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,165 @@
+/*
+ * fd.h -- C ABI of the GB300 split-KV Flash Decode library (libfd_gb300.so).
+ *
+ * The operation ("Eliminating Multi-GPU Performance Taxes", review page:
+ * notation table and core equations, "Flash Decode global reduction"):
+ * one query token per sequence attends over that sequence's KV cache, which
+ * is split into W segments; each segment yields a partial (O, m, l) and the
+ * partials are merged by OnlineSoftmaxCombine, whose associativity lets them
+ * be merged in any order (correctness check #5, Milakov & Gimelshein 2018).
+ * Here the W segments are splits of one GPU's KV cache.  fd_decode runs the
+ * whole path in ONE kernel launch: every CTA streams its K/V rows through a
+ * TMA/mbarrier shared-memory ring, computes its partial, publishes it, and the
+ * CTA that arrives last for a (sequence, KV head) combines all partials of
+ * that pair (the pages' "fully fused" variant, with a release/acquire arrival
+ * counter in place of the pages' remote inbox flags).
+ *
+ * Result, for sequence b, query head h, KV head g = h / (Hq / Hkv):
+ *   s_j = <q[b,h,:], K[cu_b + j, g, :]> / sqrt(d),  j = 0 .. L_b - 1
+ *   out[b,h,:] = sum_j softmax(s)_j V[cu_b + j, g, :]     (stored in q's type)
+ *   lse[b,h]   = ln sum_j exp(s_j)                        (fp32, natural log)
+ * with fp32 accumulation.  L_b = 0 gives out = 0 and lse = -inf.
+ *
+ * Conventions for every entry point:
+ *   - Every call returns an int status (enum fd_status).  Nothing aborts and
+ *     nothing throws across the ABI.  fd_strerror() names a status.
+ *   - Device pointers belong to the calling thread's current CUDA device.
+ *   - Calls that take a stream are asynchronous with respect to the host unless
+ *     stated otherwise; a launch error is reported as FD_ERR_CUDA.
+ */
+#ifndef FD_GB300_FD_H_
+#define FD_GB300_FD_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#include <cuda_runtime_api.h> /* cudaStream_t */
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Opaque, immutable plan.  Owns host memory only.  A plan may be shared by
+ * threads; one workspace serves one in-flight decode at a time. */
+typedef struct fd_plan_s* fd_plan_t;
+
+enum fd_dtype {
+  FD_F16 = 0,  /* IEEE binary16 q, K, V and out */
+  FD_BF16 = 1  /* bfloat16 q, K, V and out */
+};
+
+enum fd_status {
+  FD_OK = 0,
+  FD_ERR_INVALID = -1,     /* bad argument (null pointer, negative size, Hq % Hkv != 0, ...) */
+  FD_ERR_UNSUPPORTED = -2, /* valid but outside the compiled support (d, G, batch, partial count) */
+  FD_ERR_ALIGN = -3,       /* a device pointer is not 16-byte aligned */
+  FD_ERR_CUDA = -4,        /* a CUDA runtime or driver call failed */
+  FD_ERR_NOMEM = -5,       /* host allocation failed */
+  FD_ERR_STATE = -6,       /* workspace counters not at rest (debug plans check this) */
+  FD_ERR_TIMEOUT = -7      /* a bounded in-kernel wait gave up (device status word) */
+};
+
+/* fd_plan flags */
+#define FD_PLAN_LITERAL_W 0x1u /* exactly W_b partials per sequence (chunks = 1) */
+#define FD_PLAN_DEBUG 0x2u     /* fd_decode checks counters/status (synchronises the stream) */
+#define FD_PLAN_TWO_LAUNCH 0x4u /* split kernel + separate combine kernel (ablation) */
+
+/* Compiled limits. */
+#define FD_MAX_BATCH 256       /* sequences per plan */
+#define FD_MAX_PARTIALS 1024   /* W_b * chunks per sequence */
+
+/*
+ * fd_plan -- validate a decode shape and build its work decomposition (host only;
+ * no CUDA call unless num_sms == 0).
+ *
+ *   B        number of sequences, 1 .. FD_MAX_BATCH
+ *   Hq, Hkv  query / KV heads; Hq % Hkv == 0; G = Hq / Hkv in {1, 2, 4, 8}
+ *   d        head dimension, 64 or 128
+ *   seqlens  host array [B], L_b >= 0; sum_b L_b < 2^31.  Sequence b occupies
+ *            KV rows [cu_b, cu_b + L_b) with cu_b = L_0 + ... + L_{b-1}.
+ *   W        host array [B], W_b >= 1 segments for sequence b.  Segment w is
+ *            [w*S_b, min((w+1)*S_b, L_b)) with S_b = ceil(L_b / W_b); trailing
+ *            segments may be empty (the pages shard the KV cache W ways; this
+ *            split rule is the plan's reading).
+ *   dtype    enum fd_dtype
+ *   flags    FD_PLAN_* bits
+ *   chunks   chunks per segment C >= 1 (each segment is cut into C equal
+ *            pieces, so W_b * C partials are combined); 0 = choose from the
+ *            SM count.  Ignored (C = 1) with FD_PLAN_LITERAL_W.
+ *   num_sms  SM count used to choose C; 0 = query the current device
+ *            (FD_ERR_CUDA if there is none).
+ *   out_plan receives the plan; release it with fd_plan_destroy.
+ *
+ * The plan copies seqlens and W; the caller keeps ownership of its arrays.
+ */
+int fd_plan(int B, int Hq, int Hkv, int d, const int32_t* seqlens, const int32_t* W,
+            int dtype, uint32_t flags, int chunks, int num_sms, fd_plan_t* out_plan);
+
+/* Release a plan (NULL is accepted).  No CUDA call. */
+int fd_plan_destroy(fd_plan_t plan);
+
+/* Bytes of device workspace fd_decode needs for this plan: the fp32 partials
+ * O [P, d], m [P], l [P] (P = Hq * sum_b W_b * C), one uint32 arrival counter per
+ * (sequence, KV head) and a status word.  0 for a NULL plan. */
+size_t fd_workspace_bytes(fd_plan_t plan);
+
+/* Zero the workspace's counters and status word on `stream` (asynchronous).
+ * A workspace must be zeroed once before its first fd_decode (torch.zeros or
+ * this call); fd_decode leaves every counter at zero when it completes. */
+int fd_workspace_init(fd_plan_t plan, void* workspace, cudaStream_t stream);
+
+/*
+ * fd_decode -- the fused split-KV Flash Decode (one kernel launch on `stream`).
+ *
+ *   q          device [B, Hq, d] (dtype), contiguous
+ *   k, v       device [N, Hkv, d] (dtype), contiguous, N = sum_b L_b
+ *   out        device [B, Hq, d] (dtype), written
+ *   lse        device [B, Hq] float, written (natural log); may be NULL
+ *   workspace  device, fd_workspace_bytes(plan) bytes, zeroed once beforehand
+ *   stream     CUDA stream (0 = legacy default stream)
+ *
+ * All device pointers must be 16-byte aligned (FD_ERR_ALIGN otherwise).  The
+ * caller owns every buffer and the stream.  Asynchronous: returns after the
+ * launch; with FD_PLAN_DEBUG it synchronises and reports FD_ERR_TIMEOUT or
+ * FD_ERR_STATE from the device status word.  Decodes that share a workspace
+ * must not overlap in time.
+ */
+int fd_decode(fd_plan_t plan, const void* q, const void* k, const void* v, void* out,
+              float* lse, void* workspace, cudaStream_t stream);
+
+/* Synchronise `stream` and read the device status word (0 = no error; else a
+ * negative fd_status) into *status.  Then clear the word. */
+int fd_workspace_status(fd_plan_t plan, void* workspace, cudaStream_t stream,
+                        int32_t* status);
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char* fd_strerror(int status);
+
+/* Plan introspection (host only). */
+typedef struct fd_plan_info {
+  int32_t B, Hq, Hkv, d, G, dtype;
+  uint32_t flags;
+  int32_t chunks;          /* C actually used */
+  int32_t num_sms;         /* SM count the plan was sized for */
+  int32_t ctas;            /* CTAs fd_decode launches = Hkv * sum_b W_b * C */
+  int32_t max_partials;    /* max_b W_b * C */
+  int64_t total_tokens;    /* N */
+  int64_t total_partials;  /* P */
+  uint64_t workspace_bytes;
+  uint64_t kv_bytes;       /* bytes of K and V one decode reads */
+} fd_plan_info;
+
+int fd_plan_get_info(fd_plan_t plan, fd_plan_info* info);
+
+/* Token range [*begin, *end) (relative to the start of sequence b) covered by
+ * partial `slot` (0 <= slot < W_b * C) of sequence b. */
+int fd_plan_get_range(fd_plan_t plan, int b, int slot, int32_t* begin, int32_t* end);
+
+/* Library version, e.g. 0x000100 for 0.1.0. */
+int fd_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FD_GB300_FD_H_ */

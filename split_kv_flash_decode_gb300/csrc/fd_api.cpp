@@ -1,0 +1,303 @@
+// Host side of the C ABI declared in include/fd.h: argument validation, the
+// work decomposition (segments -> chunks -> CTAs), workspace layout, TMA
+// tensor-map encoding and kernel launch.  See fd.h for the contract.
+#include <algorithm>
+#include <cmath>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+#include <new>
+#include <vector>
+
+#include <cudaTypedefs.h>  // PFN_cuTensorMapEncodeTiled
+
+#include "fd_common.h"
+
+namespace {
+
+constexpr int kVersion = 0x000100;
+constexpr size_t kAlign = 256;
+constexpr int kMinChunkTokens = 256;  // auto chunking never cuts segments below this
+constexpr int kCtasPerSm = 2;         // resident CTAs per SM (launch bounds + shared memory)
+
+size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
+
+}  // namespace
+
+struct fd_plan_s {
+  int B, Hq, Hkv, d, G, dtype;
+  uint32_t flags;
+  int C;
+  int num_sms;
+  int max_partials;
+  int64_t n_tokens;
+  int64_t total_partials;
+  int ctas;
+  size_t off_counters, off_m, off_l, off_o, ws_bytes;
+  fd::Params params;  // pointers filled per call; arrays and scalars filled here
+};
+
+namespace {
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  });
+  return fn;
+}
+
+// 3-D view (d, Hkv, N) of a [N, Hkv, d] tensor; one box = kTile rows of one head.
+int encode_kv_map(CUtensorMap* map, const void* base, const fd_plan_s* pl) {
+  auto enc = tensor_map_encoder();
+  if (!enc) return FD_ERR_CUDA;
+  const cuuint64_t dims[3] = {(cuuint64_t)pl->d, (cuuint64_t)pl->Hkv, (cuuint64_t)pl->n_tokens};
+  const cuuint64_t strides[2] = {(cuuint64_t)pl->d * 2, (cuuint64_t)pl->Hkv * pl->d * 2};
+  const cuuint32_t box[3] = {(cuuint32_t)pl->d, 1u, (cuuint32_t)fd::kTile};
+  const cuuint32_t estr[3] = {1u, 1u, 1u};
+  const CUtensorMapDataType ty =
+      pl->dtype == FD_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  CUresult r = enc(map, ty, 3, const_cast<void*>(base), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? FD_OK : FD_ERR_CUDA;
+}
+
+cudaError_t launch(const fd::Params& p, int dtype, int d, int G, int mode, int grid,
+                   cudaStream_t s) {
+  return dtype == FD_F16 ? fd::launch_f16(p, d, G, mode, grid, s)
+                         : fd::launch_bf16(p, d, G, mode, grid, s);
+}
+
+}  // namespace
+
+extern "C" {
+
+int fd_version(void) { return kVersion; }
+
+const char* fd_strerror(int status) {
+  switch (status) {
+    case FD_OK: return "FD_OK";
+    case FD_ERR_INVALID: return "FD_ERR_INVALID: invalid argument";
+    case FD_ERR_UNSUPPORTED: return "FD_ERR_UNSUPPORTED: shape or option outside compiled support";
+    case FD_ERR_ALIGN: return "FD_ERR_ALIGN: device pointer not 16-byte aligned";
+    case FD_ERR_CUDA: return "FD_ERR_CUDA: CUDA call failed";
+    case FD_ERR_NOMEM: return "FD_ERR_NOMEM: host allocation failed";
+    case FD_ERR_STATE: return "FD_ERR_STATE: workspace counters not at rest";
+    case FD_ERR_TIMEOUT: return "FD_ERR_TIMEOUT: bounded in-kernel wait gave up";
+    default: return "unknown fd status";
+  }
+}
+
+int fd_plan(int B, int Hq, int Hkv, int d, const int32_t* seqlens, const int32_t* W, int dtype,
+            uint32_t flags, int chunks, int num_sms, fd_plan_t* out_plan) {
+  if (!out_plan) return FD_ERR_INVALID;
+  *out_plan = nullptr;
+  if (!seqlens || !W) return FD_ERR_INVALID;
+  if (B < 1 || Hq < 1 || Hkv < 1 || d < 1 || chunks < 0 || num_sms < 0) return FD_ERR_INVALID;
+  if (Hq % Hkv != 0) return FD_ERR_INVALID;
+  if (dtype != FD_F16 && dtype != FD_BF16) return FD_ERR_INVALID;
+  if (flags & ~(FD_PLAN_LITERAL_W | FD_PLAN_DEBUG | FD_PLAN_TWO_LAUNCH)) return FD_ERR_INVALID;
+  const int G = Hq / Hkv;
+  if (B > FD_MAX_BATCH) return FD_ERR_UNSUPPORTED;
+  if (d != 64 && d != 128) return FD_ERR_UNSUPPORTED;
+  if (G != 1 && G != 2 && G != 4 && G != 8) return FD_ERR_UNSUPPORTED;
+
+  int64_t n_tokens = 0, sum_w = 0;
+  int max_w = 0;
+  for (int b = 0; b < B; ++b) {
+    if (seqlens[b] < 0 || W[b] < 1) return FD_ERR_INVALID;
+    if (W[b] > FD_MAX_PARTIALS) return FD_ERR_UNSUPPORTED;
+    n_tokens += seqlens[b];
+    sum_w += W[b];
+    max_w = std::max(max_w, (int)W[b]);
+  }
+  if (n_tokens >= (int64_t)1 << 31) return FD_ERR_UNSUPPORTED;
+
+  if (num_sms == 0) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+      cudaGetLastError();
+      return FD_ERR_CUDA;
+    }
+  }
+
+  int C = 1;
+  if (flags & FD_PLAN_LITERAL_W) {
+    C = 1;
+  } else if (chunks > 0) {
+    C = chunks;
+  } else {
+    // Fill the resident CTA slots in one wave without cutting segments too short.
+    const int64_t units = (int64_t)Hkv * sum_w;
+    const int64_t slots = (int64_t)num_sms * kCtasPerSm;
+    int64_t c = std::max<int64_t>(1, slots / units);
+    const int64_t avg_seg = sum_w > 0 ? n_tokens / sum_w : 0;
+    c = std::min<int64_t>(c, std::max<int64_t>(1, avg_seg / kMinChunkTokens));
+    C = (int)c;
+  }
+  if ((int64_t)max_w * C > FD_MAX_PARTIALS) return FD_ERR_UNSUPPORTED;
+  const int64_t ctas = (int64_t)Hkv * sum_w * C;
+  if (ctas >= (int64_t)1 << 31) return FD_ERR_UNSUPPORTED;
+
+  fd_plan_s* pl = new (std::nothrow) fd_plan_s();
+  if (!pl) return FD_ERR_NOMEM;
+  pl->B = B; pl->Hq = Hq; pl->Hkv = Hkv; pl->d = d; pl->G = G; pl->dtype = dtype;
+  pl->flags = flags; pl->C = C; pl->num_sms = num_sms;
+  pl->max_partials = max_w * C;
+  pl->n_tokens = n_tokens;
+  pl->total_partials = (int64_t)Hq * sum_w * C;
+  pl->ctas = (int)ctas;
+
+  fd::Params& p = pl->params;
+  std::memset(&p, 0, sizeof(p));
+  p.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)d));
+  p.B = B; p.Hq = Hq; p.Hkv = Hkv; p.C = C;
+  int32_t cu = 0, ub = 0;
+  for (int b = 0; b < B; ++b) {
+    p.cu[b] = cu;
+    p.unit_base[b] = ub;
+    p.wseg[b] = (uint16_t)W[b];
+    cu += seqlens[b];
+    ub += Hkv * W[b] * C;
+  }
+  p.cu[B] = cu;
+  p.unit_base[B] = ub;
+
+  // Workspace: status | counters | m | l | O (each 256-byte aligned).
+  size_t off = kAlign;
+  pl->off_counters = off;
+  off = align_up(off + sizeof(uint32_t) * (size_t)B * Hkv);
+  pl->off_m = off;
+  off = align_up(off + sizeof(float) * (size_t)pl->total_partials);
+  pl->off_l = off;
+  off = align_up(off + sizeof(float) * (size_t)pl->total_partials);
+  pl->off_o = off;
+  off = align_up(off + sizeof(float) * (size_t)pl->total_partials * d);
+  pl->ws_bytes = off;
+
+  *out_plan = pl;
+  return FD_OK;
+}
+
+int fd_plan_destroy(fd_plan_t plan) {
+  delete plan;
+  return FD_OK;
+}
+
+size_t fd_workspace_bytes(fd_plan_t plan) { return plan ? plan->ws_bytes : 0; }
+
+int fd_plan_get_info(fd_plan_t pl, fd_plan_info* info) {
+  if (!pl || !info) return FD_ERR_INVALID;
+  info->B = pl->B; info->Hq = pl->Hq; info->Hkv = pl->Hkv; info->d = pl->d; info->G = pl->G;
+  info->dtype = pl->dtype; info->flags = pl->flags; info->chunks = pl->C;
+  info->num_sms = pl->num_sms; info->ctas = pl->ctas; info->max_partials = pl->max_partials;
+  info->total_tokens = pl->n_tokens; info->total_partials = pl->total_partials;
+  info->workspace_bytes = pl->ws_bytes;
+  info->kv_bytes = (uint64_t)pl->n_tokens * pl->Hkv * pl->d * 2 * 2;
+  return FD_OK;
+}
+
+int fd_plan_get_range(fd_plan_t pl, int b, int slot, int32_t* begin, int32_t* end) {
+  if (!pl || !begin || !end || b < 0 || b >= pl->B) return FD_ERR_INVALID;
+  const int wtot = pl->params.wseg[b] * pl->C;
+  if (slot < 0 || slot >= wtot) return FD_ERR_INVALID;
+  const int L = pl->params.cu[b + 1] - pl->params.cu[b];
+  int t0, t1;
+  fd::chunk_range(L, pl->params.wseg[b], pl->C, slot, &t0, &t1);
+  *begin = t0;
+  *end = t1;
+  return FD_OK;
+}
+
+int fd_workspace_init(fd_plan_t pl, void* workspace, cudaStream_t stream) {
+  if (!pl || !workspace) return FD_ERR_INVALID;
+  if (cudaMemsetAsync(workspace, 0, pl->off_m, stream) != cudaSuccess) {
+    cudaGetLastError();
+    return FD_ERR_CUDA;
+  }
+  return FD_OK;
+}
+
+int fd_workspace_status(fd_plan_t pl, void* workspace, cudaStream_t stream, int32_t* status) {
+  if (!pl || !workspace || !status) return FD_ERR_INVALID;
+  uint32_t word = 0;
+  if (cudaStreamSynchronize(stream) != cudaSuccess ||
+      cudaMemcpy(&word, workspace, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess ||
+      cudaMemset(workspace, 0, sizeof(word)) != cudaSuccess) {
+    cudaGetLastError();
+    return FD_ERR_CUDA;
+  }
+  *status = word == 0 ? FD_OK
+          : (word & fd::kStatusTimeout) ? FD_ERR_TIMEOUT
+                                        : FD_ERR_STATE;
+  return FD_OK;
+}
+
+int fd_decode(fd_plan_t pl, const void* q, const void* k, const void* v, void* out, float* lse,
+              void* workspace, cudaStream_t stream) {
+  if (!pl || !q || !out || !workspace) return FD_ERR_INVALID;
+  if (pl->n_tokens > 0 && (!k || !v)) return FD_ERR_INVALID;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(lse) ||
+      !aligned16(workspace))
+    return FD_ERR_ALIGN;
+
+  fd::Params p = pl->params;  // per-call copy: the plan stays immutable
+  if (pl->n_tokens > 0) {
+    int rc = encode_kv_map(&p.tm_k, k, pl);
+    if (rc == FD_OK) rc = encode_kv_map(&p.tm_v, v, pl);
+    if (rc != FD_OK) return rc;
+  }
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  p.q = q;
+  p.out = out;
+  p.lse = lse;
+  p.status = reinterpret_cast<uint32_t*>(ws);
+  p.counters = reinterpret_cast<uint32_t*>(ws + pl->off_counters);
+  p.part_m = reinterpret_cast<float*>(ws + pl->off_m);
+  p.part_l = reinterpret_cast<float*>(ws + pl->off_l);
+  p.part_o = reinterpret_cast<float*>(ws + pl->off_o);
+
+  const bool debug = (pl->flags & FD_PLAN_DEBUG) != 0;
+  if (debug) {
+    std::vector<uint32_t> cnt((size_t)pl->B * pl->Hkv + 1);
+    if (cudaStreamSynchronize(stream) != cudaSuccess ||
+        cudaMemcpy(cnt.data(), p.counters, sizeof(uint32_t) * (cnt.size() - 1),
+                   cudaMemcpyDeviceToHost) != cudaSuccess) {
+      cudaGetLastError();
+      return FD_ERR_CUDA;
+    }
+    for (size_t i = 0; i + 1 < cnt.size(); ++i)
+      if (cnt[i] != 0) return FD_ERR_STATE;
+  }
+
+  cudaError_t err;
+  if (pl->flags & FD_PLAN_TWO_LAUNCH) {
+    err = launch(p, pl->dtype, pl->d, pl->G, 1, pl->ctas, stream);
+    if (err == cudaSuccess) err = launch(p, pl->dtype, pl->d, pl->G, 2, pl->B * pl->Hkv, stream);
+  } else {
+    err = launch(p, pl->dtype, pl->d, pl->G, 0, pl->ctas, stream);
+  }
+  if (err != cudaSuccess) {
+    cudaGetLastError();
+    return FD_ERR_CUDA;
+  }
+  if (debug) {
+    int32_t st = FD_OK;
+    int rc = fd_workspace_status(pl, workspace, stream, &st);
+    if (rc != FD_OK) return rc;
+    if (st != FD_OK) return st;
+  }
+  return FD_OK;
+}
+
+}  // extern "C"

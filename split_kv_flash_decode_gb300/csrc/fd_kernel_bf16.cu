@@ -1,0 +1,8 @@
+// bf16 instantiations of the split-KV Flash Decode kernels.
+#include "fd_kernel.cuh"
+
+namespace fd {
+cudaError_t launch_bf16(const Params& p, int d, int G, int mode, int grid, cudaStream_t s) {
+  return launch_typed<__nv_bfloat16>(p, d, G, mode, grid, s);
+}
+}  // namespace fd

@@ -1,0 +1,8 @@
+// fp16 instantiations of the split-KV Flash Decode kernels.
+#include "fd_kernel.cuh"
+
+namespace fd {
+cudaError_t launch_f16(const Params& p, int d, int G, int mode, int grid, cudaStream_t s) {
+  return launch_typed<__half>(p, d, G, mode, grid, s);
+}
+}  // namespace fd

@@ -1,0 +1,73 @@
+"""Convenience layer over the C ABI: a Decoder owns a plan and its workspace.
+
+Shapes and dtypes are checked here (the C ABI sees only pointers); every byte
+of compute happens in fd_decode's kernel.
+"""
+from __future__ import annotations
+
+import torch
+
+from . import _binding as B
+
+_TORCH_DTYPE = {"f16": torch.float16, "bf16": torch.bfloat16}
+
+
+class Decoder:
+    """Plan + zeroed workspace for one decode shape on one device."""
+
+    def __init__(self, Hq, Hkv, d, seqlens, W, dtype="f16", flags=0, chunks=0, device=None,
+                 num_sms=0):
+        self.device = torch.device(device if device is not None else "cuda")
+        if self.device.type != "cuda":
+            raise ValueError("Decoder needs a CUDA device")
+        self.seqlens = [int(x) for x in seqlens]
+        self.Bsz = len(self.seqlens)
+        self.Hq, self.Hkv, self.d, self.dtype = int(Hq), int(Hkv), int(d), dtype
+        self.n_tokens = sum(self.seqlens)
+        with torch.cuda.device(self.device):
+            self.plan = B.fd_plan(self.Bsz, Hq, Hkv, d, self.seqlens, W, dtype, flags, chunks,
+                                  num_sms)
+            self.workspace = torch.zeros(max(1, self.plan.workspace_bytes), dtype=torch.uint8,
+                                         device=self.device)
+
+    @property
+    def info(self) -> dict:
+        return self.plan.info
+
+    def _check(self, name, t, shape):
+        if t.device != self.device:
+            raise ValueError(f"{name} is on {t.device}, expected {self.device}")
+        if t.dtype != _TORCH_DTYPE[self.dtype]:
+            raise ValueError(f"{name} has dtype {t.dtype}, expected {_TORCH_DTYPE[self.dtype]}")
+        if tuple(t.shape) != tuple(shape):
+            raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+
+    def __call__(self, q, k, v, out=None, lse=None, stream=None):
+        self._check("q", q, (self.Bsz, self.Hq, self.d))
+        self._check("k", k, (self.n_tokens, self.Hkv, self.d))
+        self._check("v", v, (self.n_tokens, self.Hkv, self.d))
+        if out is None:
+            out = torch.empty_like(q)
+        else:
+            self._check("out", out, (self.Bsz, self.Hq, self.d))
+        if lse is None:
+            lse = torch.empty((self.Bsz, self.Hq), dtype=torch.float32, device=self.device)
+        elif lse.dtype != torch.float32 or tuple(lse.shape) != (self.Bsz, self.Hq):
+            raise ValueError("lse must be float32 [B, Hq]")
+        with torch.cuda.device(self.device):
+            B.fd_decode(self.plan, q, k, v, out, lse, self.workspace, stream)
+        return out, lse
+
+    def status(self, stream=None) -> int:
+        with torch.cuda.device(self.device):
+            return B.fd_workspace_status(self.plan, self.workspace, stream)
+
+
+def flash_decode(q, k, v, seqlens, W, flags=0, chunks=0):
+    """One-shot decode: plan, allocate, run.  Returns (out, lse)."""
+    dtype = {torch.float16: "f16", torch.bfloat16: "bf16"}[q.dtype]
+    dec = Decoder(q.shape[1], k.shape[1], q.shape[2], seqlens, W, dtype, flags, chunks,
+                  device=q.device)
+    return dec(q, k, v)

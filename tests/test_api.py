@@ -1,0 +1,162 @@
+"""Host-side tests of the C ABI (no GPU needed: no compute call is made).
+
+They check that the library loads and exports every entry point include/fd.h
+declares, that fd_plan validates its arguments with the documented status
+codes, and that the work decomposition tiles every sequence exactly: each
+chunk lies inside the segment of the oracle's segment rule, chunks are disjoint
+and cover [0, L_b).
+"""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+import oracle
+import split_kv_flash_decode_gb300 as fd
+from split_kv_flash_decode_gb300 import _binding, build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "fd.h")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built_lib():
+    build.build()
+    return fd.lib()
+
+
+def declared_entry_points():
+    with open(HEADER) as f:
+        text = f.read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(fd_[a-z_]+)\s*\(", text)))
+
+
+def test_header_declares_what_binding_exports():
+    decl = declared_entry_points()
+    assert decl == sorted(_binding.EXPORTED)
+
+
+def test_library_exports_every_declared_symbol():
+    so = ctypes.CDLL(_binding.LIB_PATH)
+    for name in declared_entry_points():
+        assert hasattr(so, name), name
+
+
+def test_version_and_strerror():
+    assert fd.fd_version() == 0x000100
+    for code in (fd.FD_OK, fd.FD_ERR_INVALID, fd.FD_ERR_UNSUPPORTED, fd.FD_ERR_ALIGN,
+                 fd.FD_ERR_CUDA, fd.FD_ERR_NOMEM, fd.FD_ERR_STATE, fd.FD_ERR_TIMEOUT):
+        s = fd.fd_strerror(code)
+        assert s.startswith("FD_")
+    assert "unknown" in fd.fd_strerror(12345)
+
+
+def _raw_plan(B, Hq, Hkv, d, seqlens, W, dtype=0, flags=0, chunks=0, num_sms=152):
+    L = fd.lib()
+    arr = (ctypes.c_int32 * max(1, len(seqlens)))(*seqlens)
+    warr = (ctypes.c_int32 * max(1, len(W)))(*W)
+    h = ctypes.c_void_p()
+    rc = L.fd_plan(B, Hq, Hkv, d, arr, warr, dtype, flags, chunks, num_sms, ctypes.byref(h))
+    if rc == 0:
+        L.fd_plan_destroy(h)
+    return rc
+
+
+@pytest.mark.parametrize("args,code", [
+    ((0, 8, 8, 128, [], []), fd.FD_ERR_INVALID),                      # B < 1
+    ((1, 8, 3, 128, [10], [1]), fd.FD_ERR_INVALID),                   # Hq % Hkv
+    ((1, 8, 8, 128, [-1], [1]), fd.FD_ERR_INVALID),                   # negative length
+    ((1, 8, 8, 128, [10], [0]), fd.FD_ERR_INVALID),                   # W < 1
+    ((1, 8, 8, 96, [10], [1]), fd.FD_ERR_UNSUPPORTED),                # d
+    ((1, 24, 8, 128, [10], [1]), fd.FD_ERR_UNSUPPORTED),              # G = 3
+    ((1, 128, 8, 128, [10], [1]), fd.FD_ERR_UNSUPPORTED),             # G = 16
+    ((257, 8, 8, 128, [1] * 257, [1] * 257), fd.FD_ERR_UNSUPPORTED),  # batch limit
+    ((1, 8, 8, 128, [10], [1025]), fd.FD_ERR_UNSUPPORTED),            # partial limit
+    ((1, 8, 8, 128, [10], [1]), fd.FD_OK),
+])
+def test_plan_validation(args, code):
+    assert _raw_plan(*args) == code
+
+
+def test_plan_bad_dtype_flags_chunks():
+    assert _raw_plan(1, 8, 8, 128, [10], [1], dtype=2) == fd.FD_ERR_INVALID
+    assert _raw_plan(1, 8, 8, 128, [10], [1], flags=0x80) == fd.FD_ERR_INVALID
+    assert _raw_plan(1, 8, 8, 128, [10], [1], chunks=-1) == fd.FD_ERR_INVALID
+    assert _raw_plan(1, 8, 8, 128, [10], [600], chunks=2) == fd.FD_ERR_UNSUPPORTED
+    L = fd.lib()
+    assert L.fd_plan(1, 8, 8, 128, None, None, 0, 0, 0, 152, None) == fd.FD_ERR_INVALID
+    assert L.fd_plan_destroy(None) == fd.FD_OK
+    assert L.fd_workspace_bytes(None) == 0
+
+
+def test_null_pointer_rejections():
+    p = fd.fd_plan(1, 8, 8, 64, [100], 4, "f16", num_sms=152)
+    L = fd.lib()
+    assert L.fd_decode(p.handle, None, None, None, None, None, None, None) == fd.FD_ERR_INVALID
+    # misaligned device pointers are rejected before any CUDA call
+    assert L.fd_decode(p.handle, 16, 16, 16, 16, 0, 8, None) == fd.FD_ERR_ALIGN
+    assert L.fd_decode(p.handle, 24, 16, 16, 16, 0, 16, None) == fd.FD_ERR_ALIGN
+    assert L.fd_workspace_init(p.handle, None, None) == fd.FD_ERR_INVALID
+    assert L.fd_plan_get_info(None, None) == fd.FD_ERR_INVALID
+    lo, hi = ctypes.c_int32(), ctypes.c_int32()
+    assert L.fd_plan_get_range(p.handle, 1, 0, ctypes.byref(lo), ctypes.byref(hi)) == fd.FD_ERR_INVALID
+    assert L.fd_plan_get_range(p.handle, 0, 4, ctypes.byref(lo), ctypes.byref(hi)) == fd.FD_ERR_INVALID
+
+
+def _check_tiling(plan, seqlens, W):
+    C = plan.info["chunks"]
+    for b, L in enumerate(seqlens):
+        segs = oracle.segment_bounds(int(L), int(W[b]))
+        pos = 0
+        for slot in range(int(W[b]) * C):
+            lo, hi = plan.range(b, slot)
+            s0, s1 = segs[slot // C]
+            assert s0 <= lo <= hi <= s1, (b, slot, lo, hi, s0, s1)
+            assert lo == pos, (b, slot)
+            pos = hi
+        assert pos == L
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_work_decomposition_tiles_sequences(seed):
+    rs = np.random.default_rng(seed)
+    B = int(rs.integers(1, 20))
+    seqlens = rs.integers(0, 5000, size=B)
+    seqlens[rs.integers(0, B)] = 0
+    W = rs.integers(1, 40, size=B)
+    for chunks in (0, 1, 3, 7):
+        p = fd.fd_plan(B, 16, 4, 128, seqlens, W, "f16", chunks=chunks, num_sms=152)
+        if chunks:
+            assert p.info["chunks"] == chunks
+        _check_tiling(p, seqlens, W)
+        info = p.info
+        assert info["ctas"] == 4 * int(W.sum()) * info["chunks"]
+        assert info["total_partials"] == 16 * int(W.sum()) * info["chunks"]
+        assert info["total_tokens"] == int(seqlens.sum())
+        assert info["kv_bytes"] == int(seqlens.sum()) * 4 * 128 * 4
+
+
+def test_literal_w_and_auto_chunks():
+    # literal W: exactly W partials per sequence
+    p = fd.fd_plan(64, 32, 8, 128, [8192] * 64, 16, "bf16", flags=fd.FD_PLAN_LITERAL_W,
+                   chunks=5, num_sms=152)
+    assert p.info["chunks"] == 1 and p.info["ctas"] == 64 * 8 * 16
+    # auto: one wave of two CTAs per SM, segments not cut below 256 tokens
+    p = fd.fd_plan(1, 32, 8, 128, [32768], 8, "f16", num_sms=152)
+    assert p.info["chunks"] == 4 and p.info["ctas"] == 256
+    p = fd.fd_plan(1, 8, 8, 64, [4096], 4, "f16", num_sms=152)
+    assert p.info["chunks"] == 4  # 1024-token segments -> 256-token chunks
+    p = fd.fd_plan(1, 8, 8, 64, [100], 4, "f16", num_sms=152)
+    assert p.info["chunks"] == 1
+
+
+def test_workspace_layout():
+    p = fd.fd_plan(3, 8, 2, 64, [10, 0, 700], [1, 2, 5], "f16", chunks=2, num_sms=152)
+    P = 8 * (1 + 2 + 5) * 2
+    assert p.info["total_partials"] == P
+    need = 4 * 3 * 2 + 4 * P * 2 + 4 * P * 64
+    assert p.workspace_bytes >= need
+    assert p.workspace_bytes % 256 == 0

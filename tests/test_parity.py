@@ -1,0 +1,199 @@
+"""GPU parity: the CUDA path (through the C ABI) against the fp64 oracle.
+
+Tolerances (fp16/bf16 inputs, fp32 accumulation): max |out - oracle| <= 2e-3
+and max |lse - oracle| <= 1e-4, element by element.  -inf lse (empty
+sequences) must match exactly and their outputs must be exactly zero.
+"""
+import numpy as np
+import pytest
+
+import oracle
+import workloads
+
+pytestmark = pytest.mark.gpu
+
+OUT_TOL = 2e-3
+LSE_TOL = 1e-4
+
+
+@pytest.fixture(scope="module")
+def fd():
+    import split_kv_flash_decode_gb300 as fd_mod
+    from split_kv_flash_decode_gb300 import build
+    build.build()
+    return fd_mod
+
+
+def to_torch(x, dtype, device="cuda"):
+    import torch
+    if dtype == "f16":
+        t = torch.from_numpy(np.ascontiguousarray(x))
+    else:
+        t = torch.from_numpy(np.ascontiguousarray(x).view(np.int16)).view(torch.bfloat16)
+    return t.to(device)
+
+
+def out_to_f64(t):
+    import torch
+    return t.to(torch.float64).cpu().numpy()
+
+
+def run_gpu(fd, p, chunks=0, flags=0, repeat=1):
+    dec = fd.Decoder(p.Hq, p.Hkv, p.d, p.seqlens, p.W, p.dtype,
+                     flags=flags | (fd.FD_PLAN_LITERAL_W if p.literal_w else 0), chunks=chunks)
+    q, k, v = (to_torch(x, p.dtype) for x in (p.q, p.k, p.v))
+    outs = []
+    for _ in range(repeat):
+        out, lse = dec(q, k, v)
+        outs.append((out_to_f64(out), lse.cpu().numpy().astype(np.float64)))
+    assert dec.status() == fd.FD_OK
+    ws = dec.workspace.cpu().numpy()
+    counters = ws[256:256 + 4 * p.B * p.Hkv].view(np.uint32)
+    assert not counters.any(), "arrival counters must be back at zero"
+    return outs if repeat > 1 else outs[0], dec
+
+
+def check(out, lse, ref_out, ref_lse, heads=None):
+    if heads is not None:
+        idx = tuple(np.array(heads).T)
+        out, lse, ref_out, ref_lse = out[idx], lse[idx], ref_out[idx], ref_lse[idx]
+    empty = np.isneginf(ref_lse)
+    assert np.array_equal(np.isneginf(lse), empty)
+    assert np.all(out[empty] == 0.0)
+    full = ~empty
+    err_o = np.abs(out[full] - ref_out[full]).max(initial=0.0)
+    err_l = np.abs(lse[full] - ref_lse[full]).max(initial=0.0)
+    assert err_o <= OUT_TOL, f"max |out err| {err_o:.3e}"
+    assert err_l <= LSE_TOL, f"max |lse err| {err_l:.3e}"
+    return err_o, err_l
+
+
+# ---------------------------------------------------------------------------
+# The five decode cases at full size.
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("name", ["mha8_d64_L4k_W4", "gqa4_d128_L32k_W8", "gqa8_d128_L128k_W8_spiky"])
+def test_case_full(fd, name):
+    p = workloads.CASES[name]()
+    (out, lse), _ = run_gpu(fd, p)
+    ref_out, ref_lse = oracle.decode_reference(p.q, p.k, p.v, p.seqlens, p.dtype)
+    check(out, lse, ref_out, ref_lse)
+
+
+def test_ragged16_full(fd):
+    p = workloads.ragged16_gqa4_d128()
+    (out, lse), _ = run_gpu(fd, p)
+    ref_out, ref_lse = oracle.decode_reference(p.q, p.k, p.v, p.seqlens, p.dtype)
+    check(out, lse, ref_out, ref_lse)
+
+
+def test_batch64_bf16_w_sweep_deterministic(fd):
+    p1 = workloads.batch64_gqa4_d128_L8k_bf16(W=1)
+    ref_out, ref_lse = oracle.decode_reference(p1.q, p1.k, p1.v, p1.seqlens, p1.dtype)
+    for W in workloads.W_SWEEP:
+        p = workloads.batch64_gqa4_d128_L8k_bf16(W=W)
+        runs, dec = run_gpu(fd, p, repeat=20 if W == 16 else 2)
+        assert dec.info["chunks"] == 1 and dec.info["ctas"] == 64 * 8 * W
+        out0, lse0 = runs[0]
+        for out, lse in runs[1:]:
+            assert np.array_equal(out, out0) and np.array_equal(lse, lse0), "not bitwise deterministic"
+        check(out0, lse0, ref_out, ref_lse)
+
+
+# ---------------------------------------------------------------------------
+# Edge shapes: tile boundaries, W beyond L, every G and d, both dtypes.
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("G", [1, 2, 4, 8])
+def test_edge_lengths(fd, dtype, d, G):
+    Hkv = 2
+    lens = [1, 2, 31, 32, 33, 63, 64, 65, 97, 1000]
+    W = [1, 3, 31, 1, 40, 2, 64, 70, 5, 7]
+    p = workloads.make_problem("edge", len(lens), Hkv * G, Hkv, d, lens, W, dtype, seed=7 + G + d)
+    ref_out, ref_lse = oracle.decode_reference(p.q, p.k, p.v, p.seqlens, p.dtype)
+    for chunks in (0, 1, 3):
+        (out, lse), _ = run_gpu(fd, p, chunks=chunks)
+        check(out, lse, ref_out, ref_lse)
+
+
+def test_ragged_with_empty_sequences(fd):
+    lens = [0, 700, 0, 1, 4096, 0]
+    p = workloads.make_problem("ragged_empty", 6, 16, 4, 128, lens, [1, 3, 5, 2, 4, 1], "f16", seed=11)
+    ref_out, ref_lse = oracle.decode_reference(p.q, p.k, p.v, p.seqlens, p.dtype)
+    for chunks in (0, 2):
+        (out, lse), _ = run_gpu(fd, p, chunks=chunks)
+        check(out, lse, ref_out, ref_lse)
+
+
+def test_all_sequences_empty(fd):
+    p = workloads.make_problem("all_empty", 3, 8, 8, 64, [0, 0, 0], 2, "bf16", seed=12)
+    (out, lse), _ = run_gpu(fd, p)
+    assert np.all(out == 0) and np.all(np.isneginf(lse))
+
+
+def test_chunk_counts_agree(fd):
+    p = workloads.make_problem("chunks", 2, 32, 8, 128, [5000, 3001], [3, 2], "f16", seed=13)
+    ref_out, ref_lse = oracle.decode_reference(p.q, p.k, p.v, p.seqlens, p.dtype)
+    for chunks in (1, 2, 5, 16, 100):
+        (out, lse), _ = run_gpu(fd, p, chunks=chunks)
+        check(out, lse, ref_out, ref_lse)
+
+
+def test_closed_forms_on_gpu(fd):
+    """Equal V rows return that row; q = 0 returns the mean of V with lse = ln L."""
+    rs = np.random.default_rng(14)
+    L, Hkv, G, d = 3000, 2, 4, 128
+    p = workloads.make_problem("closed", 1, Hkv * G, Hkv, d, [L], 4, "f16", seed=14)
+    row = rs.standard_normal((Hkv, d)).astype(np.float16)
+    p.v[:] = row[None]
+    (out, lse), _ = run_gpu(fd, p)
+    for h in range(Hkv * G):
+        assert np.abs(out[0, h] - row[h // G].astype(np.float64)).max() <= 1e-3
+    p.q[:] = 0
+    p.v[:] = rs.standard_normal(p.v.shape).astype(np.float16)
+    (out, lse), _ = run_gpu(fd, p)
+    mean = p.v.astype(np.float64).mean(axis=0)
+    for h in range(Hkv * G):
+        assert np.abs(out[0, h] - mean[h // G]).max() <= OUT_TOL
+    assert np.abs(lse - np.log(L)).max() <= LSE_TOL
+
+
+def test_two_launch_matches_fused(fd):
+    p = workloads.make_problem("two_launch", 3, 32, 8, 128, [9000, 17, 4096], [4, 2, 8], "bf16", seed=15)
+    ref_out, ref_lse = oracle.decode_reference(p.q, p.k, p.v, p.seqlens, p.dtype)
+    (o1, l1), _ = run_gpu(fd, p)
+    (o2, l2), _ = run_gpu(fd, p, flags=fd.FD_PLAN_TWO_LAUNCH)
+    check(o2, l2, ref_out, ref_lse)
+    assert np.array_equal(o1, o2) and np.array_equal(l1, l2)
+
+
+def test_debug_plan_detects_counter_state(fd):
+    import torch
+    p = workloads.make_problem("debug", 1, 8, 8, 64, [2048], 4, "f16", seed=16)
+    dec = fd.Decoder(p.Hq, p.Hkv, p.d, p.seqlens, p.W, p.dtype, flags=fd.FD_PLAN_DEBUG)
+    q, k, v = (to_torch(x, p.dtype) for x in (p.q, p.k, p.v))
+    dec(q, k, v)                                      # clean workspace: ok
+    dec.workspace[256:260] = torch.tensor([1, 0, 0, 0], dtype=torch.uint8, device="cuda")
+    with pytest.raises(fd.FdError) as ei:
+        dec(q, k, v)                                  # host check, nothing launched
+    assert ei.value.status == fd.FD_ERR_STATE
+    fd.fd_workspace_init(dec.plan, dec.workspace)
+    out, lse = dec(q, k, v)
+    ref_out, ref_lse = oracle.decode_reference(p.q, p.k, p.v, p.seqlens, p.dtype)
+    check(out_to_f64(out), lse.cpu().numpy().astype(np.float64), ref_out, ref_lse)
+
+
+def test_lse_optional_and_misaligned_rejected(fd):
+    import torch
+    p = workloads.make_problem("opt", 1, 8, 8, 64, [300], 2, "f16", seed=17)
+    dec = fd.Decoder(p.Hq, p.Hkv, p.d, p.seqlens, p.W, p.dtype)
+    q, k, v = (to_torch(x, p.dtype) for x in (p.q, p.k, p.v))
+    out = torch.empty_like(q)
+    fd.fd_decode(dec.plan, q, k, v, out, None, dec.workspace)
+    ref_out, _ = oracle.decode_reference(p.q, p.k, p.v, p.seqlens, p.dtype)
+    assert np.abs(out_to_f64(out) - ref_out).max() <= OUT_TOL
+    with pytest.raises(fd.FdError) as ei:
+        fd.fd_decode(dec.plan, q, k, v, out.view(-1)[1:].data_ptr(), None, dec.workspace)
+    assert ei.value.status == fd.FD_ERR_ALIGN
