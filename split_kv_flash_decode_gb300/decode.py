@@ -17,9 +17,11 @@ class Decoder:
 
     def __init__(self, Hq, Hkv, d, seqlens, W, dtype="f16", flags=0, chunks=0, device=None,
                  num_sms=0):
-        self.device = torch.device(device if device is not None else "cuda")
-        if self.device.type != "cuda":
+        dev = torch.device(device if device is not None else "cuda")
+        if dev.type != "cuda":
             raise ValueError("Decoder needs a CUDA device")
+        self.device = torch.device("cuda", dev.index if dev.index is not None
+                                   else torch.cuda.current_device())
         self.seqlens = [int(x) for x in seqlens]
         self.Bsz = len(self.seqlens)
         self.Hq, self.Hkv, self.d, self.dtype = int(Hq), int(Hkv), int(d), dtype
