@@ -335,11 +335,23 @@ def run_fd(args):
             step(i)
     stream.synchronize()
 
-    # Timed region: exactly K steps with an event pair around every launch.
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
-    ev_all = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+    # Timed region: exactly K steps with an event pair around every launch.  Inside a
+    # CUDA graph the events must be "external" so that they become timing records.
+    use_graph = not args.no_graph
+    try:
+        torch.cuda.Event(enable_timing=True, external=True)
+    except TypeError:
+        use_graph = False
+
+    def timing_event():
+        if use_graph:
+            return torch.cuda.Event(enable_timing=True, external=True)
+        return torch.cuda.Event(enable_timing=True)
+
+    ev = [(timing_event(), timing_event()) for _ in range(K)]
+    ev_all = (timing_event(), timing_event())
     graph = None
-    if not args.no_graph:
+    if use_graph:
         graph = torch.cuda.CUDAGraph()
         with torch.cuda.graph(graph, stream=stream):
             ev_all[0].record(stream)
