@@ -127,6 +127,39 @@ int fd_workspace_init(fd_plan_t plan, void* workspace, cudaStream_t stream);
 int fd_decode(fd_plan_t plan, const void* q, const void* k, const void* v, void* out,
               float* lse, void* workspace, cudaStream_t stream);
 
+/* Bytes of the static device scratch array behind fd_decode_noalloc (32 MiB). */
+#define FD_NOALLOC_SCRATCH_BYTES (32u << 20)
+
+/*
+ * fd_decode_noalloc -- fd_decode for callers that cannot allocate device memory.
+ * The paper has no counterpart to this entry point; it exists for deployment.
+ *
+ * Who needs it: code that runs inside an engine or framework owning the device
+ * allocator (a plugin enqueue that must not call cudaMalloc, a caching-allocator
+ * arena that must not fragment), or any call site where a device allocation
+ * would synchronise the device.  Such callers cannot provide fd_decode's
+ * workspace.  This call takes none: the counters, status word and fp32
+ * partials live in one file-scope __device__ array of FD_NOALLOC_SCRATCH_BYTES
+ * that every GPU loading the library holds until the process exits.  The call
+ * allocates nothing (no cudaMalloc, cudaFree or allocating library routine);
+ * the plan comes from fd_plan, which allocates host memory only.
+ *
+ *   plan, q, k, v, out, lse, stream   as for fd_decode (no workspace argument)
+ *
+ * Returns FD_ERR_UNSUPPORTED when fd_workspace_bytes(plan) exceeds
+ * FD_NOALLOC_SCRATCH_BYTES (the plan needs more scratch than the array holds).
+ * The first call on each device looks up the array's device address
+ * (cudaGetSymbolAddress, with that device current); make that first call
+ * before any stream capture.  Each call clears the array's counters and status
+ * word on `stream` before its launch; the array keeps the last call's
+ * partials.  Every call in the process shares the one array per device, so
+ * fd_decode_noalloc calls that overlap on the GPU (other streams, other
+ * threads) race and must be serialised by the caller.  FD_PLAN_DEBUG checks are
+ * not performed here.  Asynchronous, like fd_decode.
+ */
+int fd_decode_noalloc(fd_plan_t plan, const void* q, const void* k, const void* v, void* out,
+                      float* lse, cudaStream_t stream);
+
 /* Synchronise `stream` and read the device status word (0 = no error; else a
  * negative fd_status) into *status.  Then clear the word. */
 int fd_workspace_status(fd_plan_t plan, void* workspace, cudaStream_t stream,

@@ -20,6 +20,7 @@ from ._binding import (  # noqa: F401
     FD_F16,
     FD_MAX_BATCH,
     FD_MAX_PARTIALS,
+    FD_NOALLOC_SCRATCH_BYTES,
     FD_OK,
     FD_PLAN_DEBUG,
     FD_PLAN_LITERAL_W,
@@ -27,6 +28,7 @@ from ._binding import (  # noqa: F401
     FdError,
     Plan,
     fd_decode,
+    fd_decode_noalloc,
     fd_plan,
     fd_plan_destroy,
     fd_plan_get_range,

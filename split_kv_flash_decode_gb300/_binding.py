@@ -36,7 +36,9 @@ DTYPES = {"f16": FD_F16, "bf16": FD_BF16}
 EXPORTED = (
     "fd_plan", "fd_plan_destroy", "fd_workspace_bytes", "fd_workspace_init", "fd_decode",
     "fd_workspace_status", "fd_strerror", "fd_plan_get_info", "fd_plan_get_range", "fd_version",
+    "fd_decode_noalloc",
 )
+FD_NOALLOC_SCRATCH_BYTES = 32 << 20
 
 
 class FdError(RuntimeError):
@@ -94,6 +96,8 @@ def lib() -> ctypes.CDLL:
             L.fd_plan_get_range.argtypes = [vp, ctypes.c_int, ctypes.c_int, ctypes.POINTER(i32),
                                             ctypes.POINTER(i32)]
             L.fd_plan_get_range.restype = ctypes.c_int
+            L.fd_decode_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp]
+            L.fd_decode_noalloc.restype = ctypes.c_int
             L.fd_version.argtypes = []
             L.fd_version.restype = ctypes.c_int
             _lib = L
@@ -194,6 +198,13 @@ def fd_decode(plan: Plan, q, k, v, out, lse, workspace, stream=None) -> None:
     """fd_decode: one fused launch on `stream` (default: torch's current stream)."""
     _check(lib().fd_decode(plan.handle, _ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse),
                            _ptr(workspace), _stream(stream)), "fd_decode")
+
+
+def fd_decode_noalloc(plan: Plan, q, k, v, out, lse, stream=None) -> None:
+    """fd_decode_noalloc: the fused decode with the library's static device scratch
+    (for callers that cannot allocate device memory; see include/fd.h)."""
+    _check(lib().fd_decode_noalloc(plan.handle, _ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse),
+                                   _stream(stream)), "fd_decode_noalloc")
 
 
 def fd_workspace_status(plan: Plan, workspace, stream=None) -> int:

@@ -11,7 +11,7 @@
 
 #include <cudaTypedefs.h>  // PFN_cuTensorMapEncodeTiled
 
-#include "fd_common.h"
+#include "fd_plan_internal.h"
 
 namespace {
 
@@ -23,19 +23,6 @@ constexpr int kCtasPerSm = 2;         // resident CTAs per SM (launch bounds + s
 size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 
 }  // namespace
-
-struct fd_plan_s {
-  int B, Hq, Hkv, d, G, dtype;
-  uint32_t flags;
-  int C;
-  int num_sms;
-  int max_partials;
-  int64_t n_tokens;
-  int64_t total_partials;
-  int ctas;
-  size_t off_counters, off_m, off_l, off_o, ws_bytes;
-  fd::Params params;  // pointers filled per call; arrays and scalars filled here
-};
 
 namespace {
 
@@ -55,8 +42,10 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   return fn;
 }
 
+}  // namespace
+
 // 3-D view (d, Hkv, N) of a [N, Hkv, d] tensor; one box = kTile rows of one head.
-int encode_kv_map(CUtensorMap* map, const void* base, const fd_plan_s* pl) {
+int fd::encode_kv_map(CUtensorMap* map, const void* base, const fd_plan_s* pl) {
   auto enc = tensor_map_encoder();
   if (!enc) return FD_ERR_CUDA;
   const cuuint64_t dims[3] = {(cuuint64_t)pl->d, (cuuint64_t)pl->Hkv, (cuuint64_t)pl->n_tokens};
@@ -70,6 +59,8 @@ int encode_kv_map(CUtensorMap* map, const void* base, const fd_plan_s* pl) {
                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? FD_OK : FD_ERR_CUDA;
 }
+
+namespace {
 
 cudaError_t launch(const fd::Params& p, int dtype, int d, int G, int mode, int grid,
                    cudaStream_t s) {
@@ -253,8 +244,8 @@ int fd_decode(fd_plan_t pl, const void* q, const void* k, const void* v, void* o
 
   fd::Params p = pl->params;  // per-call copy: the plan stays immutable
   if (pl->n_tokens > 0) {
-    int rc = encode_kv_map(&p.tm_k, k, pl);
-    if (rc == FD_OK) rc = encode_kv_map(&p.tm_v, v, pl);
+    int rc = fd::encode_kv_map(&p.tm_k, k, pl);
+    if (rc == FD_OK) rc = fd::encode_kv_map(&p.tm_v, v, pl);
     if (rc != FD_OK) return rc;
   }
   uint8_t* ws = static_cast<uint8_t*>(workspace);
