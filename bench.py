@@ -48,6 +48,8 @@ def parse_args(argv=None):
     ap.add_argument("--W", type=int, default=1, help="segments for the batch64 W-sweep workload")
     ap.add_argument("--chunks", type=int, default=0, help="chunks per segment (0 = planner)")
     ap.add_argument("--two-launch", action="store_true", help="split + combine as two kernels")
+    ap.add_argument("--ffma", action="store_true", help="CUDA-core consumers even when G >= 4")
+    ap.add_argument("--no-pdl", action="store_true", help="launch without programmatic dependent launch")
     ap.add_argument("--soak-s", type=float, default=1.5, help="untimed load before timing (clocks)")
     ap.add_argument("--e2e-steps", type=int, default=30)
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -313,7 +315,8 @@ def run_fd(args):
     copies = min(copies, max(1, int(40e9 // max(kv_bytes, 1))))
 
     flags = (fd.FD_PLAN_LITERAL_W if prob.literal_w else 0) | (
-        fd.FD_PLAN_TWO_LAUNCH if args.two_launch else 0)
+        fd.FD_PLAN_TWO_LAUNCH if args.two_launch else 0) | (fd.FD_PLAN_FFMA if args.ffma else 0) | (
+        fd.FD_PLAN_NO_PDL if args.no_pdl else 0)
     dec = fd.Decoder(prob.Hq, prob.Hkv, prob.d, prob.seqlens, prob.W, prob.dtype, flags=flags,
                      chunks=args.chunks, device=device)
     q = to_device(prob.q, prob.dtype, device)
@@ -335,8 +338,10 @@ def run_fd(args):
             step(i)
     stream.synchronize()
 
-    # Timed region: exactly K steps with an event pair around every launch.  Inside a
-    # CUDA graph the events must be "external" so that they become timing records.
+    # Two graphs over exactly K steps: A (the timed region) launches the K decodes
+    # back to back between one event pair; B puts an event pair around every launch
+    # to give the latency of a single decode.  Inside a CUDA graph the events must be
+    # "external" so that they become timing records.
     use_graph = not args.no_graph
     try:
         torch.cuda.Event(enable_timing=True, external=True)
@@ -350,29 +355,37 @@ def run_fd(args):
 
     ev = [(timing_event(), timing_event()) for _ in range(K)]
     ev_all = (timing_event(), timing_event())
-    graph = None
+    ev_b = (timing_event(), timing_event())
+
+    def record_a():
+        ev_all[0].record(stream)
+        for i in range(K):
+            step(i)
+        ev_all[1].record(stream)
+
+    def record_b():
+        ev_b[0].record(stream)
+        for i in range(K):
+            ev[i][0].record(stream)
+            step(i)
+            ev[i][1].record(stream)
+        ev_b[1].record(stream)
+
+    graphs = {}
     if use_graph:
-        graph = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(graph, stream=stream):
-            ev_all[0].record(stream)
-            for i in range(K):
-                ev[i][0].record(stream)
-                step(i)
-                ev[i][1].record(stream)
-            ev_all[1].record(stream)
+        for name, fn in (("a", record_a), ("b", record_b)):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                fn()
+            graphs[name] = g
         stream.synchronize()
 
-    def timed_once():
-        if graph is not None:
-            graph.replay()
+    def run(name):
+        if use_graph:
+            graphs[name].replay()
         else:
             with torch.cuda.stream(stream):
-                ev_all[0].record(stream)
-                for i in range(K):
-                    ev[i][0].record(stream)
-                    step(i)
-                    ev[i][1].record(stream)
-                ev_all[1].record(stream)
+                (record_a if name == "a" else record_b)()
 
     gpu_id = getattr(props, "uuid", None)
     gpu_id = f"GPU-{gpu_id}" if gpu_id is not None and not str(gpu_id).startswith("GPU-") else str(gpu_id or local)
@@ -380,25 +393,27 @@ def run_fd(args):
     t_soak = time.time()
     # Soak: the same replay, untimed, so clocks settle and the sampler sees the load.
     while time.time() - t_soak < args.soak_s:
-        timed_once()
+        run("a")
         stream.synchronize()
     barrier(world)
     torch.cuda.synchronize(device)
-    t_start = time.time()
-    timed_once()
+    run("a")                      # the timed region: exactly K steps
     stream.synchronize()
     torch.cuda.synchronize(device)
     t_end = time.time()
     barrier(world)
+    total_ms = ev_all[0].elapsed_time(ev_all[1])
+    run("b")                      # per-launch latency of the same K steps
+    stream.synchronize()
     sampler.stop()
     clocks = sampler.summary(t_soak, t_end)
     if dec.status() != fd.FD_OK:
         raise RuntimeError("device status word reported an error during the timed region")
 
-    total_ms = ev_all[0].elapsed_time(ev_all[1])
     per_launch = [a.elapsed_time(b) * 1e3 for a, b in ev]  # microseconds
     agg = aggregate_throughput(kv_bytes * K / 1e9, total_ms / 1e3, world, device)
     value = agg["throughput"]  # GB/s, whole job
+    step_us = total_ms * 1e3 / K
     mean_us = statistics.fmean(per_launch)
     qs = sorted(per_launch)
 
@@ -406,7 +421,8 @@ def run_fd(args):
         return qs[min(len(qs) - 1, max(0, int(round(p / 100 * (len(qs) - 1)))))]
 
     peak, peak_kind = load_peak()
-    achieved = kv_bytes / (mean_us * 1e-6) / 1e9
+    # Average device time per launch over the timed region (back-to-back launches).
+    achieved = kv_bytes / (step_us * 1e-6) / 1e9
 
     # e2e through the public API with pinned host buffers.
     e2e = e2e_measure(fd, dec, prob, device, args.e2e_steps, stream, kv_resident=False)
@@ -429,16 +445,22 @@ def run_fd(args):
                 "chunks_per_segment": info["chunks"], "ctas": info["ctas"],
                 "partials_per_sequence_max": info["max_partials"],
                 "kv_bytes_per_step": kv_bytes, "two_launch": bool(args.two_launch),
+                "pdl": not args.no_pdl,
+                "consumer": "mma.sync m16n8k16 (tensor cores)" if info["path"] == 1
+                            else "FFMA (CUDA cores)",
                 "l2_policy": f"K/V rotated over {copies} device copies ({copies * kv_bytes / 1e6:.0f} MB"
                              f" >= 4 x L2 {l2 / 1e6:.0f} MB)" if copies > 1 else
                              f"K/V {kv_bytes / 1e6:.0f} MB per step > 4 x L2 {l2 / 1e6:.0f} MB",
-                "launch": "CUDA graph replay of the K steps" if graph is not None else "eager",
+                "launch": "CUDA graph replay of the K steps" if use_graph else "eager",
                 "parallelism": f"replicas x{world}",
             },
             "latency_us": {"mean": mean_us, "median": statistics.median(per_launch),
-                           "p10": pct(10), "p90": pct(90), "min": qs[0], "max": qs[-1]},
+                           "p10": pct(10), "p90": pct(90), "min": qs[0], "max": qs[-1],
+                           "what": "one decode, CUDA events around each launch (second replay)"},
+            "step_us": step_us,
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "traffic": None,
+                         "achieved_from": "KV bytes per launch / (timed-region time / K)",
                          "peak_kind": f"{peak_kind} (hbm_gbs copy, burst)",
                          "kernel": "fd_split_kernel (fused)" if not args.two_launch
                          else "fd_split_kernel + fd_combine_kernel"},

@@ -63,6 +63,8 @@ enum fd_status {
 #define FD_PLAN_LITERAL_W 0x1u /* exactly W_b partials per sequence (chunks = 1) */
 #define FD_PLAN_DEBUG 0x2u     /* fd_decode checks counters/status (synchronises the stream) */
 #define FD_PLAN_TWO_LAUNCH 0x4u /* split kernel + separate combine kernel (ablation) */
+#define FD_PLAN_FFMA 0x8u       /* CUDA-core scores and P.V even when G >= 4 (ablation) */
+#define FD_PLAN_NO_PDL 0x10u    /* launch without programmatic dependent launch (ablation) */
 
 /* Compiled limits. */
 #define FD_MAX_BATCH 256       /* sequences per plan */
@@ -119,7 +121,10 @@ int fd_workspace_init(fd_plan_t plan, void* workspace, cudaStream_t stream);
  *   stream     CUDA stream (0 = legacy default stream)
  *
  * All device pointers must be 16-byte aligned (FD_ERR_ALIGN otherwise).  The
- * caller owns every buffer and the stream.  Asynchronous: returns after the
+ * caller owns every buffer and the stream.  Kernels are launched with
+ * programmatic dependent launch (unless FD_PLAN_NO_PDL): their prologue may
+ * overlap the previous kernel on the stream, but they read and write global
+ * memory only after every earlier kernel has completed.  Asynchronous: returns after the
  * launch; with FD_PLAN_DEBUG it synchronises and reports FD_ERR_TIMEOUT or
  * FD_ERR_STATE from the device status word.  Decodes that share a workspace
  * must not overlap in time.
@@ -180,6 +185,8 @@ typedef struct fd_plan_info {
   int64_t total_partials;  /* P */
   uint64_t workspace_bytes;
   uint64_t kv_bytes;       /* bytes of K and V one decode reads */
+  int32_t path;            /* 0: CUDA-core (FFMA) consumers, 1: tensor-core (mma.sync) */
+  int32_t reserved;
 } fd_plan_info;
 
 int fd_plan_get_info(fd_plan_t plan, fd_plan_info* info);

@@ -23,7 +23,9 @@ from ._binding import (  # noqa: F401
     FD_NOALLOC_SCRATCH_BYTES,
     FD_OK,
     FD_PLAN_DEBUG,
+    FD_PLAN_FFMA,
     FD_PLAN_LITERAL_W,
+    FD_PLAN_NO_PDL,
     FD_PLAN_TWO_LAUNCH,
     FdError,
     Plan,

@@ -27,6 +27,8 @@ FD_BF16 = 1
 FD_PLAN_LITERAL_W = 0x1
 FD_PLAN_DEBUG = 0x2
 FD_PLAN_TWO_LAUNCH = 0x4
+FD_PLAN_FFMA = 0x8
+FD_PLAN_NO_PDL = 0x10
 FD_MAX_BATCH = 256
 FD_MAX_PARTIALS = 1024
 
@@ -55,6 +57,7 @@ class PlanInfo(ctypes.Structure):
         ("ctas", ctypes.c_int32), ("max_partials", ctypes.c_int32),
         ("total_tokens", ctypes.c_int64), ("total_partials", ctypes.c_int64),
         ("workspace_bytes", ctypes.c_uint64), ("kv_bytes", ctypes.c_uint64),
+        ("path", ctypes.c_int32), ("reserved", ctypes.c_int32),
     ]
 
 

@@ -44,28 +44,33 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 
 }  // namespace
 
-// 3-D view (d, Hkv, N) of a [N, Hkv, d] tensor; one box = kTile rows of one head.
+// 3-D view (d, Hkv, N) of a [N, Hkv, d] tensor; one box = one tile of token rows of
+// one head.  The MMA path loads 64-column boxes (128-byte rows) with the 128-byte
+// swizzle; the FFMA path loads whole unswizzled rows.
 int fd::encode_kv_map(CUtensorMap* map, const void* base, const fd_plan_s* pl) {
   auto enc = tensor_map_encoder();
   if (!enc) return FD_ERR_CUDA;
   const cuuint64_t dims[3] = {(cuuint64_t)pl->d, (cuuint64_t)pl->Hkv, (cuuint64_t)pl->n_tokens};
   const cuuint64_t strides[2] = {(cuuint64_t)pl->d * 2, (cuuint64_t)pl->Hkv * pl->d * 2};
-  const cuuint32_t box[3] = {(cuuint32_t)pl->d, 1u, (cuuint32_t)fd::kTile};
+  const cuuint32_t box[3] = {(cuuint32_t)fd::box_cols_for(pl->path, pl->d), 1u,
+                             (cuuint32_t)fd::tile_for(pl->path)};
   const cuuint32_t estr[3] = {1u, 1u, 1u};
   const CUtensorMapDataType ty =
       pl->dtype == FD_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  const CUtensorMapSwizzle swz =
+      pl->path == fd::kPathMma ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE;
   CUresult r = enc(map, ty, 3, const_cast<void*>(base), dims, strides, box, estr,
-                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
-                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? FD_OK : FD_ERR_CUDA;
 }
 
 namespace {
 
-cudaError_t launch(const fd::Params& p, int dtype, int d, int G, int mode, int grid,
-                   cudaStream_t s) {
-  return dtype == FD_F16 ? fd::launch_f16(p, d, G, mode, grid, s)
-                         : fd::launch_bf16(p, d, G, mode, grid, s);
+cudaError_t launch(const fd_plan_s* pl, const fd::Params& p, int mode, int grid, cudaStream_t s) {
+  const bool pdl = !(pl->flags & FD_PLAN_NO_PDL);
+  return pl->dtype == FD_F16 ? fd::launch_f16(p, pl->d, pl->G, pl->path, mode, pdl, grid, s)
+                             : fd::launch_bf16(p, pl->d, pl->G, pl->path, mode, pdl, grid, s);
 }
 
 }  // namespace
@@ -96,7 +101,9 @@ int fd_plan(int B, int Hq, int Hkv, int d, const int32_t* seqlens, const int32_t
   if (B < 1 || Hq < 1 || Hkv < 1 || d < 1 || chunks < 0 || num_sms < 0) return FD_ERR_INVALID;
   if (Hq % Hkv != 0) return FD_ERR_INVALID;
   if (dtype != FD_F16 && dtype != FD_BF16) return FD_ERR_INVALID;
-  if (flags & ~(FD_PLAN_LITERAL_W | FD_PLAN_DEBUG | FD_PLAN_TWO_LAUNCH)) return FD_ERR_INVALID;
+  if (flags & ~(FD_PLAN_LITERAL_W | FD_PLAN_DEBUG | FD_PLAN_TWO_LAUNCH | FD_PLAN_FFMA |
+                FD_PLAN_NO_PDL))
+    return FD_ERR_INVALID;
   const int G = Hq / Hkv;
   if (B > FD_MAX_BATCH) return FD_ERR_UNSUPPORTED;
   if (d != 64 && d != 128) return FD_ERR_UNSUPPORTED;
@@ -144,6 +151,8 @@ int fd_plan(int B, int Hq, int Hkv, int d, const int32_t* seqlens, const int32_t
   if (!pl) return FD_ERR_NOMEM;
   pl->B = B; pl->Hq = Hq; pl->Hkv = Hkv; pl->d = d; pl->G = G; pl->dtype = dtype;
   pl->flags = flags; pl->C = C; pl->num_sms = num_sms;
+  // Tensor cores whenever the GQA group covers at least half of the mma N = 8 tile.
+  pl->path = (G >= 4 && !(flags & FD_PLAN_FFMA)) ? fd::kPathMma : fd::kPathFfma;
   pl->max_partials = max_w * C;
   pl->n_tokens = n_tokens;
   pl->total_partials = (int64_t)Hq * sum_w * C;
@@ -164,16 +173,12 @@ int fd_plan(int B, int Hq, int Hkv, int d, const int32_t* seqlens, const int32_t
   p.cu[B] = cu;
   p.unit_base[B] = ub;
 
-  // Workspace: status | counters | m | l | O (each 256-byte aligned).
+  // Workspace: status | counters | partial records [P][d + 4] (each 256-byte aligned).
   size_t off = kAlign;
   pl->off_counters = off;
   off = align_up(off + sizeof(uint32_t) * (size_t)B * Hkv);
-  pl->off_m = off;
-  off = align_up(off + sizeof(float) * (size_t)pl->total_partials);
-  pl->off_l = off;
-  off = align_up(off + sizeof(float) * (size_t)pl->total_partials);
-  pl->off_o = off;
-  off = align_up(off + sizeof(float) * (size_t)pl->total_partials * d);
+  pl->off_part = off;
+  off = align_up(off + sizeof(float) * (size_t)pl->total_partials * fd::record_floats(d));
   pl->ws_bytes = off;
 
   *out_plan = pl;
@@ -195,6 +200,8 @@ int fd_plan_get_info(fd_plan_t pl, fd_plan_info* info) {
   info->total_tokens = pl->n_tokens; info->total_partials = pl->total_partials;
   info->workspace_bytes = pl->ws_bytes;
   info->kv_bytes = (uint64_t)pl->n_tokens * pl->Hkv * pl->d * 2 * 2;
+  info->path = pl->path;
+  info->reserved = 0;
   return FD_OK;
 }
 
@@ -212,7 +219,7 @@ int fd_plan_get_range(fd_plan_t pl, int b, int slot, int32_t* begin, int32_t* en
 
 int fd_workspace_init(fd_plan_t pl, void* workspace, cudaStream_t stream) {
   if (!pl || !workspace) return FD_ERR_INVALID;
-  if (cudaMemsetAsync(workspace, 0, pl->off_m, stream) != cudaSuccess) {
+  if (cudaMemsetAsync(workspace, 0, pl->off_part, stream) != cudaSuccess) {
     cudaGetLastError();
     return FD_ERR_CUDA;
   }
@@ -254,9 +261,7 @@ int fd_decode(fd_plan_t pl, const void* q, const void* k, const void* v, void* o
   p.lse = lse;
   p.status = reinterpret_cast<uint32_t*>(ws);
   p.counters = reinterpret_cast<uint32_t*>(ws + pl->off_counters);
-  p.part_m = reinterpret_cast<float*>(ws + pl->off_m);
-  p.part_l = reinterpret_cast<float*>(ws + pl->off_l);
-  p.part_o = reinterpret_cast<float*>(ws + pl->off_o);
+  p.part = reinterpret_cast<float*>(ws + pl->off_part);
 
   const bool debug = (pl->flags & FD_PLAN_DEBUG) != 0;
   if (debug) {
@@ -273,10 +278,10 @@ int fd_decode(fd_plan_t pl, const void* q, const void* k, const void* v, void* o
 
   cudaError_t err;
   if (pl->flags & FD_PLAN_TWO_LAUNCH) {
-    err = launch(p, pl->dtype, pl->d, pl->G, 1, pl->ctas, stream);
-    if (err == cudaSuccess) err = launch(p, pl->dtype, pl->d, pl->G, 2, pl->B * pl->Hkv, stream);
+    err = launch(pl, p, 1, pl->ctas, stream);
+    if (err == cudaSuccess) err = launch(pl, p, 2, pl->B * pl->Hkv, stream);
   } else {
-    err = launch(p, pl->dtype, pl->d, pl->G, 0, pl->ctas, stream);
+    err = launch(pl, p, 0, pl->ctas, stream);
   }
   if (err != cudaSuccess) {
     cudaGetLastError();

@@ -17,19 +17,32 @@
 
 namespace fd {
 
-// Tokens per pipeline stage (rows of K and of V moved by one pair of TMA loads).
-constexpr int kTile = 32;
 // Consumer warps per CTA; one more warp issues the TMA loads.
 constexpr int kConsumerWarps = 4;
 constexpr int kThreads = (kConsumerWarps + 1) * 32;
 
-// Stages of the shared-memory ring per head dimension.
-FD_HD constexpr int stages_for(int d) { return d == 128 ? 6 : 8; }
+// Two consumer paths.  FFMA: CUDA-core dot products, unswizzled [tile][d] rows.
+// MMA: mma.sync m16n8k16 with tokens on M and the GQA heads on N, K/V staged as
+// 64-column half-tiles with the 128-byte TMA swizzle (conflict-free ldmatrix).
+constexpr int kPathFfma = 0;
+constexpr int kPathMma = 1;
 
-// Dynamic shared memory of one CTA: the K/V ring plus the mbarriers.
-FD_HD constexpr size_t smem_bytes_for(int d) {
-  return (size_t)stages_for(d) * 2 * kTile * d * 2 + 1024;
+// Tokens per pipeline stage.
+FD_HD constexpr int tile_for(int path) { return path == kPathMma ? 64 : 32; }
+// Stages of the shared-memory ring.
+FD_HD constexpr int stages_for(int path, int d) {
+  return path == kPathMma ? (d == 128 ? 3 : 4) : (d == 128 ? 6 : 8);
 }
+// Columns (elements) of one TMA box row; MMA boxes are 128-byte swizzled rows.
+FD_HD constexpr int box_cols_for(int path, int d) { return path == kPathMma ? 64 : d; }
+// Bytes of the K/V ring (also the scratch the combine reuses).
+FD_HD constexpr size_t ring_bytes_for(int path, int d) {
+  return (size_t)stages_for(path, d) * 2 * tile_for(path) * d * 2;
+}
+// Dynamic shared memory of one CTA: the ring, the mbarriers and 1 KB of alignment slack.
+FD_HD constexpr size_t smem_bytes_for(int path, int d) { return ring_bytes_for(path, d) + 2048; }
+// Floats per partial record: O[0..d), m, l and two pad words (16-byte records).
+FD_HD constexpr int record_floats(int d) { return d + 4; }
 
 // Status word values written by the kernels (the host maps them to fd_status).
 constexpr uint32_t kStatusTimeout = 1u;
@@ -42,9 +55,7 @@ struct Params {
   const void* q;     // [B, Hq, d]
   void* out;         // [B, Hq, d]
   float* lse;        // [B, Hq] or nullptr
-  float* part_o;     // [P, d]
-  float* part_m;     // [P]   (log2-domain maxima of the scaled logits)
-  float* part_l;     // [P]
+  float* part;       // [P, d + 4] records: O[0..d), m, l, 0, 0 (m in the log2 domain)
   uint32_t* counters;  // [B * Hkv]
   uint32_t* status;    // 1 word
   float scale_log2;    // log2(e) / sqrt(d)
@@ -75,7 +86,11 @@ FD_HD void chunk_range(int L, int W, int C, int slot, int* t0, int* t1) {
 
 // Launchers defined in the per-dtype kernel translation units.
 // mode 0: fused split + last-arriver combine; 1: split only (partials); 2: combine only.
-cudaError_t launch_f16(const Params& p, int d, int G, int mode, int grid, cudaStream_t s);
-cudaError_t launch_bf16(const Params& p, int d, int G, int mode, int grid, cudaStream_t s);
+// pdl: launch with programmatic stream serialization (the kernel waits on its
+// predecessors with griddepcontrol.wait before touching global memory).
+cudaError_t launch_f16(const Params& p, int d, int G, int path, int mode, bool pdl, int grid,
+                       cudaStream_t s);
+cudaError_t launch_bf16(const Params& p, int d, int G, int path, int mode, bool pdl, int grid,
+                        cudaStream_t s);
 
 }  // namespace fd

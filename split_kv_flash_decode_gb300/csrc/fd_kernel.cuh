@@ -10,14 +10,19 @@
 // (Push-model flag ordering, correctness check #4).
 //
 // GB300 mapping (one CTA = one chunk of one segment of one (sequence, KV head)):
-//   * warp 4, lane 0: TMA producer.  Per stage it issues two 3-D tensor loads
-//     (kTile K rows and kTile V rows of one KV head) into an mbarrier ring.
-//   * warps 0-3: consumers.  Lanes form groups of LPT lanes; a group owns one
-//     token at a time, each lane holding D/LPT dimensions of q (fp32, scaled into
-//     the log2 domain) for all G query heads that share this KV head, so every
-//     K/V byte loaded serves the whole GQA group.  Scores use FFMA plus an
-//     xor-shuffle reduction inside the group; each group keeps its own running
-//     (m, l, acc) with a lazy rescale (only when the max grows by > 2^8).
+//   * warp 4, lane 0: TMA producer.  Per stage it issues 3-D tensor loads of a
+//     tile of K rows and of V rows of one KV head into an mbarrier ring.
+//   * warps 0-3: consumers; every K/V byte loaded serves all G query heads that
+//     share the KV head (GQA packing).  Two consumer paths:
+//       MMA  (G >= 4): mma.sync m16n8k16 with 16 tokens on M and the G heads on
+//            N (G = 8 fills the tile, G = 4 half-fills it): S^T = K Q^T, then
+//            O^T += V^T P^T with P moved from the accumulator layout to the
+//            operand layout by movmatrix.  K/V tiles are 64-column half-tiles
+//            with the 128-byte swizzle, so ldmatrix is conflict-free.
+//       FFMA (G <= 2, or forced): lanes form groups of LPT lanes, a group owns
+//            one token at a time, scores use FFMA plus an xor-shuffle reduction.
+//     Each warp (MMA) or token group (FFMA) keeps its own running (m, l, acc)
+//     in the log2 domain with a lazy rescale (only when the max grows by > 2^8).
 //   * end of CTA: groups merge through shared memory into one fp32 partial,
 //     which is written to the workspace; one thread then does
 //     fence + atom.add.acq_rel.gpu on the (sequence, KV head) arrival counter.
@@ -90,6 +95,18 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
   }
 }
 
+// Programmatic dependent launch: let the next kernel on the stream start its
+// prologue now; and wait until every preceding kernel has finished and its
+// memory is visible (a no-op for launches without the PDL attribute).
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+__device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
 __device__ __forceinline__ uint64_t l2_evict_first_policy() {
   uint64_t pol;
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
@@ -151,6 +168,75 @@ __device__ __forceinline__ void unpack8(const uint4& raw, float* f) {
   f[4] = c.x; f[5] = c.y; f[6] = d.x; f[7] = d.y;
 }
 
+
+__device__ __forceinline__ void ldmatrix_x4(uint32_t (&r)[4], uint32_t addr) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+
+__device__ __forceinline__ void ldmatrix_x4_trans(uint32_t (&r)[4], uint32_t addr) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+
+__device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x) {
+  uint32_t y;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+  return y;
+}
+
+// D += A * B for one m16n8k16 tile, fp32 accumulate.
+template <typename T>
+__device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                         uint32_t b1);
+
+template <>
+__device__ __forceinline__ void mma16816<__half>(float (&d)[4], const uint32_t (&a)[4],
+                                                 uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+template <>
+__device__ __forceinline__ void mma16816<__nv_bfloat16>(float (&d)[4], const uint32_t (&a)[4],
+                                                        uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// Two fp32 values rounded (RN) to one packed 16-bit pair: lo in bits 0-15.
+template <typename T>
+__device__ __forceinline__ uint32_t pack2(float lo, float hi);
+
+template <>
+__device__ __forceinline__ uint32_t pack2<__half>(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+template <>
+__device__ __forceinline__ uint32_t pack2<__nv_bfloat16>(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// Shared-memory address of 16-byte chunk `ch` (0 .. D/8-1) of token row `row` in a
+// tile stored as 64-column half-tiles of `rows` rows with the 128-byte swizzle
+// (chunk index XOR row index mod 8, the pattern the TMA writes).
+__device__ __forceinline__ uint32_t swz_addr(uint32_t base, int rows, int row, int ch) {
+  return base + (uint32_t)((ch >> 3) * rows * 128 + row * 128 + (((ch & 7) ^ (row & 7)) << 4));
+}
+
 // Work item of CTA `cta` in the flattened (sequence, slot, KV head) order.
 struct Work {
   int b, kvh, slot, wtot, t0, t1;
@@ -175,30 +261,65 @@ __device__ __forceinline__ Work decode_work(const Params& p, int cta) {
   return w;
 }
 
-// OnlineSoftmaxCombine of the Wtot partials of (b, kvh): all kThreads threads take
-// part; `sm` holds at least G * wtot + 2 * G floats.  Order of summation is fixed
-// (partial index order), so the result does not depend on arrival order.
+// Merge two (max, sum) pairs of the log2-domain softmax (-inf max = empty).
+__device__ __forceinline__ void ml_merge(float& M, float& lam, float m2, float l2) {
+  if (m2 == -INFINITY) return;
+  if (M == -INFINITY) { M = m2; lam = l2; return; }
+  if (m2 > M) { lam = fmaf(lam, ex2(M - m2), l2); M = m2; }
+  else lam = fmaf(l2, ex2(m2 - M), lam);
+}
+
+// 1-D bulk copy global -> shared memory, completing on mbarrier `bar`.
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes,
+                                          uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+      "l"(src), "r"(bytes), "r"(bar)
+      : "memory");
+}
+
+// Order this thread's view of generic-proxy global writes before its later
+// async-proxy (bulk copy) reads of global memory.
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
+// Write out[b, h, 4*c4 .. 4*c4+3] and, for c4 == 0, nothing else.
+template <typename T>
+__device__ __forceinline__ void store_out4(T* dst, float4 a, float lam) {
+  dst[0] = Elem<T>::from_f(lam > 0.f ? a.x / lam : 0.f);
+  dst[1] = Elem<T>::from_f(lam > 0.f ? a.y / lam : 0.f);
+  dst[2] = Elem<T>::from_f(lam > 0.f ? a.z / lam : 0.f);
+  dst[3] = Elem<T>::from_f(lam > 0.f ? a.w / lam : 0.f);
+}
+
+// OnlineSoftmaxCombine of the Wtot partials of (b, kvh) for query heads
+// [g0, g0 + ng).  `rec` (shared memory) holds their records, head-major
+// [ng][wtot][D + 4]; `coef` holds ng * wtot + 2 * ng floats.  The summation order
+// is fixed (per-lane strides, a fixed shuffle tree, partial index order for O),
+// so the result does not depend on the order in which the partials arrived.
 template <typename T, int D, int G>
-__device__ __forceinline__ void combine_partials(const Params& p, int b, int kvh, int wtot,
-                                                 int64_t pbase, float* sm) {
-  float* coef = sm;              // [G][wtot]  e^{m_w - M}
-  float* ML = sm + G * wtot;     // [G][2]     (M, Lambda)
+__device__ __forceinline__ void combine_from_smem(const Params& p, int b, int kvh, int wtot,
+                                                  int g0, int ng, const float* rec, float* coef) {
+  constexpr int RS = record_floats(D);
+  float* ML = coef + ng * wtot;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   constexpr int kWarps = kThreads / 32;
-  for (int g = warp; g < G; g += kWarps) {
-    const int64_t row = pbase + (int64_t)(kvh * G + g) * wtot;
-    float M = -INFINITY;
-    for (int w = lane; w < wtot; w += 32) M = fmaxf(M, __ldcg(p.part_m + row + w));
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
-    float lam = 0.f;
+  for (int g = warp; g < ng; g += kWarps) {
+    float M = -INFINITY, lam = 0.f;
     for (int w = lane; w < wtot; w += 32) {
-      const float e = (M == -INFINITY) ? 0.f : ex2(__ldcg(p.part_m + row + w) - M);
-      coef[g * wtot + w] = e;
-      lam = fmaf(e, __ldcg(p.part_l + row + w), lam);
+      const float* r = rec + (size_t)(g * wtot + w) * RS + D;
+      ml_merge(M, lam, r[0], r[1]);
     }
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) lam += __shfl_xor_sync(0xffffffffu, lam, off);
+    for (int off = 16; off > 0; off >>= 1) {
+      const float m2 = __shfl_xor_sync(0xffffffffu, M, off);
+      const float l2 = __shfl_xor_sync(0xffffffffu, lam, off);
+      ml_merge(M, lam, m2, l2);
+    }
+    for (int w = lane; w < wtot; w += 32)
+      coef[g * wtot + w] =
+          (M == -INFINITY) ? 0.f : ex2(rec[(size_t)(g * wtot + w) * RS + D] - M);
     if (lane == 0) {
       ML[2 * g] = M;
       ML[2 * g + 1] = lam;
@@ -206,22 +327,88 @@ __device__ __forceinline__ void combine_partials(const Params& p, int b, int kvh
   }
   __syncthreads();
   T* out = reinterpret_cast<T*>(p.out);
-  for (int idx = tid; idx < G * D; idx += kThreads) {
-    const int g = idx / D, dim = idx - (idx / D) * D;
-    const float* po = p.part_o + (pbase + (int64_t)(kvh * G + g) * wtot) * D + dim;
+  for (int v = tid; v < ng * (D / 4); v += kThreads) {
+    const int g = v / (D / 4), c4 = v - (v / (D / 4)) * (D / 4);
+    const float4* r = reinterpret_cast<const float4*>(rec + (size_t)g * wtot * RS) + c4;
     const float* cg = coef + g * wtot;
-    float a = 0.f;
+    float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int w = 0; w < wtot; ++w) {
+      const float4 x = r[(size_t)w * (RS / 4)];
+      const float c = cg[w];
+      a.x = fmaf(c, x.x, a.x);
+      a.y = fmaf(c, x.y, a.y);
+      a.z = fmaf(c, x.z, a.z);
+      a.w = fmaf(c, x.w, a.w);
+    }
+    store_out4<T>(out + ((int64_t)b * p.Hq + kvh * G + g0 + g) * D + 4 * c4, a, ML[2 * g + 1]);
+  }
+  if (tid < ng && p.lse != nullptr) {
+    const float M = ML[2 * tid], lam = ML[2 * tid + 1];
+    p.lse[(int64_t)b * p.Hq + kvh * G + g0 + tid] = lam > 0.f ? (M + log2f(lam)) * kLn2 : -INFINITY;
+  }
+}
+
+// Same combine reading the records straight from L2 (for partial counts whose
+// records do not fit in shared memory); `coef` holds G * wtot + 2 * G floats.
+template <typename T, int D, int G>
+__device__ __forceinline__ void combine_from_global(const Params& p, int b, int kvh, int wtot,
+                                                    int64_t pbase, float* coef) {
+  constexpr int RS = record_floats(D);
+  float* ML = coef + G * wtot;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  constexpr int kWarps = kThreads / 32;
+  for (int g = warp; g < G; g += kWarps) {
+    const float* row = p.part + (pbase + (int64_t)(kvh * G + g) * wtot) * RS + D;
+    float M = -INFINITY, lam = 0.f;
+    for (int w = lane; w < wtot; w += 32) {
+      const float2 ml = __ldcg(reinterpret_cast<const float2*>(row + (size_t)w * RS));
+      coef[g * wtot + w] = ml.x;
+      ml_merge(M, lam, ml.x, ml.y);
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+      const float m2 = __shfl_xor_sync(0xffffffffu, M, off);
+      const float l2 = __shfl_xor_sync(0xffffffffu, lam, off);
+      ml_merge(M, lam, m2, l2);
+    }
+    for (int w = lane; w < wtot; w += 32)
+      coef[g * wtot + w] = (M == -INFINITY) ? 0.f : ex2(coef[g * wtot + w] - M);
+    if (lane == 0) {
+      ML[2 * g] = M;
+      ML[2 * g + 1] = lam;
+    }
+  }
+  __syncthreads();
+  T* out = reinterpret_cast<T*>(p.out);
+  for (int v = tid; v < G * (D / 4); v += kThreads) {
+    const int g = v / (D / 4), c4 = v - (v / (D / 4)) * (D / 4);
+    const float4* r =
+        reinterpret_cast<const float4*>(p.part + (pbase + (int64_t)(kvh * G + g) * wtot) * RS) + c4;
+    const float* cg = coef + g * wtot;
+    float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
     int w = 0;
     for (; w + 8 <= wtot; w += 8) {
-      float x[8];
+      float4 x[8];
 #pragma unroll
-      for (int u = 0; u < 8; ++u) x[u] = __ldcg(po + (int64_t)(w + u) * D);
+      for (int u = 0; u < 8; ++u) x[u] = __ldcg(r + (size_t)(w + u) * (RS / 4));
 #pragma unroll
-      for (int u = 0; u < 8; ++u) a = fmaf(cg[w + u], x[u], a);
+      for (int u = 0; u < 8; ++u) {
+        const float c = cg[w + u];
+        a.x = fmaf(c, x[u].x, a.x);
+        a.y = fmaf(c, x[u].y, a.y);
+        a.z = fmaf(c, x[u].z, a.z);
+        a.w = fmaf(c, x[u].w, a.w);
+      }
     }
-    for (; w < wtot; ++w) a = fmaf(cg[w], __ldcg(po + (int64_t)w * D), a);
-    const float lam = ML[2 * g + 1];
-    out[((int64_t)b * p.Hq + kvh * G + g) * D + dim] = Elem<T>::from_f(lam > 0.f ? a / lam : 0.f);
+    for (; w < wtot; ++w) {
+      const float4 x = __ldcg(r + (size_t)w * (RS / 4));
+      const float c = cg[w];
+      a.x = fmaf(c, x.x, a.x);
+      a.y = fmaf(c, x.y, a.y);
+      a.z = fmaf(c, x.z, a.z);
+      a.w = fmaf(c, x.w, a.w);
+    }
+    store_out4<T>(out + ((int64_t)b * p.Hq + kvh * G + g) * D + 4 * c4, a, ML[2 * g + 1]);
   }
   if (tid < G && p.lse != nullptr) {
     const float M = ML[2 * tid], lam = ML[2 * tid + 1];
@@ -229,207 +416,55 @@ __device__ __forceinline__ void combine_partials(const Params& p, int b, int kvh
   }
 }
 
-// MODE 0: fused split + last-arriver combine.  MODE 1: split only (partials).
-template <typename T, int D, int G, int MODE>
-__global__ void __launch_bounds__(kThreads, 2) fd_split_kernel(const __grid_constant__ Params p) {
-  constexpr int STAGES = stages_for(D);
-  constexpr int LPT = (G * D > 512) ? 16 : 8;  // lanes per token
-  constexpr int DL = D / LPT;                   // dimensions per lane
-  constexpr int NCH = DL / 8;                   // 16-byte chunks per lane per row
-  constexpr int GPW = 32 / LPT;                 // token groups per warp
-  constexpr int NGRP = kConsumerWarps * GPW;    // token groups per CTA
-  constexpr int TPG = kTile / NGRP;             // tokens per group per stage
-  constexpr uint32_t kRowsBytes = kTile * D * sizeof(T);
-  static_assert(kTile % NGRP == 0, "tile must split evenly over token groups");
-  static_assert(NGRP * G * D * 4 + 4 * NGRP * G * 4 <= STAGES * 2 * kRowsBytes,
-                "group merge must fit in the ring");
-
-  extern __shared__ __align__(1024) uint8_t smem[];
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + (size_t)STAGES * 2 * kRowsBytes);
-  int& sm_abort = *reinterpret_cast<int*>(bars + 2 * STAGES);
-  int& sm_last = *(reinterpret_cast<int*>(bars + 2 * STAGES) + 1);
-  auto full_bar = [&](int s) { return smem_addr(bars + s); };
-  auto empty_bar = [&](int s) { return smem_addr(bars + STAGES + s); };
-  auto k_rows = [&](int s) { return reinterpret_cast<const T*>(smem + (size_t)s * 2 * kRowsBytes); };
-
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const Work wk = decode_work(p, blockIdx.x);
-  const int ntiles = (wk.t1 - wk.t0 + kTile - 1) / kTile;
-
-  if (tid == 0) {
-    for (int s = 0; s < STAGES; ++s) {
-      mbar_init(full_bar(s), 1);
-      mbar_init(empty_bar(s), kConsumerWarps);
-    }
-    fence_mbar_init();
-    sm_abort = 0;
+// Combine all partials of (b, kvh).  The records of as many heads as fit are
+// pulled into shared memory (`smem`, `smem_bytes`) with one bulk copy per pass,
+// completing on mbarrier `bar` (whose next phase parity is `phase`).
+template <typename T, int D, int G>
+__device__ __forceinline__ void combine_partials(const Params& p, int b, int kvh, int wtot,
+                                                 int64_t pbase, uint8_t* smem, uint32_t smem_bytes,
+                                                 uint32_t bar, uint32_t& phase) {
+  constexpr int RS = record_floats(D);
+  const uint32_t head_bytes = (uint32_t)wtot * RS * 4;
+  const uint32_t coef_bytes = ((uint32_t)(G * wtot + 2 * G) * 4 + 15u) & ~15u;
+  const uint32_t avail = smem_bytes > coef_bytes ? smem_bytes - coef_bytes : 0u;
+  const int hpp = head_bytes > 0 ? (int)min((uint32_t)G, avail / head_bytes) : 0;
+  if (hpp == 0) {
+    combine_from_global<T, D, G>(p, b, kvh, wtot, pbase, reinterpret_cast<float*>(smem));
+    return;
   }
-  __syncthreads();
-
-  // Per-group online-softmax state (consumers only).
-  float acc[G][DL];
-  float m_run[G], l_run[G];
-  const int j = lane % LPT;                     // lane within its token group
-  const int gi = warp * GPW + lane / LPT;       // token group id
-
-  if (warp == kConsumerWarps) {
-    // ---------------- TMA producer ----------------
-    if (lane == 0 && ntiles > 0) {
-      const uint64_t policy = l2_evict_first_policy();
-      const int row0 = p.cu[wk.b] + wk.t0;
-      int kt = 0;
-      for (; kt < ntiles; ++kt) {
-        const int s = kt % STAGES;
-        if (kt >= STAGES && !mbar_wait(empty_bar(s), ((kt / STAGES) - 1) & 1)) {
-          atomicOr(p.status, kStatusTimeout);
-          *(volatile int*)&sm_abort = 1;
-          break;
-        }
-        if (*(volatile int*)&sm_abort) break;
-        const uint32_t dst = smem_addr(smem + (size_t)s * 2 * kRowsBytes);
-        mbar_arrive_expect_tx(full_bar(s), 2 * kRowsBytes);
-        tma_load_3d(dst, &p.tm_k, 0, wk.kvh, row0 + kt * kTile, full_bar(s), policy);
-        tma_load_3d(dst + kRowsBytes, &p.tm_v, 0, wk.kvh, row0 + kt * kTile, full_bar(s), policy);
-      }
-      // Every load issued must land before shared memory is reused or released.
-      for (int t = (kt > STAGES ? kt - STAGES : 0); t < kt; ++t) {
-        if (!mbar_wait(full_bar(t % STAGES), (t / STAGES) & 1)) atomicOr(p.status, kStatusTimeout);
-      }
+  float* rec = reinterpret_cast<float*>(smem);
+  float* coef = reinterpret_cast<float*>(smem + avail);
+  for (int g0 = 0; g0 < G; g0 += hpp) {
+    const int ng = min(hpp, G - g0);
+    if (threadIdx.x == 0) {
+      fence_proxy_async_global();
+      const uint32_t bytes = (uint32_t)ng * head_bytes;
+      mbar_arrive_expect_tx(bar, bytes);
+      const uint8_t* src = reinterpret_cast<const uint8_t*>(
+          p.part + (pbase + (int64_t)(kvh * G + g0) * wtot) * RS);
+      const uint32_t dst = smem_addr(smem);
+      for (uint32_t off = 0; off < bytes; off += 32768u)
+        bulk_load(dst + off, src + off, min(32768u, bytes - off), bar);
     }
-  } else {
-    // ---------------- consumers ----------------
-    const T* qg = reinterpret_cast<const T*>(p.q) + ((int64_t)wk.b * p.Hq + wk.kvh * G) * D;
-    float qf[G][DL];
-#pragma unroll
-    for (int g = 0; g < G; ++g) {
-#pragma unroll
-      for (int c = 0; c < NCH; ++c) {
-        const uint4 raw = *reinterpret_cast<const uint4*>(qg + g * D + (j + LPT * c) * 8);
-        unpack8<T>(raw, &qf[g][c * 8]);
-      }
-#pragma unroll
-      for (int e = 0; e < DL; ++e) qf[g][e] *= p.scale_log2;
-    }
-#pragma unroll
-    for (int g = 0; g < G; ++g) {
-      m_run[g] = -INFINITY;
-      l_run[g] = 0.f;
-#pragma unroll
-      for (int e = 0; e < DL; ++e) acc[g][e] = 0.f;
-    }
-
-    for (int kt = 0; kt < ntiles; ++kt) {
-      const int s = kt % STAGES;
-      // Every lane waits; the warp leaves together so shuffles never see a partial warp.
-      const bool ok = mbar_wait(full_bar(s), (kt / STAGES) & 1);
-      if (__any_sync(0xffffffffu, !ok || *(volatile int*)&sm_abort != 0)) {
-        if (!ok) {
-          atomicOr(p.status, kStatusTimeout);
-          *(volatile int*)&sm_abort = 1;
-        }
-        break;
-      }
-      const int ntok = min(kTile, wk.t1 - (wk.t0 + kt * kTile));
-      const T* Ks = k_rows(s);
-      const T* Vs = Ks + kTile * D;
-
-      // Scores of this group's tokens for all G heads (log2 domain).
-      float sc[TPG][G];
-#pragma unroll
-      for (int r = 0; r < TPG; ++r) {
-        const int tok = gi + NGRP * r;
-        float part[G];
-#pragma unroll
-        for (int g = 0; g < G; ++g) part[g] = 0.f;
-        if (tok < ntok) {
-#pragma unroll
-          for (int c = 0; c < NCH; ++c) {
-            const uint4 raw = *reinterpret_cast<const uint4*>(Ks + tok * D + (j + LPT * c) * 8);
-            float kf[8];
-            unpack8<T>(raw, kf);
-#pragma unroll
-            for (int g = 0; g < G; ++g)
-#pragma unroll
-              for (int e = 0; e < 8; ++e) part[g] = fmaf(qf[g][c * 8 + e], kf[e], part[g]);
-          }
-        }
-#pragma unroll
-        for (int off = 1; off < LPT; off <<= 1)
-#pragma unroll
-          for (int g = 0; g < G; ++g) part[g] += __shfl_xor_sync(0xffffffffu, part[g], off);
-#pragma unroll
-        for (int g = 0; g < G; ++g) sc[r][g] = (tok < ntok) ? part[g] : -INFINITY;
-      }
-
-      // Online softmax with lazy rescaling.
-      float pr[TPG][G];
-#pragma unroll
-      for (int g = 0; g < G; ++g) {
-        float mx = sc[0][g];
-#pragma unroll
-        for (int r = 1; r < TPG; ++r) mx = fmaxf(mx, sc[r][g]);
-        if (mx > m_run[g] + kRescaleThreshold) {
-          const float corr = ex2(m_run[g] - mx);
-          l_run[g] *= corr;
-#pragma unroll
-          for (int e = 0; e < DL; ++e) acc[g][e] *= corr;
-          m_run[g] = mx;
-        }
-#pragma unroll
-        for (int r = 0; r < TPG; ++r) {
-          pr[r][g] = (gi + NGRP * r < ntok) ? ex2(sc[r][g] - m_run[g]) : 0.f;
-          l_run[g] += pr[r][g];
-        }
-      }
-
-      // P . V
-#pragma unroll
-      for (int r = 0; r < TPG; ++r) {
-        const int tok = gi + NGRP * r;
-        if (tok < ntok) {
-#pragma unroll
-          for (int c = 0; c < NCH; ++c) {
-            const uint4 raw = *reinterpret_cast<const uint4*>(Vs + tok * D + (j + LPT * c) * 8);
-            float vf[8];
-            unpack8<T>(raw, vf);
-#pragma unroll
-            for (int g = 0; g < G; ++g)
-#pragma unroll
-              for (int e = 0; e < 8; ++e) acc[g][c * 8 + e] = fmaf(pr[r][g], vf[e], acc[g][c * 8 + e]);
-          }
-        }
-      }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(empty_bar(s));
-    }
+    if (!mbar_wait(bar, phase)) atomicOr(p.status, kStatusTimeout);
+    phase ^= 1u;
+    combine_from_smem<T, D, G>(p, b, kvh, wtot, g0, ng, rec, coef);
+    __syncthreads();  // the next pass overwrites the records
   }
-  __syncthreads();
-  if (sm_abort) return;
+}
 
-  // ---------------- merge the token groups into one partial ----------------
-  float* sm_acc = reinterpret_cast<float*>(smem);  // [NGRP][G][D]
-  float* sm_m = sm_acc + NGRP * G * D;              // [NGRP][G]
-  float* sm_l = sm_m + NGRP * G;                    // [NGRP][G]
-  float* sm_fac = sm_l + NGRP * G;                  // [NGRP][G]
-  float* sm_ML = sm_fac + NGRP * G;                 // [G][2]
-  if (warp < kConsumerWarps) {
-#pragma unroll
-    for (int g = 0; g < G; ++g)
-#pragma unroll
-      for (int c = 0; c < NCH; ++c) {
-        float4* dst = reinterpret_cast<float4*>(sm_acc + (gi * G + g) * D + (j + LPT * c) * 8);
-        dst[0] = make_float4(acc[g][c * 8 + 0], acc[g][c * 8 + 1], acc[g][c * 8 + 2], acc[g][c * 8 + 3]);
-        dst[1] = make_float4(acc[g][c * 8 + 4], acc[g][c * 8 + 5], acc[g][c * 8 + 6], acc[g][c * 8 + 7]);
-      }
-    if (j == 0) {
-#pragma unroll
-      for (int g = 0; g < G; ++g) {
-        sm_m[gi * G + g] = m_run[g];
-        sm_l[gi * G + g] = l_run[g];
-      }
-    }
-  }
-  __syncthreads();
+// Merge NGRP running states (sm_acc [NGRP][G][D], sm_m / sm_l [NGRP][G], all in
+// shared memory) into this CTA's partial; then either finish directly (a single
+// partial), or publish the partial, arrive, and combine if this CTA arrived last.
+template <typename T, int D, int G, int NGRP, int MODE>
+__device__ __forceinline__ void finish_cta(const Params& p, const Work& wk, float* sm_acc,
+                                           int& sm_last, uint8_t* combine_smem,
+                                           uint32_t combine_bytes, uint32_t combine_bar) {
+  float* sm_m = sm_acc + NGRP * G * D;  // [NGRP][G]
+  float* sm_l = sm_m + NGRP * G;        // [NGRP][G]
+  float* sm_fac = sm_l + NGRP * G;      // [NGRP][G]
+  float* sm_ML = sm_fac + NGRP * G;     // [G][2]
+  const int tid = threadIdx.x;
   if (tid < G) {
     const int g = tid;
     float M = -INFINITY;
@@ -464,24 +499,33 @@ __global__ void __launch_bounds__(kThreads, 2) fd_split_kernel(const __grid_cons
     return;
   }
 
-  // Publish this CTA's partial (O unnormalised w.r.t. M, M, Lambda).
-  for (int idx = tid; idx < G * D; idx += kThreads) {
-    const int g = idx / D, dim = idx - (idx / D) * D;
-    float a = 0.f;
+  // Publish this CTA's partial record (O unnormalised w.r.t. M, then M, Lambda).
+  constexpr int RS = record_floats(D);
+  for (int idx = tid; idx < G * D / 4; idx += kThreads) {
+    const int g = idx / (D / 4), c4 = idx - (idx / (D / 4)) * (D / 4);
+    float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll 4
-    for (int q = 0; q < NGRP; ++q) a = fmaf(sm_acc[(q * G + g) * D + dim], sm_fac[q * G + g], a);
+    for (int q = 0; q < NGRP; ++q) {
+      const float4 x = reinterpret_cast<const float4*>(sm_acc + (q * G + g) * D)[c4];
+      const float f = sm_fac[q * G + g];
+      a.x = fmaf(x.x, f, a.x);
+      a.y = fmaf(x.y, f, a.y);
+      a.z = fmaf(x.z, f, a.z);
+      a.w = fmaf(x.w, f, a.w);
+    }
     const int64_t pidx = wk.pbase + (int64_t)(h0 + g) * wk.wtot + wk.slot;
-    __stcg(p.part_o + pidx * D + dim, a);
+    __stcg(reinterpret_cast<float4*>(p.part + pidx * RS) + c4, a);
   }
   if (tid < G) {
     const int64_t pidx = wk.pbase + (int64_t)(h0 + tid) * wk.wtot + wk.slot;
-    __stcg(p.part_m + pidx, sm_ML[2 * tid]);
-    __stcg(p.part_l + pidx, sm_ML[2 * tid + 1]);
+    __stcg(reinterpret_cast<float4*>(p.part + pidx * RS + D),
+           make_float4(sm_ML[2 * tid], sm_ML[2 * tid + 1], 0.f, 0.f));
   }
   if (MODE == 1) return;
 
-  // Arrival: data first, then the counter (release); the last arriver acquires.
-  __threadfence();
+  // Arrival: the CTA's stores are ordered before thread 0's release by the barrier
+  // (release is cumulative); the acquiring RMW makes every earlier CTA's record
+  // visible to the last arriver, whose threads are ordered after it by the barrier.
   __syncthreads();
   uint32_t* cnt = p.counters + (int64_t)wk.b * p.Hkv + wk.kvh;
   if (tid == 0) {
@@ -491,31 +535,372 @@ __global__ void __launch_bounds__(kThreads, 2) fd_split_kernel(const __grid_cons
   }
   __syncthreads();
   if (!sm_last) return;
-  __threadfence();
-  combine_partials<T, D, G>(p, wk.b, wk.kvh, wk.wtot, wk.pbase, reinterpret_cast<float*>(smem));
+  uint32_t phase = 0;
+  combine_partials<T, D, G>(p, wk.b, wk.kvh, wk.wtot, wk.pbase, combine_smem, combine_bytes,
+                            combine_bar, phase);
   if (tid == 0) *cnt = 0u;
 }
 
+// MODE 0: fused split + last-arriver combine.  MODE 1: split only (partials).
+template <typename T, int D, int G, int PATH, int MODE>
+__global__ void __launch_bounds__(kThreads, 2) fd_split_kernel(const __grid_constant__ Params p) {
+  constexpr int TILE = tile_for(PATH);
+  constexpr int STAGES = stages_for(PATH, D);
+  constexpr int BOXC = box_cols_for(PATH, D);   // columns per TMA box
+  constexpr int NBOX = D / BOXC;                // boxes per tensor per stage
+  constexpr uint32_t kRowsBytes = TILE * D * sizeof(T);
+  constexpr uint32_t kStageBytes = 2 * kRowsBytes;
+  constexpr int NGRP_FFMA = kConsumerWarps * (32 / ((G * D > 512) ? 16 : 8));
+  constexpr int NGRP = PATH == kPathMma ? kConsumerWarps : NGRP_FFMA;
+  static_assert(PATH == kPathFfma || G >= 4, "the MMA path needs G >= 4 heads on N");
+  static_assert(NGRP * G * D * 4 + 4 * NGRP * G * 4 <= STAGES * kStageBytes,
+                "group merge must fit in the ring");
+
+  extern __shared__ uint8_t smem_raw[];
+  // 1024-byte aligned base: the 128-byte swizzle pattern repeats every 1024 bytes.
+  uint8_t* smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + (size_t)STAGES * kStageBytes);
+  int& sm_abort = *reinterpret_cast<int*>(bars + 2 * STAGES + 1);
+  int& sm_last = *(reinterpret_cast<int*>(bars + 2 * STAGES + 1) + 1);
+  auto full_bar = [&](int s) { return smem_addr(bars + s); };
+  auto empty_bar = [&](int s) { return smem_addr(bars + STAGES + s); };
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  pdl_launch_dependents();
+  // Prologue that touches no global memory: it may overlap the previous kernel.
+  const Work wk = decode_work(p, blockIdx.x);
+  const int ntiles = (wk.t1 - wk.t0 + TILE - 1) / TILE;
+  if (tid == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(full_bar(s), 1);
+      mbar_init(empty_bar(s), kConsumerWarps);
+    }
+    mbar_init(smem_addr(bars + 2 * STAGES), 1);  // combine copies
+    fence_mbar_init();
+    sm_abort = 0;
+  }
+  if (warp == kConsumerWarps && lane == 0 && ntiles > 0) {
+    prefetch_tensormap(&p.tm_k);
+    prefetch_tensormap(&p.tm_v);
+  }
+  pdl_wait();  // q, K, V, the workspace and out may come from earlier kernels
+  __syncthreads();
+
+  float* sm_acc = reinterpret_cast<float*>(smem);  // [NGRP][G][D] after the ring drains
+  float* sm_m = sm_acc + NGRP * G * D;
+  float* sm_l = sm_m + NGRP * G;
+
+  if (warp == kConsumerWarps) {
+    // ---------------- TMA producer ----------------
+    if (lane == 0 && ntiles > 0) {
+      const uint64_t policy = l2_evict_first_policy();
+      const int row0 = p.cu[wk.b] + wk.t0;
+      int kt = 0;
+      for (; kt < ntiles; ++kt) {
+        const int s = kt % STAGES;
+        if (kt >= STAGES && !mbar_wait(empty_bar(s), ((kt / STAGES) - 1) & 1)) {
+          atomicOr(p.status, kStatusTimeout);
+          *(volatile int*)&sm_abort = 1;
+          break;
+        }
+        if (*(volatile int*)&sm_abort) break;
+        const uint32_t dst = smem_addr(smem + (size_t)s * kStageBytes);
+        mbar_arrive_expect_tx(full_bar(s), kStageBytes);
+#pragma unroll
+        for (int bx = 0; bx < NBOX; ++bx)
+          tma_load_3d(dst + bx * (TILE * BOXC * 2), &p.tm_k, bx * BOXC, wk.kvh, row0 + kt * TILE,
+                      full_bar(s), policy);
+#pragma unroll
+        for (int bx = 0; bx < NBOX; ++bx)
+          tma_load_3d(dst + kRowsBytes + bx * (TILE * BOXC * 2), &p.tm_v, bx * BOXC, wk.kvh,
+                      row0 + kt * TILE, full_bar(s), policy);
+      }
+      // Every load issued must land before shared memory is reused or released.
+      for (int t = (kt > STAGES ? kt - STAGES : 0); t < kt; ++t) {
+        if (!mbar_wait(full_bar(t % STAGES), (t / STAGES) & 1)) atomicOr(p.status, kStatusTimeout);
+      }
+    }
+    __syncthreads();
+  } else if constexpr (PATH == kPathMma) {
+    // ---------------- MMA consumers ----------------
+    constexpr int KT = D / 16;            // k-steps of S = K Q^T, m-tiles of O^T
+    const int qrow = lane >> 2;           // C/B fragment row (token) or column (head)
+    const int qcol = (lane & 3) * 2;      // C fragment column pair (heads qcol, qcol+1)
+    const int mj = lane >> 3, mr = lane & 7;  // ldmatrix: matrix and row this lane addresses
+    // q as the B operand of S^T = K Q^T: B[k][n] = q[head n][k]; heads >= G are zero.
+    uint32_t qb[KT][2];
+    {
+      const T* qh = reinterpret_cast<const T*>(p.q) + ((int64_t)wk.b * p.Hq + wk.kvh * G + qrow) * D;
+#pragma unroll
+      for (int kk = 0; kk < KT; ++kk) {
+        qb[kk][0] = qrow < G ? *reinterpret_cast<const uint32_t*>(qh + kk * 16 + qcol) : 0u;
+        qb[kk][1] = qrow < G ? *reinterpret_cast<const uint32_t*>(qh + kk * 16 + qcol + 8) : 0u;
+      }
+    }
+    float o[KT][4];
+#pragma unroll
+    for (int mi = 0; mi < KT; ++mi) o[mi][0] = o[mi][1] = o[mi][2] = o[mi][3] = 0.f;
+    float mA = -INFINITY, mB = -INFINITY, lA = 0.f, lB = 0.f;
+    const float scale = p.scale_log2;
+    const int tok0 = warp * 16;
+    const int krow = tok0 + (mj & 1) * 8 + mr;   // K rows this lane addresses (A = K)
+    const int vrow = tok0 + (mj >> 1) * 8 + mr;  // V rows this lane addresses (A = V^T)
+
+    for (int kt = 0; kt < ntiles; ++kt) {
+      const int s = kt % STAGES;
+      const bool ok = mbar_wait(full_bar(s), (kt / STAGES) & 1);
+      if (__any_sync(0xffffffffu, !ok || *(volatile int*)&sm_abort != 0)) {
+        if (!ok) {
+          atomicOr(p.status, kStatusTimeout);
+          *(volatile int*)&sm_abort = 1;
+        }
+        break;
+      }
+      const int ntok = min(TILE, wk.t1 - (wk.t0 + kt * TILE));
+      if (tok0 < ntok) {
+        const uint32_t kbase = smem_addr(smem + (size_t)s * kStageBytes);
+        const uint32_t vbase = kbase + kRowsBytes;
+        float sc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int kk = 0; kk < KT; ++kk) {
+          uint32_t a[4];
+          ldmatrix_x4(a, swz_addr(kbase, TILE, krow, 2 * kk + (mj >> 1)));
+          mma16816<T>(sc, a, qb[kk][0], qb[kk][1]);
+        }
+        const bool v0 = tok0 + qrow < ntok, v1 = tok0 + qrow + 8 < ntok;
+        const float sA0 = v0 ? sc[0] * scale : -INFINITY, sB0 = v0 ? sc[1] * scale : -INFINITY;
+        const float sA1 = v1 ? sc[2] * scale : -INFINITY, sB1 = v1 ? sc[3] * scale : -INFINITY;
+        float xA = fmaxf(sA0, sA1), xB = fmaxf(sB0, sB1);
+#pragma unroll
+        for (int off = 4; off < 32; off <<= 1) {
+          xA = fmaxf(xA, __shfl_xor_sync(0xffffffffu, xA, off));
+          xB = fmaxf(xB, __shfl_xor_sync(0xffffffffu, xB, off));
+        }
+        if (xA > mA + kRescaleThreshold) {
+          const float corr = ex2(mA - xA);
+          lA *= corr;
+#pragma unroll
+          for (int mi = 0; mi < KT; ++mi) { o[mi][0] *= corr; o[mi][2] *= corr; }
+          mA = xA;
+        }
+        if (xB > mB + kRescaleThreshold) {
+          const float corr = ex2(mB - xB);
+          lB *= corr;
+#pragma unroll
+          for (int mi = 0; mi < KT; ++mi) { o[mi][1] *= corr; o[mi][3] *= corr; }
+          mB = xB;
+        }
+        // Row tok0 is valid, so the column maxima (and mA, mB) are finite here.
+        const float pA0 = ex2(sA0 - mA), pB0 = ex2(sB0 - mB);
+        const float pA1 = ex2(sA1 - mA), pB1 = ex2(sB1 - mB);
+        lA += pA0 + pA1;
+        lB += pB0 + pB1;
+        // P (tokens x heads, accumulator layout) -> P^T as the B operand (k = token).
+        const uint32_t pb0 = movmatrix_trans(pack2<T>(pA0, pB0));
+        const uint32_t pb1 = movmatrix_trans(pack2<T>(pA1, pB1));
+#pragma unroll
+        for (int mi = 0; mi < KT; ++mi) {
+          uint32_t a[4];
+          ldmatrix_x4_trans(a, swz_addr(vbase, TILE, vrow, 2 * mi + (mj & 1)));
+          mma16816<T>(o[mi], a, pb0, pb1);
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(empty_bar(s));
+    }
+    // Row sums: lanes sharing a head pair hold partial sums over their tokens.
+#pragma unroll
+    for (int off = 4; off < 32; off <<= 1) {
+      lA += __shfl_xor_sync(0xffffffffu, lA, off);
+      lB += __shfl_xor_sync(0xffffffffu, lB, off);
+    }
+    __syncthreads();  // ring drained: reuse it for the per-warp states
+    if (*(volatile int*)&sm_abort == 0 && qcol < G) {
+      float* accA = sm_acc + (warp * G + qcol) * D;
+      float* accB = accA + D;
+#pragma unroll
+      for (int mi = 0; mi < KT; ++mi) {
+        accA[16 * mi + qrow] = o[mi][0];
+        accB[16 * mi + qrow] = o[mi][1];
+        accA[16 * mi + qrow + 8] = o[mi][2];
+        accB[16 * mi + qrow + 8] = o[mi][3];
+      }
+      if (qrow == 0) {
+        sm_m[warp * G + qcol] = mA;
+        sm_m[warp * G + qcol + 1] = mB;
+        sm_l[warp * G + qcol] = lA;
+        sm_l[warp * G + qcol + 1] = lB;
+      }
+    }
+  } else {
+    // ---------------- FFMA consumers ----------------
+    constexpr int LPT = (G * D > 512) ? 16 : 8;  // lanes per token
+    constexpr int DL = D / LPT;                   // dimensions per lane
+    constexpr int NCH = DL / 8;                   // 16-byte chunks per lane per row
+    constexpr int GPW = 32 / LPT;                 // token groups per warp
+    constexpr int TPG = TILE / NGRP;              // tokens per group per stage
+    static_assert(TILE % NGRP == 0, "tile must split evenly over token groups");
+    const int j = lane % LPT;                     // lane within its token group
+    const int gi = warp * GPW + lane / LPT;       // token group id
+    float acc[G][DL];
+    float m_run[G], l_run[G];
+    const T* qg = reinterpret_cast<const T*>(p.q) + ((int64_t)wk.b * p.Hq + wk.kvh * G) * D;
+    float qf[G][DL];
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+#pragma unroll
+      for (int c = 0; c < NCH; ++c) {
+        const uint4 raw = *reinterpret_cast<const uint4*>(qg + g * D + (j + LPT * c) * 8);
+        unpack8<T>(raw, &qf[g][c * 8]);
+      }
+#pragma unroll
+      for (int e = 0; e < DL; ++e) qf[g][e] *= p.scale_log2;
+    }
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+      m_run[g] = -INFINITY;
+      l_run[g] = 0.f;
+#pragma unroll
+      for (int e = 0; e < DL; ++e) acc[g][e] = 0.f;
+    }
+
+    for (int kt = 0; kt < ntiles; ++kt) {
+      const int s = kt % STAGES;
+      // Every lane waits; the warp leaves together so shuffles never see a partial warp.
+      const bool ok = mbar_wait(full_bar(s), (kt / STAGES) & 1);
+      if (__any_sync(0xffffffffu, !ok || *(volatile int*)&sm_abort != 0)) {
+        if (!ok) {
+          atomicOr(p.status, kStatusTimeout);
+          *(volatile int*)&sm_abort = 1;
+        }
+        break;
+      }
+      const int ntok = min(TILE, wk.t1 - (wk.t0 + kt * TILE));
+      const T* Ks = reinterpret_cast<const T*>(smem + (size_t)s * kStageBytes);
+      const T* Vs = Ks + TILE * D;
+
+      float sc[TPG][G];
+#pragma unroll
+      for (int r = 0; r < TPG; ++r) {
+        const int tok = gi + NGRP * r;
+        float part[G];
+#pragma unroll
+        for (int g = 0; g < G; ++g) part[g] = 0.f;
+        if (tok < ntok) {
+#pragma unroll
+          for (int c = 0; c < NCH; ++c) {
+            const uint4 raw = *reinterpret_cast<const uint4*>(Ks + tok * D + (j + LPT * c) * 8);
+            float kf[8];
+            unpack8<T>(raw, kf);
+#pragma unroll
+            for (int g = 0; g < G; ++g)
+#pragma unroll
+              for (int e = 0; e < 8; ++e) part[g] = fmaf(qf[g][c * 8 + e], kf[e], part[g]);
+          }
+        }
+#pragma unroll
+        for (int off = 1; off < LPT; off <<= 1)
+#pragma unroll
+          for (int g = 0; g < G; ++g) part[g] += __shfl_xor_sync(0xffffffffu, part[g], off);
+#pragma unroll
+        for (int g = 0; g < G; ++g) sc[r][g] = (tok < ntok) ? part[g] : -INFINITY;
+      }
+
+      float pr[TPG][G];
+#pragma unroll
+      for (int g = 0; g < G; ++g) {
+        float mx = sc[0][g];
+#pragma unroll
+        for (int r = 1; r < TPG; ++r) mx = fmaxf(mx, sc[r][g]);
+        if (mx > m_run[g] + kRescaleThreshold) {
+          const float corr = ex2(m_run[g] - mx);
+          l_run[g] *= corr;
+#pragma unroll
+          for (int e = 0; e < DL; ++e) acc[g][e] *= corr;
+          m_run[g] = mx;
+        }
+#pragma unroll
+        for (int r = 0; r < TPG; ++r) {
+          pr[r][g] = (gi + NGRP * r < ntok) ? ex2(sc[r][g] - m_run[g]) : 0.f;
+          l_run[g] += pr[r][g];
+        }
+      }
+
+#pragma unroll
+      for (int r = 0; r < TPG; ++r) {
+        const int tok = gi + NGRP * r;
+        if (tok < ntok) {
+#pragma unroll
+          for (int c = 0; c < NCH; ++c) {
+            const uint4 raw = *reinterpret_cast<const uint4*>(Vs + tok * D + (j + LPT * c) * 8);
+            float vf[8];
+            unpack8<T>(raw, vf);
+#pragma unroll
+            for (int g = 0; g < G; ++g)
+#pragma unroll
+              for (int e = 0; e < 8; ++e) acc[g][c * 8 + e] = fmaf(pr[r][g], vf[e], acc[g][c * 8 + e]);
+          }
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(empty_bar(s));
+    }
+    __syncthreads();  // ring drained: reuse it for the per-group states
+    if (*(volatile int*)&sm_abort == 0) {
+#pragma unroll
+      for (int g = 0; g < G; ++g)
+#pragma unroll
+        for (int c = 0; c < NCH; ++c) {
+          float4* dst = reinterpret_cast<float4*>(sm_acc + (gi * G + g) * D + (j + LPT * c) * 8);
+          dst[0] = make_float4(acc[g][c * 8 + 0], acc[g][c * 8 + 1], acc[g][c * 8 + 2], acc[g][c * 8 + 3]);
+          dst[1] = make_float4(acc[g][c * 8 + 4], acc[g][c * 8 + 5], acc[g][c * 8 + 6], acc[g][c * 8 + 7]);
+        }
+      if (j == 0) {
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+          sm_m[gi * G + g] = m_run[g];
+          sm_l[gi * G + g] = l_run[g];
+        }
+      }
+    }
+  }
+  __syncthreads();
+  if (sm_abort) return;
+  finish_cta<T, D, G, NGRP, MODE>(p, wk, sm_acc, sm_last, smem, STAGES * kStageBytes,
+                                  smem_addr(bars + 2 * STAGES));
+}
+
 // Two-launch ablation, second kernel: one CTA per (sequence, KV head) combines
-// the partials written by fd_split_kernel<..., 1>.
-template <typename T, int D, int G>
+// the partials written by fd_split_kernel<..., MODE = 1>.
+template <typename T, int D, int G, int PATH>
 __global__ void __launch_bounds__(kThreads, 2) fd_combine_kernel(const __grid_constant__ Params p) {
-  extern __shared__ __align__(1024) uint8_t smem[];
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
+  constexpr uint32_t kBytes = (uint32_t)ring_bytes_for(PATH, D);
+  uint64_t* bar = reinterpret_cast<uint64_t*>(smem + kBytes);
+  pdl_launch_dependents();
+  if (threadIdx.x == 0) {
+    mbar_init(smem_addr(bar), 1);
+    fence_mbar_init();
+  }
+  pdl_wait();
+  __syncthreads();
   const int b = blockIdx.x / p.Hkv, kvh = blockIdx.x - (blockIdx.x / p.Hkv) * p.Hkv;
   const int wtot = (p.unit_base[b + 1] - p.unit_base[b]) / p.Hkv;
   const int64_t pbase = (int64_t)(p.unit_base[b] / p.Hkv) * p.Hq;
-  combine_partials<T, D, G>(p, b, kvh, wtot, pbase, reinterpret_cast<float*>(smem));
+  uint32_t phase = 0;
+  combine_partials<T, D, G>(p, b, kvh, wtot, pbase, smem, kBytes, smem_addr(bar), phase);
 }
 
 }  // namespace dev
 
-template <typename T, int D, int G>
-cudaError_t launch_dg(const Params& p, int mode, int grid, cudaStream_t stream) {
-  const size_t smem = smem_bytes_for(D);
+template <typename T, int D, int G, int PATH>
+cudaError_t launch_dgp(const Params& p, int mode, bool pdl, int grid, cudaStream_t stream) {
+  const size_t smem = smem_bytes_for(PATH, D);
   const void* fn;
-  if (mode == 0) fn = reinterpret_cast<const void*>(&dev::fd_split_kernel<T, D, G, 0>);
-  else if (mode == 1) fn = reinterpret_cast<const void*>(&dev::fd_split_kernel<T, D, G, 1>);
-  else fn = reinterpret_cast<const void*>(&dev::fd_combine_kernel<T, D, G>);
+  if (mode == 0) fn = reinterpret_cast<const void*>(&dev::fd_split_kernel<T, D, G, PATH, 0>);
+  else if (mode == 1) fn = reinterpret_cast<const void*>(&dev::fd_split_kernel<T, D, G, PATH, 1>);
+  else fn = reinterpret_cast<const void*>(&dev::fd_combine_kernel<T, D, G, PATH>);
   int dev_id = 0;
   cudaError_t err = cudaGetDevice(&dev_id);
   if (err != cudaSuccess) return err;
@@ -528,15 +913,29 @@ cudaError_t launch_dg(const Params& p, int mode, int grid, cudaStream_t stream) 
     __atomic_fetch_or(&done_mask[mode], bit, __ATOMIC_RELEASE);
   }
   void* args[] = {const_cast<Params*>(&p)};
-  return cudaLaunchKernel(fn, dim3(grid), dim3(kThreads), args, smem, stream);
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelExC(&cfg, fn, args);
 }
 
 template <typename T>
-cudaError_t launch_typed(const Params& p, int d, int G, int mode, int grid, cudaStream_t s) {
-#define FD_CASE(DD, GG) \
-  if (d == DD && G == GG) return launch_dg<T, DD, GG>(p, mode, grid, s);
-  FD_CASE(64, 1) FD_CASE(64, 2) FD_CASE(64, 4) FD_CASE(64, 8)
-  FD_CASE(128, 1) FD_CASE(128, 2) FD_CASE(128, 4) FD_CASE(128, 8)
+cudaError_t launch_typed(const Params& p, int d, int G, int path, int mode, bool pdl, int grid,
+                         cudaStream_t s) {
+#define FD_CASE(DD, GG, PP) \
+  if (d == DD && G == GG && path == PP) return launch_dgp<T, DD, GG, PP>(p, mode, pdl, grid, s);
+  FD_CASE(64, 1, kPathFfma) FD_CASE(64, 2, kPathFfma) FD_CASE(64, 4, kPathFfma)
+  FD_CASE(64, 8, kPathFfma) FD_CASE(128, 1, kPathFfma) FD_CASE(128, 2, kPathFfma)
+  FD_CASE(128, 4, kPathFfma) FD_CASE(128, 8, kPathFfma)
+  FD_CASE(64, 4, kPathMma) FD_CASE(64, 8, kPathMma) FD_CASE(128, 4, kPathMma)
+  FD_CASE(128, 8, kPathMma)
 #undef FD_CASE
   return cudaErrorInvalidValue;
 }

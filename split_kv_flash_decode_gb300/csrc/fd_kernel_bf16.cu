@@ -2,7 +2,8 @@
 #include "fd_kernel.cuh"
 
 namespace fd {
-cudaError_t launch_bf16(const Params& p, int d, int G, int mode, int grid, cudaStream_t s) {
-  return launch_typed<__nv_bfloat16>(p, d, G, mode, grid, s);
+cudaError_t launch_bf16(const Params& p, int d, int G, int path, int mode, bool pdl, int grid,
+                        cudaStream_t s) {
+  return launch_typed<__nv_bfloat16>(p, d, G, path, mode, pdl, grid, s);
 }
 }  // namespace fd

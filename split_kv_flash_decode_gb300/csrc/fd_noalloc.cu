@@ -74,20 +74,20 @@ extern "C" int fd_decode_noalloc(fd_plan_t pl, const void* q, const void* k, con
   p.lse = lse;
   p.status = reinterpret_cast<uint32_t*>(ws);
   p.counters = reinterpret_cast<uint32_t*>(ws + pl->off_counters);
-  p.part_m = reinterpret_cast<float*>(ws + pl->off_m);
-  p.part_l = reinterpret_cast<float*>(ws + pl->off_l);
-  p.part_o = reinterpret_cast<float*>(ws + pl->off_o);
+  p.part = reinterpret_cast<float*>(ws + pl->off_part);
 
   // The array keeps whatever the previous call left: the status word and the
   // arrival counters must start at zero, so clear them on the stream first.
-  cudaError_t err = cudaMemsetAsync(ws, 0, pl->off_m, stream);
+  cudaError_t err = cudaMemsetAsync(ws, 0, pl->off_part, stream);
   if (err == cudaSuccess) {
     auto launch = pl->dtype == FD_F16 ? fd::launch_f16 : fd::launch_bf16;
+    const bool pdl = !(pl->flags & FD_PLAN_NO_PDL);
     if (pl->flags & FD_PLAN_TWO_LAUNCH) {
-      err = launch(p, pl->d, pl->G, 1, pl->ctas, stream);
-      if (err == cudaSuccess) err = launch(p, pl->d, pl->G, 2, pl->B * pl->Hkv, stream);
+      err = launch(p, pl->d, pl->G, pl->path, 1, pdl, pl->ctas, stream);
+      if (err == cudaSuccess)
+        err = launch(p, pl->d, pl->G, pl->path, 2, pdl, pl->B * pl->Hkv, stream);
     } else {
-      err = launch(p, pl->d, pl->G, 0, pl->ctas, stream);
+      err = launch(p, pl->d, pl->G, pl->path, 0, pdl, pl->ctas, stream);
     }
   }
   if (err != cudaSuccess) {

@@ -7,12 +7,13 @@ struct fd_plan_s {
   int B, Hq, Hkv, d, G, dtype;
   uint32_t flags;
   int C;
+  int path;  // fd::kPathFfma or fd::kPathMma
   int num_sms;
   int max_partials;
   int64_t n_tokens;
   int64_t total_partials;
   int ctas;
-  size_t off_counters, off_m, off_l, off_o, ws_bytes;
+  size_t off_counters, off_part, ws_bytes;
   fd::Params params;  // pointers filled per call; arrays and scalars filled by fd_plan
 };
 

@@ -153,6 +153,15 @@ def test_literal_w_and_auto_chunks():
     assert p.info["chunks"] == 1
 
 
+def test_consumer_path_choice():
+    # tensor cores once the GQA group fills at least half of the mma N = 8 tile
+    for G, path in ((1, 0), (2, 0), (4, 1), (8, 1)):
+        p = fd.fd_plan(1, 8 * G, 8, 128, [1000], 2, "f16", num_sms=152)
+        assert p.info["path"] == path, G
+    p = fd.fd_plan(1, 64, 8, 128, [1000], 2, "bf16", flags=fd.FD_PLAN_FFMA, num_sms=152)
+    assert p.info["path"] == 0
+
+
 def test_workspace_layout():
     p = fd.fd_plan(3, 8, 2, 64, [10, 0, 700], [1, 2, 5], "f16", chunks=2, num_sms=152)
     P = 8 * (1 + 2 + 5) * 2

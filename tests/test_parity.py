@@ -137,6 +137,16 @@ def test_edge_lengths(fd, dtype, d, G):
         check(out, lse, ref_out, ref_lse, dtype=dtype)
 
 
+@pytest.mark.parametrize("G", [4, 8])
+def test_forced_ffma_path(fd, G):
+    """The CUDA-core consumers stay correct for the groups the tensor-core path serves."""
+    p = workloads.make_problem("ffma", 2, 8 * G, 8, 128, [3000, 77], [3, 5], "f16", seed=20 + G)
+    ref_out, ref_lse = oracle.decode_reference(p.q, p.k, p.v, p.seqlens, p.dtype)
+    (out, lse), dec = run_gpu(fd, p, flags=fd.FD_PLAN_FFMA)
+    assert dec.info["path"] == 0
+    check(out, lse, ref_out, ref_lse, dtype=p.dtype)
+
+
 def test_ragged_with_empty_sequences(fd):
     lens = [0, 700, 0, 1, 4096, 0]
     p = workloads.make_problem("ragged_empty", 6, 16, 4, 128, lens, [1, 3, 5, 2, 4, 1], "f16", seed=11)
@@ -185,6 +195,14 @@ def test_two_launch_matches_fused(fd):
     (o1, l1), _ = run_gpu(fd, p)
     (o2, l2), _ = run_gpu(fd, p, flags=fd.FD_PLAN_TWO_LAUNCH)
     check(o2, l2, ref_out, ref_lse, dtype=p.dtype)
+    assert np.array_equal(o1, o2) and np.array_equal(l1, l2)
+
+
+def test_pdl_off_matches_pdl_on(fd):
+    """Programmatic dependent launch changes scheduling only, never the numbers."""
+    p = workloads.make_problem("pdl", 2, 32, 8, 128, [6000, 999], [4, 3], "f16", seed=18)
+    (o1, l1), _ = run_gpu(fd, p, repeat=1)
+    (o2, l2), _ = run_gpu(fd, p, flags=fd.FD_PLAN_NO_PDL)
     assert np.array_equal(o1, o2) and np.array_equal(l1, l2)
 
 
