@@ -275,6 +275,33 @@ def run_reference(args):
 # GPU arm.
 # ---------------------------------------------------------------------------
 
+KERNEL_SOURCES = ("split_kv_flash_decode_gb300/csrc/fd_kernel.cuh",
+                  "split_kv_flash_decode_gb300/csrc/fd_common.h")
+
+
+def kernel_source_hash() -> str:
+    import hashlib
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def load_traffic(workload: str, kernel: str):
+    """DRAM bytes (read + write) per launch from a committed ncu capture of this
+    kernel on this workload; None when there is none or the kernel changed since."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            entry = json.load(f).get(workload, {}).get(kernel)
+    except (OSError, ValueError):
+        return None
+    if not entry or entry.get("kernel_source_sha256_16") != kernel_source_hash():
+        return None
+    return int(entry["dram__bytes_read.sum"]) + int(entry["dram__bytes_write.sum"])
+
+
 def load_peak():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -433,8 +460,10 @@ def run_fd(args):
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = run_cpu_baseline_subprocess(args)
 
+    info = dec.info
+    kernel_label = ("fd_split_kernel+fd_combine_kernel" if args.two_launch else "fd_split_kernel") + (
+        "/mma" if info["path"] == 1 else "/ffma")
     if rank == 0:
-        info = dec.info
         line = {
             "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": K,
             "warmup": Wm, "ms_per_step": agg["elapsed_s"] * 1e3 / K, "higher_is_better": True,
@@ -459,11 +488,13 @@ def run_fd(args):
                            "what": "one decode, CUDA events around each launch (second replay)"},
             "step_us": step_us,
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                         "frac": achieved / peak, "traffic": None,
+                         "frac": achieved / peak,
+                         "traffic": load_traffic(prob.name, kernel_label),
+                         "traffic_unit": "bytes per launch (ncu dram read + write)",
+                         "algorithmic_bytes": kv_bytes,
                          "achieved_from": "KV bytes per launch / (timed-region time / K)",
                          "peak_kind": f"{peak_kind} (hbm_gbs copy, burst)",
-                         "kernel": "fd_split_kernel (fused)" if not args.two_launch
-                         else "fd_split_kernel + fd_combine_kernel"},
+                         "kernel": kernel_label},
             "e2e": e2e, "e2e_resident_kv": e2e_res,
             "gpu_launches": K * launches_per_step,
             "clocks": clocks, "cpu_baseline": cpu,
