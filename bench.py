@@ -50,6 +50,8 @@ def parse_args(argv=None):
     ap.add_argument("--two-launch", action="store_true", help="split + combine as two kernels")
     ap.add_argument("--ffma", action="store_true", help="CUDA-core consumers even when G >= 4")
     ap.add_argument("--no-pdl", action="store_true", help="launch without programmatic dependent launch")
+    ap.add_argument("--waits", action="store_true",
+                    help="fine-grained waits: slot 0 combines partials as their flags arrive")
     ap.add_argument("--soak-s", type=float, default=1.5, help="untimed load before timing (clocks)")
     ap.add_argument("--e2e-steps", type=int, default=30)
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -343,7 +345,7 @@ def run_fd(args):
 
     flags = (fd.FD_PLAN_LITERAL_W if prob.literal_w else 0) | (
         fd.FD_PLAN_TWO_LAUNCH if args.two_launch else 0) | (fd.FD_PLAN_FFMA if args.ffma else 0) | (
-        fd.FD_PLAN_NO_PDL if args.no_pdl else 0)
+        fd.FD_PLAN_NO_PDL if args.no_pdl else 0) | (fd.FD_PLAN_WAITS if args.waits else 0)
     dec = fd.Decoder(prob.Hq, prob.Hkv, prob.d, prob.seqlens, prob.W, prob.dtype, flags=flags,
                      chunks=args.chunks, device=device)
     q = to_device(prob.q, prob.dtype, device)
@@ -462,7 +464,7 @@ def run_fd(args):
 
     info = dec.info
     kernel_label = ("fd_split_kernel+fd_combine_kernel" if args.two_launch else "fd_split_kernel") + (
-        "/mma" if info["path"] == 1 else "/ffma")
+        "/mma" if info["path"] == 1 else "/ffma") + ("/waits" if args.waits else "")
     if rank == 0:
         line = {
             "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": K,
@@ -474,7 +476,10 @@ def run_fd(args):
                 "chunks_per_segment": info["chunks"], "ctas": info["ctas"],
                 "partials_per_sequence_max": info["max_partials"],
                 "kv_bytes_per_step": kv_bytes, "two_launch": bool(args.two_launch),
-                "pdl": not args.no_pdl,
+                "pdl": not args.no_pdl and not args.waits,
+                "combine": "fine-grained waits (slot 0 combines as flags arrive)" if args.waits
+                           else ("separate combine kernel" if args.two_launch
+                                 else "last arriver (atomic counter)"),
                 "consumer": "mma.sync m16n8k16 (tensor cores)" if info["path"] == 1
                             else "FFMA (CUDA cores)",
                 "l2_policy": f"K/V rotated over {copies} device copies ({copies * kv_bytes / 1e6:.0f} MB"

@@ -65,6 +65,15 @@ enum fd_status {
 #define FD_PLAN_TWO_LAUNCH 0x4u /* split kernel + separate combine kernel (ablation) */
 #define FD_PLAN_FFMA 0x8u       /* CUDA-core scores and P.V even when G >= 4 (ablation) */
 #define FD_PLAN_NO_PDL 0x10u    /* launch without programmatic dependent launch (ablation) */
+/* Fine-grained waits (the pages' V3 reading): partial slot 0 of every (sequence,
+ * KV head) waits on per-partial ready flags and combines partials as they arrive.
+ * Cooperative launch: FD_ERR_UNSUPPORTED when the grid cannot be co-resident.
+ * The combine order follows arrival, so results are not bitwise reproducible. */
+#define FD_PLAN_WAITS 0x20u
+/* Test hook for FD_PLAN_WAITS: partial slot 1 of (sequence 0, KV head 0) never
+ * sets its flag, so that combiner's bounded wait runs out (~1 s) and the status
+ * word reports FD_ERR_TIMEOUT.  Its out/lse are left unwritten. */
+#define FD_PLAN_TEST_DROP_FLAG 0x40u
 
 /* Compiled limits. */
 #define FD_MAX_BATCH 256       /* sequences per plan */
@@ -100,12 +109,13 @@ int fd_plan(int B, int Hq, int Hkv, int d, const int32_t* seqlens, const int32_t
 /* Release a plan (NULL is accepted).  No CUDA call. */
 int fd_plan_destroy(fd_plan_t plan);
 
-/* Bytes of device workspace fd_decode needs for this plan: the fp32 partials
- * O [P, d], m [P], l [P] (P = Hq * sum_b W_b * C), one uint32 arrival counter per
- * (sequence, KV head) and a status word.  0 for a NULL plan. */
+/* Bytes of device workspace fd_decode needs for this plan: a status word, one
+ * uint32 arrival counter per (sequence, KV head), one uint32 ready flag per CTA,
+ * and the fp32 partial records [P][d + 4] (O, m, l; P = Hq * sum_b W_b * C).
+ * 0 for a NULL plan. */
 size_t fd_workspace_bytes(fd_plan_t plan);
 
-/* Zero the workspace's counters and status word on `stream` (asynchronous).
+/* Zero the workspace's counters, flags and status word on `stream` (asynchronous).
  * A workspace must be zeroed once before its first fd_decode (torch.zeros or
  * this call); fd_decode leaves every counter at zero when it completes. */
 int fd_workspace_init(fd_plan_t plan, void* workspace, cudaStream_t stream);

@@ -29,6 +29,8 @@ FD_PLAN_DEBUG = 0x2
 FD_PLAN_TWO_LAUNCH = 0x4
 FD_PLAN_FFMA = 0x8
 FD_PLAN_NO_PDL = 0x10
+FD_PLAN_WAITS = 0x20
+FD_PLAN_TEST_DROP_FLAG = 0x40
 FD_MAX_BATCH = 256
 FD_MAX_PARTIALS = 1024
 

@@ -102,8 +102,10 @@ int fd_plan(int B, int Hq, int Hkv, int d, const int32_t* seqlens, const int32_t
   if (Hq % Hkv != 0) return FD_ERR_INVALID;
   if (dtype != FD_F16 && dtype != FD_BF16) return FD_ERR_INVALID;
   if (flags & ~(FD_PLAN_LITERAL_W | FD_PLAN_DEBUG | FD_PLAN_TWO_LAUNCH | FD_PLAN_FFMA |
-                FD_PLAN_NO_PDL))
+                FD_PLAN_NO_PDL | FD_PLAN_WAITS | FD_PLAN_TEST_DROP_FLAG))
     return FD_ERR_INVALID;
+  if ((flags & FD_PLAN_WAITS) && (flags & FD_PLAN_TWO_LAUNCH)) return FD_ERR_INVALID;
+  if ((flags & FD_PLAN_TEST_DROP_FLAG) && !(flags & FD_PLAN_WAITS)) return FD_ERR_INVALID;
   const int G = Hq / Hkv;
   if (B > FD_MAX_BATCH) return FD_ERR_UNSUPPORTED;
   if (d != 64 && d != 128) return FD_ERR_UNSUPPORTED;
@@ -173,10 +175,12 @@ int fd_plan(int B, int Hq, int Hkv, int d, const int32_t* seqlens, const int32_t
   p.cu[B] = cu;
   p.unit_base[B] = ub;
 
-  // Workspace: status | counters | partial records [P][d + 4] (each 256-byte aligned).
+  // Workspace: status | counters | flags | partial records [P][d + 4] (each 256-byte aligned).
   size_t off = kAlign;
   pl->off_counters = off;
   off = align_up(off + sizeof(uint32_t) * (size_t)B * Hkv);
+  pl->off_flags = off;
+  off = align_up(off + sizeof(uint32_t) * (size_t)pl->ctas);
   pl->off_part = off;
   off = align_up(off + sizeof(float) * (size_t)pl->total_partials * fd::record_floats(d));
   pl->ws_bytes = off;
@@ -262,6 +266,8 @@ int fd_decode(fd_plan_t pl, const void* q, const void* k, const void* v, void* o
   p.status = reinterpret_cast<uint32_t*>(ws);
   p.counters = reinterpret_cast<uint32_t*>(ws + pl->off_counters);
   p.part = reinterpret_cast<float*>(ws + pl->off_part);
+  p.flags = reinterpret_cast<uint32_t*>(ws + pl->off_flags);
+  p.drop_flag = (pl->flags & FD_PLAN_TEST_DROP_FLAG) ? 1 : 0;
 
   const bool debug = (pl->flags & FD_PLAN_DEBUG) != 0;
   if (debug) {
@@ -281,11 +287,11 @@ int fd_decode(fd_plan_t pl, const void* q, const void* k, const void* v, void* o
     err = launch(pl, p, 1, pl->ctas, stream);
     if (err == cudaSuccess) err = launch(pl, p, 2, pl->B * pl->Hkv, stream);
   } else {
-    err = launch(pl, p, 0, pl->ctas, stream);
+    err = launch(pl, p, (pl->flags & FD_PLAN_WAITS) ? 3 : 0, pl->ctas, stream);
   }
   if (err != cudaSuccess) {
     cudaGetLastError();
-    return FD_ERR_CUDA;
+    return err == cudaErrorCooperativeLaunchTooLarge ? FD_ERR_UNSUPPORTED : FD_ERR_CUDA;
   }
   if (debug) {
     int32_t st = FD_OK;

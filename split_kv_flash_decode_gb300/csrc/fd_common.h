@@ -57,7 +57,9 @@ struct Params {
   float* lse;        // [B, Hq] or nullptr
   float* part;       // [P, d + 4] records: O[0..d), m, l, 0, 0 (m in the log2 domain)
   uint32_t* counters;  // [B * Hkv]
+  uint32_t* flags;     // [CTAs] per-partial ready flags (fine-grained-waits variant)
   uint32_t* status;    // 1 word
+  int32_t drop_flag;   // test hook: partial slot 1 of (b=0, kvh=0) never sets its flag
   float scale_log2;    // log2(e) / sqrt(d)
   int32_t B, Hq, Hkv, C;
   int32_t cu[FD_MAX_BATCH + 1];         // token prefix sums
@@ -85,7 +87,9 @@ FD_HD void chunk_range(int L, int W, int C, int slot, int* t0, int* t1) {
 }
 
 // Launchers defined in the per-dtype kernel translation units.
-// mode 0: fused split + last-arriver combine; 1: split only (partials); 2: combine only.
+// mode 0: fused split + last-arriver combine; 1: split only (partials); 2: combine only;
+// 3: fused split + fine-grained waits (slot 0 combines partials as their flags arrive;
+//    cooperative launch).
 // pdl: launch with programmatic stream serialization (the kernel waits on its
 // predecessors with griddepcontrol.wait before touching global memory).
 cudaError_t launch_f16(const Params& p, int d, int G, int path, int mode, bool pdl, int grid,

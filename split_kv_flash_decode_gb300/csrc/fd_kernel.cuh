@@ -132,6 +132,16 @@ __device__ __forceinline__ uint32_t atom_add_acq_rel_gpu(uint32_t* addr, uint32_
   return old;
 }
 
+__device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t* addr) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(addr) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void st_release_gpu(uint32_t* addr, uint32_t v) {
+  asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(addr), "r"(v) : "memory");
+}
+
 __device__ __forceinline__ float ex2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
@@ -453,6 +463,115 @@ __device__ __forceinline__ void combine_partials(const Params& p, int b, int kvh
   }
 }
 
+// Fine-grained waits (the pages' "combine each partial as it arrives"): the CTA
+// of slot 0 of (b, kvh) polls the ready flags of all Wtot partials and folds every
+// batch that has arrived into a running (M, Lambda, O), in arrival order.  The
+// whole grid is co-resident (cooperative launch), so every producer can finish;
+// the poll is still bounded and reports a timeout through the status word.
+// `sm` provides G * (D + 2) + 2 * wtot + G * wtot + 4 floats of scratch.
+template <typename T, int D, int G>
+__device__ __forceinline__ void combine_as_arrived(const Params& p, const Work& wk, float* sm) {
+  constexpr int RS = record_floats(D);
+  const int wtot = wk.wtot;
+  float* run_O = sm;                       // [G][D]
+  float* run_M = run_O + G * D;            // [G]
+  float* run_L = run_M + G;                // [G]
+  float* coef = run_L + G;                 // [G][wtot] (this batch)
+  float* scl = coef + G * wtot;            // [G]
+  int* ready = reinterpret_cast<int*>(scl + G);  // [wtot] slots of this batch
+  int* done = ready + wtot;                // [wtot]
+  int* ctl = done + wtot;                  // [0] batch size, [1] stop
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  constexpr int kWarps = kThreads / 32;
+  const int fbase = p.unit_base[wk.b] + wk.kvh;  // flag of slot w: fbase + w * Hkv
+  for (int i = tid; i < G * D; i += kThreads) run_O[i] = 0.f;
+  for (int g = tid; g < G; g += kThreads) { run_M[g] = -INFINITY; run_L[g] = 0.f; }
+  for (int w = tid; w < wtot; w += kThreads) done[w] = 0;
+  if (tid == 0) ctl[1] = 0;
+  __syncthreads();
+  const uint64_t start = global_timer_ns();
+  int merged = 0;
+  while (merged < wtot) {
+    if (tid == 0) ctl[0] = 0;
+    __syncthreads();
+    for (int w = tid; w < wtot; w += kThreads) {
+      if (!done[w] && (w == wk.slot || ld_acquire_gpu(p.flags + fbase + w * p.Hkv) != 0u)) {
+        done[w] = 1;
+        ready[atomicAdd(&ctl[0], 1)] = w;
+      }
+    }
+    if (tid == 0 && global_timer_ns() - start > kWaitLimitNs) ctl[1] = 1;
+    __syncthreads();
+    const int n = ctl[0];
+    if (n == 0) {
+      if (ctl[1]) {
+        if (tid == 0) atomicOr(p.status, kStatusTimeout);
+        break;
+      }
+      continue;
+    }
+    // (M, Lambda) update per head for this batch.
+    for (int g = warp; g < G; g += kWarps) {
+      const int64_t row = wk.pbase + (int64_t)(wk.kvh * G + g) * wtot;
+      float mx = -INFINITY;
+      for (int i = lane; i < n; i += 32)
+        mx = fmaxf(mx, __ldcg(p.part + (row + ready[i]) * RS + D));
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+      const float Mold = run_M[g];
+      const float Mnew = fmaxf(Mold, mx);
+      float lam = 0.f;
+      for (int i = lane; i < n; i += 32) {
+        const float2 ml = __ldcg(reinterpret_cast<const float2*>(p.part + (row + ready[i]) * RS + D));
+        const float c = (ml.x == -INFINITY) ? 0.f : ex2(ml.x - Mnew);
+        coef[g * wtot + i] = c;
+        lam = fmaf(c, ml.y, lam);
+      }
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) lam += __shfl_xor_sync(0xffffffffu, lam, off);
+      if (lane == 0) {
+        const float sc = (Mold == -INFINITY) ? 0.f : ex2(Mold - Mnew);
+        scl[g] = sc;
+        run_L[g] = fmaf(run_L[g], sc, lam);
+        run_M[g] = Mnew;
+      }
+    }
+    __syncthreads();
+    for (int v = tid; v < G * (D / 4); v += kThreads) {
+      const int g = v / (D / 4), c4 = v - (v / (D / 4)) * (D / 4);
+      const int64_t row = wk.pbase + (int64_t)(wk.kvh * G + g) * wtot;
+      float4 a = reinterpret_cast<float4*>(run_O + g * D)[c4];
+      const float sc = scl[g];
+      a.x *= sc; a.y *= sc; a.z *= sc; a.w *= sc;
+      for (int i = 0; i < n; ++i) {
+        const float4 x = __ldcg(reinterpret_cast<const float4*>(p.part + (row + ready[i]) * RS) + c4);
+        const float c = coef[g * wtot + i];
+        a.x = fmaf(c, x.x, a.x);
+        a.y = fmaf(c, x.y, a.y);
+        a.z = fmaf(c, x.z, a.z);
+        a.w = fmaf(c, x.w, a.w);
+      }
+      reinterpret_cast<float4*>(run_O + g * D)[c4] = a;
+    }
+    merged += n;
+    __syncthreads();
+  }
+  // Flags go back to zero for the next decode (the ones that were set).
+  for (int w = tid; w < wtot; w += kThreads)
+    if (done[w] && w != wk.slot) p.flags[fbase + w * p.Hkv] = 0u;
+  if (merged < wtot) return;  // timed out: status is set, out is not written
+  T* out = reinterpret_cast<T*>(p.out);
+  for (int v = tid; v < G * (D / 4); v += kThreads) {
+    const int g = v / (D / 4), c4 = v - (v / (D / 4)) * (D / 4);
+    store_out4<T>(out + ((int64_t)wk.b * p.Hq + wk.kvh * G + g) * D + 4 * c4,
+                  reinterpret_cast<float4*>(run_O + g * D)[c4], run_L[g]);
+  }
+  if (tid < G && p.lse != nullptr) {
+    const float M = run_M[tid], lam = run_L[tid];
+    p.lse[(int64_t)wk.b * p.Hq + wk.kvh * G + tid] = lam > 0.f ? (M + log2f(lam)) * kLn2 : -INFINITY;
+  }
+}
+
 // Merge NGRP running states (sm_acc [NGRP][G][D], sm_m / sm_l [NGRP][G], all in
 // shared memory) into this CTA's partial; then either finish directly (a single
 // partial), or publish the partial, arrive, and combine if this CTA arrived last.
@@ -481,7 +600,7 @@ __device__ __forceinline__ void finish_cta(const Params& p, const Work& wk, floa
   __syncthreads();
 
   const int h0 = wk.kvh * G;
-  if (MODE == 0 && wk.wtot == 1) {
+  if ((MODE == 0 || MODE == 3) && wk.wtot == 1) {
     // A single partial is already the answer: normalise and store.
     T* out = reinterpret_cast<T*>(p.out);
     for (int idx = tid; idx < G * D; idx += kThreads) {
@@ -522,6 +641,16 @@ __device__ __forceinline__ void finish_cta(const Params& p, const Work& wk, floa
            make_float4(sm_ML[2 * tid], sm_ML[2 * tid + 1], 0.f, 0.f));
   }
   if (MODE == 1) return;
+  if (MODE == 3) {
+    __syncthreads();
+    if (wk.slot != 0) {
+      const bool dropped = p.drop_flag && wk.b == 0 && wk.kvh == 0 && wk.slot == 1;
+      if (tid == 0 && !dropped) st_release_gpu(p.flags + blockIdx.x, 1u);
+      return;
+    }
+    combine_as_arrived<T, D, G>(p, wk, reinterpret_cast<float*>(combine_smem));
+    return;
+  }
 
   // Arrival: the CTA's stores are ordered before thread 0's release by the barrier
   // (release is cumulative); the acquiring RMW makes every earlier CTA's record
@@ -900,12 +1029,13 @@ cudaError_t launch_dgp(const Params& p, int mode, bool pdl, int grid, cudaStream
   const void* fn;
   if (mode == 0) fn = reinterpret_cast<const void*>(&dev::fd_split_kernel<T, D, G, PATH, 0>);
   else if (mode == 1) fn = reinterpret_cast<const void*>(&dev::fd_split_kernel<T, D, G, PATH, 1>);
-  else fn = reinterpret_cast<const void*>(&dev::fd_combine_kernel<T, D, G, PATH>);
+  else if (mode == 2) fn = reinterpret_cast<const void*>(&dev::fd_combine_kernel<T, D, G, PATH>);
+  else fn = reinterpret_cast<const void*>(&dev::fd_split_kernel<T, D, G, PATH, 3>);
   int dev_id = 0;
   cudaError_t err = cudaGetDevice(&dev_id);
   if (err != cudaSuccess) return err;
   // The opt-in shared-memory size is a per-device function attribute.
-  static uint64_t done_mask[3] = {0, 0, 0};
+  static uint64_t done_mask[4] = {0, 0, 0, 0};
   const uint64_t bit = 1ull << (dev_id & 63);
   if (!(__atomic_load_n(&done_mask[mode], __ATOMIC_ACQUIRE) & bit)) {
     err = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
@@ -914,8 +1044,19 @@ cudaError_t launch_dgp(const Params& p, int mode, bool pdl, int grid, cudaStream
   }
   void* args[] = {const_cast<Params*>(&p)};
   cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
+  if (mode == 3) {
+    // The designated combiners wait for other CTAs: the whole grid must be resident.
+    int per_sm = 0, sms = 0;
+    err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, kThreads, smem);
+    if (err == cudaSuccess) err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev_id);
+    if (err != cudaSuccess) return err;
+    if ((int64_t)per_sm * sms < grid) return cudaErrorCooperativeLaunchTooLarge;
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+  } else {
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
+  }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(kThreads);

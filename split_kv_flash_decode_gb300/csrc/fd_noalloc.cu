@@ -75,6 +75,8 @@ extern "C" int fd_decode_noalloc(fd_plan_t pl, const void* q, const void* k, con
   p.status = reinterpret_cast<uint32_t*>(ws);
   p.counters = reinterpret_cast<uint32_t*>(ws + pl->off_counters);
   p.part = reinterpret_cast<float*>(ws + pl->off_part);
+  p.flags = reinterpret_cast<uint32_t*>(ws + pl->off_flags);
+  p.drop_flag = (pl->flags & FD_PLAN_TEST_DROP_FLAG) ? 1 : 0;
 
   // The array keeps whatever the previous call left: the status word and the
   // arrival counters must start at zero, so clear them on the stream first.
@@ -87,12 +89,13 @@ extern "C" int fd_decode_noalloc(fd_plan_t pl, const void* q, const void* k, con
       if (err == cudaSuccess)
         err = launch(p, pl->d, pl->G, pl->path, 2, pdl, pl->B * pl->Hkv, stream);
     } else {
-      err = launch(p, pl->d, pl->G, pl->path, 0, pdl, pl->ctas, stream);
+      err = launch(p, pl->d, pl->G, pl->path, (pl->flags & FD_PLAN_WAITS) ? 3 : 0, pdl, pl->ctas,
+                   stream);
     }
   }
   if (err != cudaSuccess) {
     cudaGetLastError();
-    return FD_ERR_CUDA;
+    return err == cudaErrorCooperativeLaunchTooLarge ? FD_ERR_UNSUPPORTED : FD_ERR_CUDA;
   }
   return FD_OK;
 }

@@ -13,7 +13,7 @@ struct fd_plan_s {
   int64_t n_tokens;
   int64_t total_partials;
   int ctas;
-  size_t off_counters, off_part, ws_bytes;
+  size_t off_counters, off_flags, off_part, ws_bytes;
   fd::Params params;  // pointers filled per call; arrays and scalars filled by fd_plan
 };
 

@@ -86,6 +86,10 @@ def test_plan_bad_dtype_flags_chunks():
     assert _raw_plan(1, 8, 8, 128, [10], [1], flags=0x80) == fd.FD_ERR_INVALID
     assert _raw_plan(1, 8, 8, 128, [10], [1], chunks=-1) == fd.FD_ERR_INVALID
     assert _raw_plan(1, 8, 8, 128, [10], [600], chunks=2) == fd.FD_ERR_UNSUPPORTED
+    # flag combinations
+    assert _raw_plan(1, 8, 8, 128, [10], [1], flags=fd.FD_PLAN_WAITS | fd.FD_PLAN_TWO_LAUNCH) == fd.FD_ERR_INVALID
+    assert _raw_plan(1, 8, 8, 128, [10], [1], flags=fd.FD_PLAN_TEST_DROP_FLAG) == fd.FD_ERR_INVALID
+    assert _raw_plan(1, 8, 8, 128, [10], [1], flags=fd.FD_PLAN_WAITS | fd.FD_PLAN_TEST_DROP_FLAG) == fd.FD_OK
     L = fd.lib()
     assert L.fd_plan(1, 8, 8, 128, None, None, 0, 0, 0, 152, None) == fd.FD_ERR_INVALID
     assert L.fd_plan_destroy(None) == fd.FD_OK
@@ -166,6 +170,6 @@ def test_workspace_layout():
     p = fd.fd_plan(3, 8, 2, 64, [10, 0, 700], [1, 2, 5], "f16", chunks=2, num_sms=152)
     P = 8 * (1 + 2 + 5) * 2
     assert p.info["total_partials"] == P
-    need = 4 * 3 * 2 + 4 * P * 2 + 4 * P * 64
+    need = 4 * 3 * 2 + 4 * p.info["ctas"] + 4 * P * (64 + 4)
     assert p.workspace_bytes >= need
     assert p.workspace_bytes % 256 == 0

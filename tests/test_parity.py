@@ -56,6 +56,9 @@ def run_gpu(fd, p, chunks=0, flags=0, repeat=1):
     ws = dec.workspace.cpu().numpy()
     counters = ws[256:256 + 4 * p.B * p.Hkv].view(np.uint32)
     assert not counters.any(), "arrival counters must be back at zero"
+    flag_off = 256 + -(-4 * p.B * p.Hkv // 256) * 256
+    flags = ws[flag_off:flag_off + 4 * dec.info["ctas"]].view(np.uint32)
+    assert not flags.any(), "ready flags must be back at zero"
     return outs if repeat > 1 else outs[0], dec
 
 
@@ -204,6 +207,61 @@ def test_pdl_off_matches_pdl_on(fd):
     (o1, l1), _ = run_gpu(fd, p, repeat=1)
     (o2, l2), _ = run_gpu(fd, p, flags=fd.FD_PLAN_NO_PDL)
     assert np.array_equal(o1, o2) and np.array_equal(l1, l2)
+
+
+@pytest.mark.parametrize("dtype,G,d", [("f16", 4, 128), ("bf16", 8, 128), ("f16", 1, 64),
+                                       ("bf16", 4, 64)])
+def test_fine_grained_waits_variant(fd, dtype, G, d):
+    """Slot 0 of each (sequence, KV head) combines the partials as their flags arrive."""
+    p = workloads.make_problem("waits", 3, 8 * G, 8, d, [20000, 0, 3001], [4, 2, 3], dtype,
+                               seed=30 + G + d)
+    ref_out, ref_lse = oracle.decode_reference(p.q, p.k, p.v, p.seqlens, p.dtype)
+    for chunks in (0, 1):
+        (out, lse), dec = run_gpu(fd, p, flags=fd.FD_PLAN_WAITS, chunks=chunks)
+        check(out, lse, ref_out, ref_lse, dtype=p.dtype)
+
+
+def test_fine_grained_waits_full_32k(fd):
+    p = workloads.gqa4_d128_L32k_W8()
+    (out, lse), dec = run_gpu(fd, p, flags=fd.FD_PLAN_WAITS)
+    assert dec.info["ctas"] == 256
+    ref_out, ref_lse = oracle.decode_reference(p.q, p.k, p.v, p.seqlens, p.dtype)
+    check(out, lse, ref_out, ref_lse)
+
+
+def test_fine_grained_waits_timeout_is_reported(fd):
+    """A flag that nothing sets: the bounded wait gives up, the status word says so,
+    the other (sequence, KV head) pairs are still correct and the context stays usable."""
+    import torch
+    p = workloads.make_problem("timeout", 2, 16, 4, 128, [5000, 700], [4, 2], "f16", seed=40)
+    ref_out, ref_lse = oracle.decode_reference(p.q, p.k, p.v, p.seqlens, p.dtype)
+    dec = fd.Decoder(p.Hq, p.Hkv, p.d, p.seqlens, p.W, p.dtype,
+                     flags=fd.FD_PLAN_WAITS | fd.FD_PLAN_TEST_DROP_FLAG)
+    q, k, v = (to_torch(x, p.dtype) for x in (p.q, p.k, p.v))
+    out = torch.full_like(q, float("nan"))
+    lse = torch.full((p.B, p.Hq), float("nan"), dtype=torch.float32, device="cuda")
+    dec(q, k, v, out, lse)
+    assert dec.status() == fd.FD_ERR_TIMEOUT
+    o, l = out_to_f64(out), lse.cpu().numpy().astype(np.float64)
+    G = p.Hq // p.Hkv
+    assert np.isnan(o[0, :G]).all() and np.isnan(l[0, :G]).all()   # the starved pair: untouched
+    keep = np.ones((p.B, p.Hq), dtype=bool)
+    keep[0, :G] = False
+    assert np.abs(o[keep] - ref_out[keep]).max() <= OUT_TOL
+    assert np.abs(l[keep] - ref_lse[keep]).max() <= LSE_TOL
+    # Same context, clean workspace, no dropped flag: a normal decode.
+    (out2, lse2), _ = run_gpu(fd, p, flags=fd.FD_PLAN_WAITS)
+    check(out2, lse2, ref_out, ref_lse, dtype=p.dtype)
+
+
+def test_fine_grained_waits_needs_coresidency(fd):
+    p = workloads.make_problem("big", 64, 32, 8, 128, [512] * 64, 16, "bf16", seed=41)
+    dec = fd.Decoder(p.Hq, p.Hkv, p.d, p.seqlens, p.W, p.dtype,
+                     flags=fd.FD_PLAN_WAITS | fd.FD_PLAN_LITERAL_W)
+    q, k, v = (to_torch(x, p.dtype) for x in (p.q, p.k, p.v))
+    with pytest.raises(fd.FdError) as ei:
+        dec(q, k, v)                       # 8192 CTAs cannot all be resident: refused
+    assert ei.value.status == fd.FD_ERR_UNSUPPORTED
 
 
 def test_debug_plan_detects_counter_state(fd):
