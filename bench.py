@@ -410,10 +410,11 @@ def run_fd(args):
         stream.synchronize()
 
     def run(name):
-        if use_graph:
-            graphs[name].replay()
-        else:
-            with torch.cuda.stream(stream):
+        # A graph replays on torch's current stream: make that the decode stream.
+        with torch.cuda.stream(stream):
+            if use_graph:
+                graphs[name].replay()
+            else:
                 (record_a if name == "a" else record_b)()
 
     gpu_id = getattr(props, "uuid", None)
