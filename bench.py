@@ -50,6 +50,8 @@ def parse_args(argv=None):
     ap.add_argument("--two-launch", action="store_true", help="split + combine as two kernels")
     ap.add_argument("--ffma", action="store_true", help="CUDA-core consumers even when G >= 4")
     ap.add_argument("--no-pdl", action="store_true", help="launch without programmatic dependent launch")
+    ap.add_argument("--paged", type=int, default=0, metavar="P",
+                    help="K/V in a shuffled page pool with P tokens per page (block tables)")
     ap.add_argument("--waits", action="store_true",
                     help="fine-grained waits: slot 0 combines partials as their flags arrive")
     ap.add_argument("--soak-s", type=float, default=1.5, help="untimed load before timing (clocks)")
@@ -347,10 +349,17 @@ def run_fd(args):
         fd.FD_PLAN_TWO_LAUNCH if args.two_launch else 0) | (fd.FD_PLAN_FFMA if args.ffma else 0) | (
         fd.FD_PLAN_NO_PDL if args.no_pdl else 0) | (fd.FD_PLAN_WAITS if args.waits else 0)
     dec = fd.Decoder(prob.Hq, prob.Hkv, prob.d, prob.seqlens, prob.W, prob.dtype, flags=flags,
-                     chunks=args.chunks, device=device)
+                     chunks=args.chunks, device=device, page_size=args.paged)
     q = to_device(prob.q, prob.dtype, device)
-    k0 = to_device(prob.k, prob.dtype, device)
-    v0 = to_device(prob.v, prob.dtype, device)
+    if args.paged:
+        import workloads
+        kp, vp, table = workloads.to_paged(prob, args.paged)
+        k0, v0 = to_device(kp, prob.dtype, device), to_device(vp, prob.dtype, device)
+        bt = torch.from_numpy(table).to(device)
+        num_pages = kp.shape[0]
+    else:
+        k0 = to_device(prob.k, prob.dtype, device)
+        v0 = to_device(prob.v, prob.dtype, device)
     ks = [k0] + [k0.clone() for _ in range(copies - 1)]
     vs = [v0] + [v0.clone() for _ in range(copies - 1)]
     out = torch.empty_like(q)
@@ -359,7 +368,12 @@ def run_fd(args):
     launches_per_step = 2 if args.two_launch else 1
 
     def step(i):
-        fd.fd_decode(dec.plan, q, ks[i % copies], vs[i % copies], out, lse, dec.workspace, stream)
+        if args.paged:
+            fd.fd_decode_paged(dec.plan, q, ks[i % copies], vs[i % copies], num_pages, bt,
+                               bt.shape[1], out, lse, dec.workspace, stream)
+        else:
+            fd.fd_decode(dec.plan, q, ks[i % copies], vs[i % copies], out, lse, dec.workspace,
+                         stream)
 
     K, Wm = max(1, args.steps), max(3, args.warmup)
     with torch.cuda.stream(stream):
@@ -455,9 +469,12 @@ def run_fd(args):
     achieved = kv_bytes / (step_us * 1e-6) / 1e9
 
     # e2e through the public API with pinned host buffers.
-    e2e = e2e_measure(fd, dec, prob, device, args.e2e_steps, stream, kv_resident=False)
-    e2e_res = e2e_measure(fd, dec, prob, device, max(args.e2e_steps, 200), stream, kv_resident=True,
-                          dev_kv=(k0, v0))
+    if args.paged:
+        e2e = e2e_res = None  # the host-buffer path is measured on the contiguous layout
+    else:
+        e2e = e2e_measure(fd, dec, prob, device, args.e2e_steps, stream, kv_resident=False)
+        e2e_res = e2e_measure(fd, dec, prob, device, max(args.e2e_steps, 200), stream,
+                              kv_resident=True, dev_kv=(k0, v0))
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -478,6 +495,8 @@ def run_fd(args):
                 "partials_per_sequence_max": info["max_partials"],
                 "kv_bytes_per_step": kv_bytes, "two_launch": bool(args.two_launch),
                 "pdl": not args.no_pdl and not args.waits,
+                "kv_layout": f"paged ({args.paged} tokens per page, shuffled pool)" if args.paged
+                             else "contiguous [N, Hkv, d]",
                 "combine": "fine-grained waits (slot 0 combines as flags arrive)" if args.waits
                            else ("separate combine kernel" if args.two_launch
                                  else "last arriver (atomic counter)"),

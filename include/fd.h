@@ -106,6 +106,19 @@ enum fd_status {
 int fd_plan(int B, int Hq, int Hkv, int d, const int32_t* seqlens, const int32_t* W,
             int dtype, uint32_t flags, int chunks, int num_sms, fd_plan_t* out_plan);
 
+/*
+ * fd_plan_paged -- fd_plan for a paged KV cache (block tables; a deployment
+ * layout the pages do not discuss).  Same arguments plus
+ *   page_size  tokens per page: a power of two in [16, 256]
+ * Segment and chunk lengths are rounded up to whole kernel tiles (64 tokens on
+ * the tensor-core path, 32 on CUDA cores) so that every TMA box stays inside one
+ * page; the split changes, the result does not (the combine is exact for any
+ * partition).  Decode with fd_decode_paged.
+ */
+int fd_plan_paged(int B, int Hq, int Hkv, int d, const int32_t* seqlens, const int32_t* W,
+                  int page_size, int dtype, uint32_t flags, int chunks, int num_sms,
+                  fd_plan_t* out_plan);
+
 /* Release a plan (NULL is accepted).  No CUDA call. */
 int fd_plan_destroy(fd_plan_t plan);
 
@@ -141,6 +154,25 @@ int fd_workspace_init(fd_plan_t plan, void* workspace, cudaStream_t stream);
  */
 int fd_decode(fd_plan_t plan, const void* q, const void* k, const void* v, void* out,
               float* lse, void* workspace, cudaStream_t stream);
+
+/*
+ * fd_decode_paged -- fd_decode over a paged KV cache.
+ *
+ *   k_pages, v_pages  device [num_pages, page_size, Hkv, d] (dtype), contiguous pools
+ *   num_pages         pages in each pool (num_pages * page_size < 2^31)
+ *   block_table       device int32 [B, bt_stride]: row b lists, in order, the pool
+ *                     pages holding tokens [j*page_size, (j+1)*page_size) of
+ *                     sequence b, for j < ceil(L_b / page_size)
+ *   bt_stride         entries per row, >= max_b ceil(L_b / page_size)
+ *   q, out, lse, workspace, stream   as for fd_decode
+ *
+ * Returns FD_ERR_INVALID for a contiguous plan or a short bt_stride.  Page
+ * indices outside [0, num_pages) read zeros (TMA out-of-bounds fill); they never
+ * fault, but the result is then meaningless.  fd_decode rejects paged plans.
+ */
+int fd_decode_paged(fd_plan_t plan, const void* q, const void* k_pages, const void* v_pages,
+                    int num_pages, const int32_t* block_table, int bt_stride, void* out,
+                    float* lse, void* workspace, cudaStream_t stream);
 
 /* Bytes of the static device scratch array behind fd_decode_noalloc (32 MiB). */
 #define FD_NOALLOC_SCRATCH_BYTES (32u << 20)

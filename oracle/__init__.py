@@ -14,6 +14,7 @@ from .fd_oracle import (  # noqa: F401
     decode_reference,
     default_scale,
     finalize,
+    gather_paged,
     online_softmax_combine,
     segment_bounds,
     segment_partial,

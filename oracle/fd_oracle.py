@@ -55,6 +55,25 @@ def widen(x: np.ndarray, dtype: str) -> np.ndarray:
     raise ValueError(f"unknown dtype {dtype!r}")
 
 
+def gather_paged(k_pool, v_pool, block_table, seqlens, page_size):
+    """Contiguous [N, Hkv, d] K and V from a paged cache.
+
+    Token t of sequence b lives in pool page block_table[b][t // page_size], row
+    t % page_size.  (Layout only: no arithmetic of the method.)
+    """
+    ks, vs = [], []
+    for b, L in enumerate(np.asarray(seqlens, dtype=np.int64)):
+        for t0 in range(0, int(L), page_size):
+            page = int(block_table[b][t0 // page_size])
+            n = min(page_size, int(L) - t0)
+            ks.append(k_pool[page, :n])
+            vs.append(v_pool[page, :n])
+    if not ks:
+        shape = (0,) + tuple(k_pool.shape[2:])
+        return np.zeros(shape, k_pool.dtype), np.zeros(shape, v_pool.dtype)
+    return np.concatenate(ks), np.concatenate(vs)
+
+
 def default_scale(d: int) -> float:
     return 1.0 / math.sqrt(d)
 

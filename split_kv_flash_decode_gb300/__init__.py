@@ -33,7 +33,9 @@ from ._binding import (  # noqa: F401
     Plan,
     fd_decode,
     fd_decode_noalloc,
+    fd_decode_paged,
     fd_plan,
+    fd_plan_paged,
     fd_plan_destroy,
     fd_plan_get_range,
     fd_version,

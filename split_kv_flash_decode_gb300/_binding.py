@@ -40,7 +40,7 @@ DTYPES = {"f16": FD_F16, "bf16": FD_BF16}
 EXPORTED = (
     "fd_plan", "fd_plan_destroy", "fd_workspace_bytes", "fd_workspace_init", "fd_decode",
     "fd_workspace_status", "fd_strerror", "fd_plan_get_info", "fd_plan_get_range", "fd_version",
-    "fd_decode_noalloc",
+    "fd_decode_noalloc", "fd_plan_paged", "fd_decode_paged",
 )
 FD_NOALLOC_SCRATCH_BYTES = 32 << 20
 
@@ -101,6 +101,14 @@ def lib() -> ctypes.CDLL:
             L.fd_plan_get_range.argtypes = [vp, ctypes.c_int, ctypes.c_int, ctypes.POINTER(i32),
                                             ctypes.POINTER(i32)]
             L.fd_plan_get_range.restype = ctypes.c_int
+            L.fd_plan_paged.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                        ctypes.POINTER(i32), ctypes.POINTER(i32), ctypes.c_int,
+                                        ctypes.c_int, u32, ctypes.c_int, ctypes.c_int,
+                                        ctypes.POINTER(vp)]
+            L.fd_plan_paged.restype = ctypes.c_int
+            L.fd_decode_paged.argtypes = [vp, vp, vp, vp, ctypes.c_int, vp, ctypes.c_int, vp, vp,
+                                          vp, vp]
+            L.fd_decode_paged.restype = ctypes.c_int
             L.fd_decode_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp]
             L.fd_decode_noalloc.restype = ctypes.c_int
             L.fd_version.argtypes = []
@@ -184,6 +192,30 @@ def fd_plan(B, Hq, Hkv, d, seqlens, W, dtype="f16", flags=0, chunks=0, num_sms=0
                        int(flags), int(chunks), int(num_sms), ctypes.byref(handle))
     _check(rc, "fd_plan")
     return Plan(handle.value)
+
+
+def fd_plan_paged(B, Hq, Hkv, d, seqlens, W, page_size, dtype="f16", flags=0, chunks=0,
+                  num_sms=0) -> Plan:
+    """fd_plan_paged: plan a decode over a paged KV cache (host only)."""
+    seqlens = list(seqlens)
+    W = [W] * B if isinstance(W, int) else list(W)
+    if len(seqlens) != B or len(W) != B:
+        raise FdError(FD_ERR_INVALID, "fd_plan_paged: seqlens and W need B entries")
+    handle = ctypes.c_void_p()
+    rc = lib().fd_plan_paged(int(B), int(Hq), int(Hkv), int(d), _i32_array(seqlens, B),
+                             _i32_array(W, B), int(page_size),
+                             DTYPES[dtype] if isinstance(dtype, str) else int(dtype), int(flags),
+                             int(chunks), int(num_sms), ctypes.byref(handle))
+    _check(rc, "fd_plan_paged")
+    return Plan(handle.value)
+
+
+def fd_decode_paged(plan: Plan, q, k_pages, v_pages, num_pages, block_table, bt_stride, out, lse,
+                    workspace, stream=None) -> None:
+    """fd_decode_paged: the fused decode over a paged cache (block tables)."""
+    _check(lib().fd_decode_paged(plan.handle, _ptr(q), _ptr(k_pages), _ptr(v_pages),
+                                 int(num_pages), _ptr(block_table), int(bt_stride), _ptr(out),
+                                 _ptr(lse), _ptr(workspace), _stream(stream)), "fd_decode_paged")
 
 
 def fd_plan_destroy(plan: Plan) -> None:

@@ -47,13 +47,14 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 // 3-D view (d, Hkv, N) of a [N, Hkv, d] tensor; one box = one tile of token rows of
 // one head.  The MMA path loads 64-column boxes (128-byte rows) with the 128-byte
 // swizzle; the FFMA path loads whole unswizzled rows.
-int fd::encode_kv_map(CUtensorMap* map, const void* base, const fd_plan_s* pl) {
+int fd::encode_kv_map(CUtensorMap* map, const void* base, int64_t rows, int box_rows,
+                      const fd_plan_s* pl) {
   auto enc = tensor_map_encoder();
   if (!enc) return FD_ERR_CUDA;
-  const cuuint64_t dims[3] = {(cuuint64_t)pl->d, (cuuint64_t)pl->Hkv, (cuuint64_t)pl->n_tokens};
+  const cuuint64_t dims[3] = {(cuuint64_t)pl->d, (cuuint64_t)pl->Hkv, (cuuint64_t)rows};
   const cuuint64_t strides[2] = {(cuuint64_t)pl->d * 2, (cuuint64_t)pl->Hkv * pl->d * 2};
   const cuuint32_t box[3] = {(cuuint32_t)fd::box_cols_for(pl->path, pl->d), 1u,
-                             (cuuint32_t)fd::tile_for(pl->path)};
+                             (cuuint32_t)box_rows};
   const cuuint32_t estr[3] = {1u, 1u, 1u};
   const CUtensorMapDataType ty =
       pl->dtype == FD_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
@@ -93,8 +94,14 @@ const char* fd_strerror(int status) {
   }
 }
 
-int fd_plan(int B, int Hq, int Hkv, int d, const int32_t* seqlens, const int32_t* W, int dtype,
-            uint32_t flags, int chunks, int num_sms, fd_plan_t* out_plan) {
+}  // extern "C"
+
+namespace {
+
+// fd_plan and fd_plan_paged: page_size == 0 plans the contiguous layout.
+int plan_impl(int B, int Hq, int Hkv, int d, const int32_t* seqlens, const int32_t* W,
+              int page_size, int dtype, uint32_t flags, int chunks, int num_sms,
+              fd_plan_t* out_plan) {
   if (!out_plan) return FD_ERR_INVALID;
   *out_plan = nullptr;
   if (!seqlens || !W) return FD_ERR_INVALID;
@@ -107,6 +114,8 @@ int fd_plan(int B, int Hq, int Hkv, int d, const int32_t* seqlens, const int32_t
   if ((flags & FD_PLAN_WAITS) && (flags & FD_PLAN_TWO_LAUNCH)) return FD_ERR_INVALID;
   if ((flags & FD_PLAN_TEST_DROP_FLAG) && !(flags & FD_PLAN_WAITS)) return FD_ERR_INVALID;
   const int G = Hq / Hkv;
+  if (page_size != 0 && (page_size < 16 || page_size > 256 || (page_size & (page_size - 1))))
+    return FD_ERR_UNSUPPORTED;
   if (B > FD_MAX_BATCH) return FD_ERR_UNSUPPORTED;
   if (d != 64 && d != 128) return FD_ERR_UNSUPPORTED;
   if (G != 1 && G != 2 && G != 4 && G != 8) return FD_ERR_UNSUPPORTED;
@@ -155,6 +164,11 @@ int fd_plan(int B, int Hq, int Hkv, int d, const int32_t* seqlens, const int32_t
   pl->flags = flags; pl->C = C; pl->num_sms = num_sms;
   // Tensor cores whenever the GQA group covers at least half of the mma N = 8 tile.
   pl->path = (G >= 4 && !(flags & FD_PLAN_FFMA)) ? fd::kPathMma : fd::kPathFfma;
+  pl->page_size = page_size;
+  pl->max_pages = 0;
+  if (page_size)
+    for (int b = 0; b < B; ++b)
+      pl->max_pages = std::max(pl->max_pages, (seqlens[b] + page_size - 1) / page_size);
   pl->max_partials = max_w * C;
   pl->n_tokens = n_tokens;
   pl->total_partials = (int64_t)Hq * sum_w * C;
@@ -164,6 +178,11 @@ int fd_plan(int B, int Hq, int Hkv, int d, const int32_t* seqlens, const int32_t
   std::memset(&p, 0, sizeof(p));
   p.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)d));
   p.B = B; p.Hq = Hq; p.Hkv = Hkv; p.C = C;
+  // Paged caches: boundaries on whole tiles, so that every TMA box stays in one page.
+  p.align = page_size ? fd::tile_for(pl->path) : 1;
+  p.box_rows = page_size ? std::min(fd::tile_for(pl->path), page_size) : fd::tile_for(pl->path);
+  p.page_shift = 0;
+  while (page_size && (1 << p.page_shift) < page_size) ++p.page_shift;
   int32_t cu = 0, ub = 0;
   for (int b = 0; b < B; ++b) {
     p.cu[b] = cu;
@@ -187,6 +206,23 @@ int fd_plan(int B, int Hq, int Hkv, int d, const int32_t* seqlens, const int32_t
 
   *out_plan = pl;
   return FD_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int fd_plan(int B, int Hq, int Hkv, int d, const int32_t* seqlens, const int32_t* W, int dtype,
+            uint32_t flags, int chunks, int num_sms, fd_plan_t* out_plan) {
+  return plan_impl(B, Hq, Hkv, d, seqlens, W, 0, dtype, flags, chunks, num_sms, out_plan);
+}
+
+int fd_plan_paged(int B, int Hq, int Hkv, int d, const int32_t* seqlens, const int32_t* W,
+                  int page_size, int dtype, uint32_t flags, int chunks, int num_sms,
+                  fd_plan_t* out_plan) {
+  if (page_size == 0) return FD_ERR_INVALID;
+  return plan_impl(B, Hq, Hkv, d, seqlens, W, page_size, dtype, flags, chunks, num_sms,
+                   out_plan);
 }
 
 int fd_plan_destroy(fd_plan_t plan) {
@@ -215,7 +251,7 @@ int fd_plan_get_range(fd_plan_t pl, int b, int slot, int32_t* begin, int32_t* en
   if (slot < 0 || slot >= wtot) return FD_ERR_INVALID;
   const int L = pl->params.cu[b + 1] - pl->params.cu[b];
   int t0, t1;
-  fd::chunk_range(L, pl->params.wseg[b], pl->C, slot, &t0, &t1);
+  fd::chunk_range(L, pl->params.wseg[b], pl->C, slot, pl->params.align, &t0, &t1);
   *begin = t0;
   *end = t1;
   return FD_OK;
@@ -245,8 +281,15 @@ int fd_workspace_status(fd_plan_t pl, void* workspace, cudaStream_t stream, int3
   return FD_OK;
 }
 
-int fd_decode(fd_plan_t pl, const void* q, const void* k, const void* v, void* out, float* lse,
-              void* workspace, cudaStream_t stream) {
+}  // extern "C"
+
+namespace {
+
+// fd_decode and fd_decode_paged.  `rows` is N (contiguous) or the page pool's
+// num_pages * page_size rows; block_table is nullptr for the contiguous layout.
+int decode_impl(fd_plan_t pl, const void* q, const void* k, const void* v, int64_t rows,
+                const int32_t* block_table, int bt_stride, void* out, float* lse, void* workspace,
+                cudaStream_t stream) {
   if (!pl || !q || !out || !workspace) return FD_ERR_INVALID;
   if (pl->n_tokens > 0 && (!k || !v)) return FD_ERR_INVALID;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(lse) ||
@@ -255,10 +298,12 @@ int fd_decode(fd_plan_t pl, const void* q, const void* k, const void* v, void* o
 
   fd::Params p = pl->params;  // per-call copy: the plan stays immutable
   if (pl->n_tokens > 0) {
-    int rc = fd::encode_kv_map(&p.tm_k, k, pl);
-    if (rc == FD_OK) rc = fd::encode_kv_map(&p.tm_v, v, pl);
+    int rc = fd::encode_kv_map(&p.tm_k, k, rows, p.box_rows, pl);
+    if (rc == FD_OK) rc = fd::encode_kv_map(&p.tm_v, v, rows, p.box_rows, pl);
     if (rc != FD_OK) return rc;
   }
+  p.block_table = block_table;
+  p.bt_stride = bt_stride;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   p.q = q;
   p.out = out;
@@ -300,6 +345,28 @@ int fd_decode(fd_plan_t pl, const void* q, const void* k, const void* v, void* o
     if (st != FD_OK) return st;
   }
   return FD_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int fd_decode(fd_plan_t pl, const void* q, const void* k, const void* v, void* out, float* lse,
+              void* workspace, cudaStream_t stream) {
+  if (pl && pl->page_size != 0) return FD_ERR_INVALID;  // paged plans use fd_decode_paged
+  return decode_impl(pl, q, k, v, pl ? pl->n_tokens : 0, nullptr, 0, out, lse, workspace, stream);
+}
+
+int fd_decode_paged(fd_plan_t pl, const void* q, const void* k_pages, const void* v_pages,
+                    int num_pages, const int32_t* block_table, int bt_stride, void* out, float* lse,
+                    void* workspace, cudaStream_t stream) {
+  if (!pl || pl->page_size == 0) return FD_ERR_INVALID;
+  if (pl->n_tokens > 0) {
+    if (num_pages < 1 || !block_table || bt_stride < pl->max_pages) return FD_ERR_INVALID;
+    if ((int64_t)num_pages * pl->page_size >= (int64_t)1 << 31) return FD_ERR_UNSUPPORTED;
+  }
+  return decode_impl(pl, q, k_pages, v_pages, (int64_t)num_pages * pl->page_size, block_table,
+                     bt_stride, out, lse, workspace, stream);
 }
 
 }  // extern "C"

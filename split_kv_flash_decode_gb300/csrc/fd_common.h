@@ -60,6 +60,13 @@ struct Params {
   uint32_t* flags;     // [CTAs] per-partial ready flags (fine-grained-waits variant)
   uint32_t* status;    // 1 word
   int32_t drop_flag;   // test hook: partial slot 1 of (b=0, kvh=0) never sets its flag
+  // Paged KV cache: K/V rows of sequence b, token t live at pool row
+  // block_table[b * bt_stride + (t >> page_shift)] * page_size + (t & (page_size - 1)).
+  const int32_t* block_table;  // nullptr: contiguous [N, Hkv, d] layout
+  int32_t bt_stride;
+  int32_t page_shift;
+  int32_t box_rows;    // token rows per TMA box (the tile, or one page when pages are smaller)
+  int32_t align;       // segment / chunk boundaries are multiples of this many tokens
   float scale_log2;    // log2(e) / sqrt(d)
   int32_t B, Hq, Hkv, C;
   int32_t cu[FD_MAX_BATCH + 1];         // token prefix sums
@@ -69,16 +76,18 @@ struct Params {
 static_assert(sizeof(Params) <= 4096, "kernel parameters must stay within 4 KB");
 
 // Token range of partial `slot` of a sequence of length L split into W segments
-// of ceil(L/W) tokens, each cut into C chunks of ceil(n/C) tokens.
-FD_HD void chunk_range(int L, int W, int C, int slot, int* t0, int* t1) {
+// of ceil(L/W) tokens, each cut into C chunks of ceil(n/C) tokens.  With align > 1
+// (paged caches) both lengths are rounded up to multiples of `align` tokens.
+FD_HD void chunk_range(int L, int W, int C, int slot, int align, int* t0, int* t1) {
   const int w = slot / C, c = slot - (slot / C) * C;
-  const int64_t S = L > 0 ? ((int64_t)L + W - 1) / W : 0;
+  int64_t S = L > 0 ? ((int64_t)L + W - 1) / W : 0;
+  S = (S + align - 1) / align * align;
   int64_t sb = (int64_t)w * S;
   if (sb > L) sb = L;
   int64_t se = sb + S;
   if (se > L) se = L;
   const int64_t n = se - sb;
-  const int64_t cl = (n + C - 1) / C;
+  const int64_t cl = ((n + C - 1) / C + align - 1) / align * align;
   int64_t a = (int64_t)c * cl, e = (int64_t)(c + 1) * cl;
   if (a > n) a = n;
   if (e > n) e = n;

@@ -266,7 +266,7 @@ __device__ __forceinline__ Work decode_work(const Params& p, int cta) {
   w.slot = r / p.Hkv;
   w.wtot = (p.unit_base[lo + 1] - p.unit_base[lo]) / p.Hkv;
   const int L = p.cu[lo + 1] - p.cu[lo];
-  chunk_range(L, p.wseg[lo], p.C, w.slot, &w.t0, &w.t1);
+  chunk_range(L, p.wseg[lo], p.C, w.slot, p.align, &w.t0, &w.t1);
   w.pbase = (int64_t)(p.unit_base[lo] / p.Hkv) * p.Hq;
   return w;
 }
@@ -735,14 +735,35 @@ __global__ void __launch_bounds__(kThreads, 2) fd_split_kernel(const __grid_cons
         if (*(volatile int*)&sm_abort) break;
         const uint32_t dst = smem_addr(smem + (size_t)s * kStageBytes);
         mbar_arrive_expect_tx(full_bar(s), kStageBytes);
+        if (p.block_table == nullptr) {
 #pragma unroll
-        for (int bx = 0; bx < NBOX; ++bx)
-          tma_load_3d(dst + bx * (TILE * BOXC * 2), &p.tm_k, bx * BOXC, wk.kvh, row0 + kt * TILE,
-                      full_bar(s), policy);
+          for (int bx = 0; bx < NBOX; ++bx)
+            tma_load_3d(dst + bx * (TILE * BOXC * 2), &p.tm_k, bx * BOXC, wk.kvh,
+                        row0 + kt * TILE, full_bar(s), policy);
 #pragma unroll
-        for (int bx = 0; bx < NBOX; ++bx)
-          tma_load_3d(dst + kRowsBytes + bx * (TILE * BOXC * 2), &p.tm_v, bx * BOXC, wk.kvh,
-                      row0 + kt * TILE, full_bar(s), policy);
+          for (int bx = 0; bx < NBOX; ++bx)
+            tma_load_3d(dst + kRowsBytes + bx * (TILE * BOXC * 2), &p.tm_v, bx * BOXC, wk.kvh,
+                        row0 + kt * TILE, full_bar(s), policy);
+        } else {
+          // Paged: one box per page piece of the tile.  Tiles start on multiples of
+          // the tile size, so each box stays inside one page; boxes past the end of
+          // the sequence reload its last page (their rows are masked).
+          const int32_t* bt = p.block_table + (int64_t)wk.b * p.bt_stride;
+          const int last_pg = (p.cu[wk.b + 1] - p.cu[wk.b] - 1) >> p.page_shift;
+          const int a = wk.t0 + kt * TILE;
+          for (int j = 0; j < TILE; j += p.box_rows) {
+            const int pg = min((a + j) >> p.page_shift, last_pg);
+            const int row = __ldg(bt + pg) * (1 << p.page_shift) + ((a + j) & ((1 << p.page_shift) - 1));
+#pragma unroll
+            for (int bx = 0; bx < NBOX; ++bx)
+              tma_load_3d(dst + bx * (TILE * BOXC * 2) + j * BOXC * 2, &p.tm_k, bx * BOXC, wk.kvh,
+                          row, full_bar(s), policy);
+#pragma unroll
+            for (int bx = 0; bx < NBOX; ++bx)
+              tma_load_3d(dst + kRowsBytes + bx * (TILE * BOXC * 2) + j * BOXC * 2, &p.tm_v,
+                          bx * BOXC, wk.kvh, row, full_bar(s), policy);
+          }
+        }
       }
       // Every load issued must land before shared memory is reused or released.
       for (int t = (kt > STAGES ? kt - STAGES : 0); t < kt; ++t) {

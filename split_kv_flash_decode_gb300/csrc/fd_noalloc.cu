@@ -52,6 +52,7 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 extern "C" int fd_decode_noalloc(fd_plan_t pl, const void* q, const void* k, const void* v,
                                  void* out, float* lse, cudaStream_t stream) {
   if (!pl || !q || !out) return FD_ERR_INVALID;
+  if (pl->page_size != 0) return FD_ERR_INVALID;  // contiguous K/V only
   if (pl->n_tokens > 0 && (!k || !v)) return FD_ERR_INVALID;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(lse))
     return FD_ERR_ALIGN;
@@ -64,8 +65,8 @@ extern "C" int fd_decode_noalloc(fd_plan_t pl, const void* q, const void* k, con
 
   fd::Params p = pl->params;
   if (pl->n_tokens > 0) {
-    rc = fd::encode_kv_map(&p.tm_k, k, pl);
-    if (rc == FD_OK) rc = fd::encode_kv_map(&p.tm_v, v, pl);
+    rc = fd::encode_kv_map(&p.tm_k, k, pl->n_tokens, p.box_rows, pl);
+    if (rc == FD_OK) rc = fd::encode_kv_map(&p.tm_v, v, pl->n_tokens, p.box_rows, pl);
     if (rc != FD_OK) return rc;
   }
   uint8_t* ws = static_cast<uint8_t*>(scratch);

@@ -16,7 +16,7 @@ class Decoder:
     """Plan + zeroed workspace for one decode shape on one device."""
 
     def __init__(self, Hq, Hkv, d, seqlens, W, dtype="f16", flags=0, chunks=0, device=None,
-                 num_sms=0):
+                 num_sms=0, page_size=0):
         dev = torch.device(device if device is not None else "cuda")
         if dev.type != "cuda":
             raise ValueError("Decoder needs a CUDA device")
@@ -26,9 +26,14 @@ class Decoder:
         self.Bsz = len(self.seqlens)
         self.Hq, self.Hkv, self.d, self.dtype = int(Hq), int(Hkv), int(d), dtype
         self.n_tokens = sum(self.seqlens)
+        self.page_size = int(page_size)
         with torch.cuda.device(self.device):
-            self.plan = B.fd_plan(self.Bsz, Hq, Hkv, d, self.seqlens, W, dtype, flags, chunks,
-                                  num_sms)
+            if self.page_size:
+                self.plan = B.fd_plan_paged(self.Bsz, Hq, Hkv, d, self.seqlens, W, self.page_size,
+                                            dtype, flags, chunks, num_sms)
+            else:
+                self.plan = B.fd_plan(self.Bsz, Hq, Hkv, d, self.seqlens, W, dtype, flags, chunks,
+                                      num_sms)
             self.workspace = torch.zeros(max(1, self.plan.workspace_bytes), dtype=torch.uint8,
                                          device=self.device)
 
@@ -60,6 +65,27 @@ class Decoder:
             raise ValueError("lse must be float32 [B, Hq]")
         with torch.cuda.device(self.device):
             B.fd_decode(self.plan, q, k, v, out, lse, self.workspace, stream)
+        return out, lse
+
+    def decode_paged(self, q, k_pages, v_pages, block_table, out=None, lse=None, stream=None):
+        """Decode over a paged cache: pools [num_pages, page_size, Hkv, d], int32 block_table [B, stride]."""
+        if not self.page_size:
+            raise ValueError("this Decoder was planned for contiguous K/V")
+        self._check("q", q, (self.Bsz, self.Hq, self.d))
+        num_pages = k_pages.shape[0]
+        for name, t in (("k_pages", k_pages), ("v_pages", v_pages)):
+            self._check(name, t, (num_pages, self.page_size, self.Hkv, self.d))
+        if block_table.dtype != torch.int32 or block_table.dim() != 2 or \
+                block_table.shape[0] != self.Bsz or not block_table.is_contiguous() or \
+                block_table.device != self.device:
+            raise ValueError("block_table must be a contiguous int32 [B, stride] tensor on the device")
+        if out is None:
+            out = torch.empty_like(q)
+        if lse is None:
+            lse = torch.empty((self.Bsz, self.Hq), dtype=torch.float32, device=self.device)
+        with torch.cuda.device(self.device):
+            B.fd_decode_paged(self.plan, q, k_pages, v_pages, num_pages, block_table,
+                              block_table.shape[1], out, lse, self.workspace, stream)
         return out, lse
 
     def status(self, stream=None) -> int:

@@ -173,3 +173,32 @@ def test_workspace_layout():
     need = 4 * 3 * 2 + 4 * p.info["ctas"] + 4 * P * (64 + 4)
     assert p.workspace_bytes >= need
     assert p.workspace_bytes % 256 == 0
+
+
+def test_paged_plan_validation_and_alignment():
+    L = fd.lib()
+    arr = (ctypes.c_int32 * 2)(1000, 77)
+    warr = (ctypes.c_int32 * 2)(3, 2)
+    h = ctypes.c_void_p()
+    for ps, code in ((0, fd.FD_ERR_INVALID), (8, fd.FD_ERR_UNSUPPORTED), (48, fd.FD_ERR_UNSUPPORTED),
+                     (512, fd.FD_ERR_UNSUPPORTED), (16, fd.FD_OK), (256, fd.FD_OK)):
+        rc = L.fd_plan_paged(2, 32, 8, 128, arr, warr, ps, 0, 0, 0, 152, ctypes.byref(h))
+        assert rc == code, ps
+        if rc == fd.FD_OK:
+            L.fd_plan_destroy(h)
+    for G, tile in ((4, 64), (1, 32)):
+        p = fd.fd_plan_paged(2, 8 * G, 8, 128, [1000, 77], [3, 2], 16, "f16", chunks=3, num_sms=152)
+        for b, Lb in enumerate((1000, 77)):
+            pos = 0
+            for slot in range((3, 2)[b] * 3):
+                lo, hi = p.range(b, slot)
+                assert lo == pos and hi >= lo and (lo % tile == 0 or lo == hi)
+                pos = hi
+            assert pos == Lb
+        # contiguous decode entry point refuses paged plans (before any CUDA call)
+        assert L.fd_decode(p.handle, 16, 16, 16, 16, 0, 16, None) == fd.FD_ERR_INVALID
+        # short block-table stride
+        need = -(-1000 // 16)
+        assert L.fd_decode_paged(p.handle, 16, 16, 16, 100, 16, need - 1, 16, 0, 16, None) == fd.FD_ERR_INVALID
+    c = fd.fd_plan(1, 8, 8, 64, [100], 1, "f16", num_sms=152)
+    assert L.fd_decode_paged(c.handle, 16, 16, 16, 10, 16, 10, 16, 0, 16, None) == fd.FD_ERR_INVALID

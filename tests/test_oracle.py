@@ -470,3 +470,16 @@ def test_planted_mistake_is_caught(mutation, monkeypatch):
         if not ok:
             failed.append(name)
     assert failed, f"no pin caught the planted mistake {mutation}"
+
+
+def test_paged_gather_round_trip():
+    """A block table means: token t of sequence b is row t % P of page table[b][t // P]."""
+    for page_size in (16, 64, 256):
+        p = workloads.make_problem("paged", 4, 8, 2, 16, [0, 1, 300, 1025], [1, 2, 3, 4], "f16",
+                                   seed=page_size)
+        kp, vp, table = workloads.to_paged(p, page_size)
+        k, v = oracle.gather_paged(kp, vp, table, p.seqlens, page_size)
+        assert np.array_equal(k, p.k) and np.array_equal(v, p.v)
+        # every used page appears once; spare pages are not referenced
+        used = table[table >= 0]
+        assert len(set(used.tolist())) == len(used) and len(used) == kp.shape[0] - 3

@@ -264,6 +264,40 @@ def test_fine_grained_waits_needs_coresidency(fd):
     assert ei.value.status == fd.FD_ERR_UNSUPPORTED
 
 
+def run_paged(fd, p, page_size, flags=0, chunks=0):
+    import torch
+    kp, vp, table = workloads.to_paged(p, page_size)
+    dec = fd.Decoder(p.Hq, p.Hkv, p.d, p.seqlens, p.W, p.dtype, flags=flags, chunks=chunks,
+                     page_size=page_size)
+    q = to_torch(p.q, p.dtype)
+    out, lse = dec.decode_paged(q, to_torch(kp, p.dtype), to_torch(vp, p.dtype),
+                                torch.from_numpy(table).cuda())
+    assert dec.status() == fd.FD_OK
+    return out_to_f64(out), lse.cpu().numpy().astype(np.float64), dec, (kp, vp, table)
+
+
+@pytest.mark.parametrize("page_size", [16, 32, 64, 128, 256])
+@pytest.mark.parametrize("dtype,G", [("f16", 4), ("bf16", 8), ("f16", 1)])
+def test_paged_cache(fd, page_size, dtype, G):
+    p = workloads.make_problem("paged", 4, 8 * G, 8, 128, [5000, 0, 33, 1031], [3, 1, 2, 4], dtype,
+                               seed=50 + page_size + G)
+    ref_out, ref_lse = oracle.decode_reference(p.q, p.k, p.v, p.seqlens, p.dtype)
+    for chunks in (0, 2):
+        out, lse, dec, (kp, vp, table) = run_paged(fd, p, page_size, chunks=chunks)
+        check(out, lse, ref_out, ref_lse, dtype=p.dtype)
+    # the oracle over the gathered pages is the same problem
+    k, v = oracle.gather_paged(kp, vp, table, p.seqlens, page_size)
+    assert np.array_equal(k, p.k) and np.array_equal(v, p.v)
+
+
+def test_paged_cache_full_32k_and_variants(fd):
+    p = workloads.gqa4_d128_L32k_W8()
+    ref_out, ref_lse = oracle.decode_reference(p.q, p.k, p.v, p.seqlens, p.dtype)
+    for flags in (0, fd.FD_PLAN_TWO_LAUNCH, fd.FD_PLAN_WAITS):
+        out, lse, _, _ = run_paged(fd, p, 64, flags=flags)
+        check(out, lse, ref_out, ref_lse)
+
+
 def test_debug_plan_detects_counter_state(fd):
     import torch
     p = workloads.make_problem("debug", 1, 8, 8, 64, [2048], 4, "f16", seed=16)

@@ -155,6 +155,43 @@ def make_problem(name, B, Hq, Hkv, d, seqlens, W, dtype=F16, seed=0, literal_w=F
                          literal_w, dict(notes or {}))
 
 
+_STREAM_PAGES = 6
+
+
+def to_paged(problem: DecodeProblem, page_size: int, spare_pages: int = 3, seed: int = None):
+    """Scatter a problem's contiguous K/V into a shuffled page pool.
+
+    Returns ``(k_pool, v_pool, block_table)``: pools ``[num_pages, page_size, Hkv, d]``
+    and an int32 table ``[B, max_pages]`` (unused entries -1) whose row b lists the
+    pool pages holding tokens ``[j*page_size, (j+1)*page_size)`` of sequence b.  Page
+    order is a seeded permutation, with ``spare_pages`` pages that no sequence uses.
+    Rows of a sequence's last page beyond its length are filled with random values.
+    """
+    seed = problem.seed if seed is None else seed
+    gen = rng(seed, _STREAM_PAGES)
+    lens = problem.seqlens.astype(np.int64)
+    npg = (lens + page_size - 1) // page_size
+    total = int(npg.sum()) + spare_pages
+    max_pages = max(1, int(npg.max()) if len(npg) else 1)
+    perm = gen.permutation(total)
+    shape = (total, page_size, problem.Hkv, problem.d)
+    k_pool = normal(gen, shape, problem.dtype)
+    v_pool = normal(gen, shape, problem.dtype)
+    table = np.full((problem.B, max_pages), -1, dtype=np.int32)
+    cu = problem.cu_seqlens
+    nxt = 0
+    for b in range(problem.B):
+        for j in range(int(npg[b])):
+            page = int(perm[nxt])
+            nxt += 1
+            table[b, j] = page
+            t0 = j * page_size
+            t1 = min(int(lens[b]), t0 + page_size)
+            k_pool[page, :t1 - t0] = problem.k[cu[b] + t0:cu[b] + t1]
+            v_pool[page, :t1 - t0] = problem.v[cu[b] + t0:cu[b] + t1]
+    return k_pool, v_pool, table
+
+
 # ---------------------------------------------------------------------------
 # The five decode cases (one fixed seed each, 1000 + index).
 # ---------------------------------------------------------------------------
