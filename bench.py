@@ -68,6 +68,8 @@ def make_problem(args):
     import workloads
     if args.workload.startswith("batch64"):
         return workloads.batch64_gqa4_d128_L8k_bf16(W=args.W)
+    if args.workload in workloads.EXTRA:
+        return workloads.EXTRA[args.workload]()
     return workloads.CASES[args.workload]()
 
 

@@ -84,7 +84,8 @@ enum fd_status {
  * no CUDA call unless num_sms == 0).
  *
  *   B        number of sequences, 1 .. FD_MAX_BATCH
- *   Hq, Hkv  query / KV heads; Hq % Hkv == 0; G = Hq / Hkv in {1, 2, 4, 8}
+ *   Hq, Hkv  query / KV heads; Hq % Hkv == 0; G = Hq / Hkv in {1, 2, 4, 8, 16}
+ *            (G >= 4 runs on tensor cores; G = 16 only there)
  *   d        head dimension, 64 or 128
  *   seqlens  host array [B], L_b >= 0; sum_b L_b < 2^31.  Sequence b occupies
  *            KV rows [cu_b, cu_b + L_b) with cu_b = L_0 + ... + L_{b-1}.

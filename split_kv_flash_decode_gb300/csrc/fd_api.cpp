@@ -118,7 +118,8 @@ int plan_impl(int B, int Hq, int Hkv, int d, const int32_t* seqlens, const int32
     return FD_ERR_UNSUPPORTED;
   if (B > FD_MAX_BATCH) return FD_ERR_UNSUPPORTED;
   if (d != 64 && d != 128) return FD_ERR_UNSUPPORTED;
-  if (G != 1 && G != 2 && G != 4 && G != 8) return FD_ERR_UNSUPPORTED;
+  if (G != 1 && G != 2 && G != 4 && G != 8 && G != 16) return FD_ERR_UNSUPPORTED;
+  if (G == 16 && (flags & FD_PLAN_FFMA)) return FD_ERR_UNSUPPORTED;  // tensor cores only
 
   int64_t n_tokens = 0, sum_w = 0;
   int max_w = 0;
@@ -155,6 +156,15 @@ int plan_impl(int B, int Hq, int Hkv, int d, const int32_t* seqlens, const int32
     C = (int)c;
   }
   if ((int64_t)max_w * C > FD_MAX_PARTIALS) return FD_ERR_UNSUPPORTED;
+  {
+    // The combine's shared-memory scratch must fit in the ring it reuses.
+    const int path = (G >= 4 && !(flags & FD_PLAN_FFMA)) ? fd::kPathMma : fd::kPathFfma;
+    const int64_t wt = (int64_t)max_w * C;
+    int64_t need = (G * wt + 2 * G) * 4 + 16;                       // coefficients
+    if (flags & FD_PLAN_WAITS)                                      // running state + lists
+      need = std::max<int64_t>(need, (int64_t)(G * d + 3 * G + G * wt) * 4 + (2 * wt + 2) * 4);
+    if (need > (int64_t)fd::ring_bytes_for(path, d)) return FD_ERR_UNSUPPORTED;
+  }
   const int64_t ctas = (int64_t)Hkv * sum_w * C;
   if (ctas >= (int64_t)1 << 31) return FD_ERR_UNSUPPORTED;
 

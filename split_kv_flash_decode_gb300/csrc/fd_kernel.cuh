@@ -774,23 +774,32 @@ __global__ void __launch_bounds__(kThreads, 2) fd_split_kernel(const __grid_cons
   } else if constexpr (PATH == kPathMma) {
     // ---------------- MMA consumers ----------------
     constexpr int KT = D / 16;            // k-steps of S = K Q^T, m-tiles of O^T
+    constexpr int NT = G >= 8 ? G / 8 : 1;  // N tiles of 8 query heads
     const int qrow = lane >> 2;           // C/B fragment row (token) or column (head)
     const int qcol = (lane & 3) * 2;      // C fragment column pair (heads qcol, qcol+1)
     const int mj = lane >> 3, mr = lane & 7;  // ldmatrix: matrix and row this lane addresses
     // q as the B operand of S^T = K Q^T: B[k][n] = q[head n][k]; heads >= G are zero.
-    uint32_t qb[KT][2];
-    {
-      const T* qh = reinterpret_cast<const T*>(p.q) + ((int64_t)wk.b * p.Hq + wk.kvh * G + qrow) * D;
+    uint32_t qb[NT][KT][2];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      const int head = nt * 8 + qrow;
+      const T* qh = reinterpret_cast<const T*>(p.q) +
+                    ((int64_t)wk.b * p.Hq + wk.kvh * G + (head < G ? head : 0)) * D;
 #pragma unroll
       for (int kk = 0; kk < KT; ++kk) {
-        qb[kk][0] = qrow < G ? *reinterpret_cast<const uint32_t*>(qh + kk * 16 + qcol) : 0u;
-        qb[kk][1] = qrow < G ? *reinterpret_cast<const uint32_t*>(qh + kk * 16 + qcol + 8) : 0u;
+        qb[nt][kk][0] = head < G ? *reinterpret_cast<const uint32_t*>(qh + kk * 16 + qcol) : 0u;
+        qb[nt][kk][1] = head < G ? *reinterpret_cast<const uint32_t*>(qh + kk * 16 + qcol + 8) : 0u;
       }
     }
-    float o[KT][4];
+    float o[NT][KT][4];
+    float mA[NT], mB[NT], lA[NT], lB[NT];
 #pragma unroll
-    for (int mi = 0; mi < KT; ++mi) o[mi][0] = o[mi][1] = o[mi][2] = o[mi][3] = 0.f;
-    float mA = -INFINITY, mB = -INFINITY, lA = 0.f, lB = 0.f;
+    for (int nt = 0; nt < NT; ++nt) {
+#pragma unroll
+      for (int mi = 0; mi < KT; ++mi) o[nt][mi][0] = o[nt][mi][1] = o[nt][mi][2] = o[nt][mi][3] = 0.f;
+      mA[nt] = mB[nt] = -INFINITY;
+      lA[nt] = lB[nt] = 0.f;
+    }
     const float scale = p.scale_log2;
     const int tok0 = warp * 16;
     const int krow = tok0 + (mj & 1) * 8 + mr;   // K rows this lane addresses (A = K)
@@ -810,49 +819,59 @@ __global__ void __launch_bounds__(kThreads, 2) fd_split_kernel(const __grid_cons
       if (tok0 < ntok) {
         const uint32_t kbase = smem_addr(smem + (size_t)s * kStageBytes);
         const uint32_t vbase = kbase + kRowsBytes;
-        float sc[4] = {0.f, 0.f, 0.f, 0.f};
+        float sc[NT][4];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
 #pragma unroll
         for (int kk = 0; kk < KT; ++kk) {
           uint32_t a[4];
           ldmatrix_x4(a, swz_addr(kbase, TILE, krow, 2 * kk + (mj >> 1)));
-          mma16816<T>(sc, a, qb[kk][0], qb[kk][1]);
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt) mma16816<T>(sc[nt], a, qb[nt][kk][0], qb[nt][kk][1]);
         }
         const bool v0 = tok0 + qrow < ntok, v1 = tok0 + qrow + 8 < ntok;
-        const float sA0 = v0 ? sc[0] * scale : -INFINITY, sB0 = v0 ? sc[1] * scale : -INFINITY;
-        const float sA1 = v1 ? sc[2] * scale : -INFINITY, sB1 = v1 ? sc[3] * scale : -INFINITY;
-        float xA = fmaxf(sA0, sA1), xB = fmaxf(sB0, sB1);
+        uint32_t pb0[NT], pb1[NT];
 #pragma unroll
-        for (int off = 4; off < 32; off <<= 1) {
-          xA = fmaxf(xA, __shfl_xor_sync(0xffffffffu, xA, off));
-          xB = fmaxf(xB, __shfl_xor_sync(0xffffffffu, xB, off));
-        }
-        if (xA > mA + kRescaleThreshold) {
-          const float corr = ex2(mA - xA);
-          lA *= corr;
+        for (int nt = 0; nt < NT; ++nt) {
+          const float sA0 = v0 ? sc[nt][0] * scale : -INFINITY;
+          const float sB0 = v0 ? sc[nt][1] * scale : -INFINITY;
+          const float sA1 = v1 ? sc[nt][2] * scale : -INFINITY;
+          const float sB1 = v1 ? sc[nt][3] * scale : -INFINITY;
+          float xA = fmaxf(sA0, sA1), xB = fmaxf(sB0, sB1);
 #pragma unroll
-          for (int mi = 0; mi < KT; ++mi) { o[mi][0] *= corr; o[mi][2] *= corr; }
-          mA = xA;
-        }
-        if (xB > mB + kRescaleThreshold) {
-          const float corr = ex2(mB - xB);
-          lB *= corr;
+          for (int off = 4; off < 32; off <<= 1) {
+            xA = fmaxf(xA, __shfl_xor_sync(0xffffffffu, xA, off));
+            xB = fmaxf(xB, __shfl_xor_sync(0xffffffffu, xB, off));
+          }
+          if (xA > mA[nt] + kRescaleThreshold) {
+            const float corr = ex2(mA[nt] - xA);
+            lA[nt] *= corr;
 #pragma unroll
-          for (int mi = 0; mi < KT; ++mi) { o[mi][1] *= corr; o[mi][3] *= corr; }
-          mB = xB;
+            for (int mi = 0; mi < KT; ++mi) { o[nt][mi][0] *= corr; o[nt][mi][2] *= corr; }
+            mA[nt] = xA;
+          }
+          if (xB > mB[nt] + kRescaleThreshold) {
+            const float corr = ex2(mB[nt] - xB);
+            lB[nt] *= corr;
+#pragma unroll
+            for (int mi = 0; mi < KT; ++mi) { o[nt][mi][1] *= corr; o[nt][mi][3] *= corr; }
+            mB[nt] = xB;
+          }
+          // Row tok0 is valid, so the column maxima (and mA, mB) are finite here.
+          const float pA0 = ex2(sA0 - mA[nt]), pB0 = ex2(sB0 - mB[nt]);
+          const float pA1 = ex2(sA1 - mA[nt]), pB1 = ex2(sB1 - mB[nt]);
+          lA[nt] += pA0 + pA1;
+          lB[nt] += pB0 + pB1;
+          // P (tokens x heads, accumulator layout) -> P^T as the B operand (k = token).
+          pb0[nt] = movmatrix_trans(pack2<T>(pA0, pB0));
+          pb1[nt] = movmatrix_trans(pack2<T>(pA1, pB1));
         }
-        // Row tok0 is valid, so the column maxima (and mA, mB) are finite here.
-        const float pA0 = ex2(sA0 - mA), pB0 = ex2(sB0 - mB);
-        const float pA1 = ex2(sA1 - mA), pB1 = ex2(sB1 - mB);
-        lA += pA0 + pA1;
-        lB += pB0 + pB1;
-        // P (tokens x heads, accumulator layout) -> P^T as the B operand (k = token).
-        const uint32_t pb0 = movmatrix_trans(pack2<T>(pA0, pB0));
-        const uint32_t pb1 = movmatrix_trans(pack2<T>(pA1, pB1));
 #pragma unroll
         for (int mi = 0; mi < KT; ++mi) {
           uint32_t a[4];
           ldmatrix_x4_trans(a, swz_addr(vbase, TILE, vrow, 2 * mi + (mj & 1)));
-          mma16816<T>(o[mi], a, pb0, pb1);
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt) mma16816<T>(o[nt][mi], a, pb0[nt], pb1[nt]);
         }
       }
       __syncwarp();
@@ -860,26 +879,35 @@ __global__ void __launch_bounds__(kThreads, 2) fd_split_kernel(const __grid_cons
     }
     // Row sums: lanes sharing a head pair hold partial sums over their tokens.
 #pragma unroll
-    for (int off = 4; off < 32; off <<= 1) {
-      lA += __shfl_xor_sync(0xffffffffu, lA, off);
-      lB += __shfl_xor_sync(0xffffffffu, lB, off);
+    for (int nt = 0; nt < NT; ++nt) {
+#pragma unroll
+      for (int off = 4; off < 32; off <<= 1) {
+        lA[nt] += __shfl_xor_sync(0xffffffffu, lA[nt], off);
+        lB[nt] += __shfl_xor_sync(0xffffffffu, lB[nt], off);
+      }
     }
     __syncthreads();  // ring drained: reuse it for the per-warp states
-    if (*(volatile int*)&sm_abort == 0 && qcol < G) {
-      float* accA = sm_acc + (warp * G + qcol) * D;
-      float* accB = accA + D;
+    if (*(volatile int*)&sm_abort == 0) {
 #pragma unroll
-      for (int mi = 0; mi < KT; ++mi) {
-        accA[16 * mi + qrow] = o[mi][0];
-        accB[16 * mi + qrow] = o[mi][1];
-        accA[16 * mi + qrow + 8] = o[mi][2];
-        accB[16 * mi + qrow + 8] = o[mi][3];
-      }
-      if (qrow == 0) {
-        sm_m[warp * G + qcol] = mA;
-        sm_m[warp * G + qcol + 1] = mB;
-        sm_l[warp * G + qcol] = lA;
-        sm_l[warp * G + qcol + 1] = lB;
+      for (int nt = 0; nt < NT; ++nt) {
+        const int hA = nt * 8 + qcol;
+        if (hA < G) {
+          float* accA = sm_acc + (warp * G + hA) * D;
+          float* accB = accA + D;
+#pragma unroll
+          for (int mi = 0; mi < KT; ++mi) {
+            accA[16 * mi + qrow] = o[nt][mi][0];
+            accB[16 * mi + qrow] = o[nt][mi][1];
+            accA[16 * mi + qrow + 8] = o[nt][mi][2];
+            accB[16 * mi + qrow + 8] = o[nt][mi][3];
+          }
+          if (qrow == 0) {
+            sm_m[warp * G + hA] = mA[nt];
+            sm_m[warp * G + hA + 1] = mB[nt];
+            sm_l[warp * G + hA] = lA[nt];
+            sm_l[warp * G + hA + 1] = lB[nt];
+          }
+        }
       }
     }
   } else {
@@ -1096,8 +1124,8 @@ cudaError_t launch_typed(const Params& p, int d, int G, int path, int mode, bool
   FD_CASE(64, 1, kPathFfma) FD_CASE(64, 2, kPathFfma) FD_CASE(64, 4, kPathFfma)
   FD_CASE(64, 8, kPathFfma) FD_CASE(128, 1, kPathFfma) FD_CASE(128, 2, kPathFfma)
   FD_CASE(128, 4, kPathFfma) FD_CASE(128, 8, kPathFfma)
-  FD_CASE(64, 4, kPathMma) FD_CASE(64, 8, kPathMma) FD_CASE(128, 4, kPathMma)
-  FD_CASE(128, 8, kPathMma)
+  FD_CASE(64, 4, kPathMma) FD_CASE(64, 8, kPathMma) FD_CASE(64, 16, kPathMma)
+  FD_CASE(128, 4, kPathMma) FD_CASE(128, 8, kPathMma) FD_CASE(128, 16, kPathMma)
 #undef FD_CASE
   return cudaErrorInvalidValue;
 }

@@ -72,7 +72,8 @@ def _raw_plan(B, Hq, Hkv, d, seqlens, W, dtype=0, flags=0, chunks=0, num_sms=152
     ((1, 8, 8, 128, [10], [0]), fd.FD_ERR_INVALID),                   # W < 1
     ((1, 8, 8, 96, [10], [1]), fd.FD_ERR_UNSUPPORTED),                # d
     ((1, 24, 8, 128, [10], [1]), fd.FD_ERR_UNSUPPORTED),              # G = 3
-    ((1, 128, 8, 128, [10], [1]), fd.FD_ERR_UNSUPPORTED),             # G = 16
+    ((1, 256, 8, 128, [10], [1]), fd.FD_ERR_UNSUPPORTED),             # G = 32
+    ((1, 128, 8, 128, [10], [1]), fd.FD_OK),                          # G = 16 (tensor cores)
     ((257, 8, 8, 128, [1] * 257, [1] * 257), fd.FD_ERR_UNSUPPORTED),  # batch limit
     ((1, 8, 8, 128, [10], [1025]), fd.FD_ERR_UNSUPPORTED),            # partial limit
     ((1, 8, 8, 128, [10], [1]), fd.FD_OK),
@@ -164,6 +165,18 @@ def test_consumer_path_choice():
         assert p.info["path"] == path, G
     p = fd.fd_plan(1, 64, 8, 128, [1000], 2, "bf16", flags=fd.FD_PLAN_FFMA, num_sms=152)
     assert p.info["path"] == 0
+    assert fd.fd_plan(1, 128, 8, 128, [1000], 2, "f16", num_sms=152).info["path"] == 1
+    with pytest.raises(fd.FdError) as ei:
+        fd.fd_plan(1, 128, 8, 128, [1000], 2, "f16", flags=fd.FD_PLAN_FFMA, num_sms=152)
+    assert ei.value.status == fd.FD_ERR_UNSUPPORTED
+
+
+def test_combine_scratch_limit():
+    # G = 16 with 1024 partials needs more combine scratch than the d = 64 ring holds
+    with pytest.raises(fd.FdError) as ei:
+        fd.fd_plan(1, 128, 8, 64, [100000], 1024, "f16", flags=fd.FD_PLAN_LITERAL_W, num_sms=152)
+    assert ei.value.status == fd.FD_ERR_UNSUPPORTED
+    fd.fd_plan(1, 128, 8, 128, [100000], 1024, "f16", flags=fd.FD_PLAN_LITERAL_W, num_sms=152)
 
 
 def test_workspace_layout():

@@ -150,6 +150,18 @@ def test_forced_ffma_path(fd, G):
     check(out, lse, ref_out, ref_lse, dtype=p.dtype)
 
 
+@pytest.mark.parametrize("dtype,d", [("f16", 128), ("bf16", 64)])
+def test_gqa16_tensor_core_path(fd, dtype, d):
+    """G = 16 query heads per KV head: two mma N tiles per KV tile."""
+    p = workloads.make_problem("gqa16", 3, 128, 8, d, [9000, 1, 2049], [4, 1, 3], dtype,
+                               seed=60 + d)
+    ref_out, ref_lse = oracle.decode_reference(p.q, p.k, p.v, p.seqlens, p.dtype)
+    for flags in (0, fd.FD_PLAN_TWO_LAUNCH, fd.FD_PLAN_WAITS):
+        (out, lse), dec = run_gpu(fd, p, flags=flags)
+        assert dec.info["path"] == 1 and dec.info["G"] == 16
+        check(out, lse, ref_out, ref_lse, dtype=p.dtype)
+
+
 def test_ragged_with_empty_sequences(fd):
     lens = [0, 700, 0, 1, 4096, 0]
     p = workloads.make_problem("ragged_empty", 6, 16, 4, 128, lens, [1, 3, 5, 2, 4, 1], "f16", seed=11)

@@ -238,12 +238,25 @@ def batch64_gqa4_d128_L8k_bf16(W: int = 1, seed: int = 1004) -> DecodeProblem:
     return p
 
 
+def gqa16_d128_L32k_W8(seed: int = 1005) -> DecodeProblem:
+    """B=1, Hq=128 / Hkv=8 (16 query heads per KV head), d=128, L=32768, W=8; fp16 N(0,1).
+
+    Not one of the five decode cases: a larger GQA group for the tensor-core path.
+    """
+    return make_problem("gqa16_d128_L32k_W8", 1, 128, 8, 128, [32768], 8, F16, seed)
+
+
 CASES = {
     "mha8_d64_L4k_W4": mha8_d64_L4k_W4,
     "gqa4_d128_L32k_W8": gqa4_d128_L32k_W8,
     "gqa8_d128_L128k_W8_spiky": gqa8_d128_L128k_W8_spiky,
     "ragged16_gqa4_d128": ragged16_gqa4_d128,
     "batch64_gqa4_d128_L8k_bf16": batch64_gqa4_d128_L8k_bf16,
+}
+
+# Extra shapes (not among the five decode cases).
+EXTRA = {
+    "gqa16_d128_L32k_W8": gqa16_d128_L32k_W8,
 }
 
 W_SWEEP = (1, 2, 4, 8, 16)
