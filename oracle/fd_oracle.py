@@ -50,6 +50,14 @@ def widen(x: np.ndarray, dtype: str) -> np.ndarray:
     if dtype == "bf16":
         bits = np.asarray(x, dtype=np.uint16).astype(np.uint32) << 16
         return bits.view(np.float32).astype(np.float64)
+    if dtype == "e4m3":
+        # OCP FP8 E4M3: sign, 4 exponent bits (bias 7), 3 mantissa bits; exponent 0 is
+        # subnormal (m/8 * 2^-6); code S.1111.111 is NaN; there are no infinities.
+        c = np.asarray(x, dtype=np.uint8).astype(np.int64)
+        e, m = (c >> 3) & 0xF, c & 0x7
+        mag = np.where(e == 0, m / 8.0 * 2.0 ** -6, (1.0 + m / 8.0) * 2.0 ** (e - 7))
+        mag = np.where((e == 15) & (m == 7), np.nan, mag)
+        return np.where(c & 0x80, -mag, mag)
     if dtype == "f64":
         return np.asarray(x, dtype=np.float64)
     raise ValueError(f"unknown dtype {dtype!r}")
@@ -89,7 +97,7 @@ def _cu(seqlens) -> np.ndarray:
 # Definition: single-query softmax attention (Flash Decode computes exactly this).
 # ---------------------------------------------------------------------------
 
-def decode_reference(q, k, v, seqlens, dtype="f16", scale=None, heads=None):
+def decode_reference(q, k, v, seqlens, dtype="f16", scale=None, heads=None, kv_dtype=None):
     """Plain single-token attention, fp64.
 
     For each sequence b and query head h (KV head g = h // G):
@@ -100,7 +108,8 @@ def decode_reference(q, k, v, seqlens, dtype="f16", scale=None, heads=None):
     Empty sequences give out = 0 and lse = -inf.
 
     ``heads`` (optional) is a list of (b, h) pairs; only those rows are computed
-    and the rest are left as NaN (used to sample very large cases).
+    and the rest are left as NaN (used to sample very large cases).  ``kv_dtype``
+    is the storage type of K and V when it differs from q's (e.g. "e4m3").
     Returns ``(out [B,Hq,dv] float64, lse [B,Hq] float64)``; dv = v.shape[2]
     (equal to d in every decode case; the oracle does not require it).
     """
@@ -123,8 +132,8 @@ def decode_reference(q, k, v, seqlens, dtype="f16", scale=None, heads=None):
                     out[b, h] = 0.0
                     lse[b, h] = NEG_INF
                 continue
-            K = widen(k[cu[b]:cu[b + 1], g, :], dtype)          # [L, d]
-            V = widen(v[cu[b]:cu[b + 1], g, :], dtype)          # [L, d]
+            K = widen(k[cu[b]:cu[b + 1], g, :], kv_dtype or dtype)  # [L, d]
+            V = widen(v[cu[b]:cu[b + 1], g, :], kv_dtype or dtype)  # [L, d]
             Q = widen(q[b, hs, :], dtype)                       # [n, d]
             S = scale * (Q @ K.T)                               # [n, L]
             M = S.max(axis=1, keepdims=True)
@@ -201,7 +210,8 @@ def finalize(O, m, l):
     return O / l, m + math.log(l)
 
 
-def split_kv_decode(q, k, v, seqlens, W, dtype="f16", scale=None, order=None, heads=None):
+def split_kv_decode(q, k, v, seqlens, W, dtype="f16", scale=None, order=None, heads=None,
+                    kv_dtype=None):
     """Split-KV Flash Decode, literally: segments -> partials -> combine -> normalise.
 
     ``W`` is an int or a per-sequence array.  ``order(b, h, n)`` (optional)
@@ -229,8 +239,8 @@ def split_kv_decode(q, k, v, seqlens, W, dtype="f16", scale=None, order=None, he
             qh = widen(q[b, h, :], dtype)
             parts = []
             for (s0, s1) in bounds:
-                K = widen(k[cu[b] + s0:cu[b] + s1, g, :], dtype)
-                V = widen(v[cu[b] + s0:cu[b] + s1, g, :], dtype)
+                K = widen(k[cu[b] + s0:cu[b] + s1, g, :], kv_dtype or dtype)
+                V = widen(v[cu[b] + s0:cu[b] + s1, g, :], kv_dtype or dtype)
                 parts.append(segment_partial(qh, K, V, scale))
             seq = parts if order is None else [parts[i] for i in order(b, h, len(parts))]
             O, m, l = online_softmax_combine(seq, dv)

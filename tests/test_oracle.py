@@ -483,3 +483,31 @@ def test_paged_gather_round_trip():
         # every used page appears once; spare pages are not referenced
         used = table[table >= 0]
         assert len(set(used.tolist())) == len(used) and len(used) == kp.shape[0] - 3
+
+
+def test_e4m3_widening_known_codes():
+    """OCP FP8 E4M3 codes of known values, and the round trip through the generator."""
+    codes = {0x00: 0.0, 0x38: 1.0, 0x40: 2.0, 0x3C: 1.5, 0x7E: 448.0, 0x01: 2.0 ** -9,
+             0x08: 2.0 ** -6, 0x07: 7 * 2.0 ** -9, 0xB8: -1.0, 0xC4: -3.0, 0x30: 0.5}
+    arr = np.array(list(codes), dtype=np.uint8)
+    assert np.array_equal(oracle.widen(arr, "e4m3"), np.array(list(codes.values())))
+    assert np.isnan(oracle.widen(np.array([0x7F, 0xFF], dtype=np.uint8), "e4m3")).all()
+    # every finite code survives the generator's rounding unchanged
+    finite = np.array([c for c in range(256) if c not in (0x7F, 0xFF, 0x80)], dtype=np.uint8)
+    vals = oracle.widen(finite, "e4m3").astype(np.float32)
+    assert np.array_equal(workloads.f32_to_e4m3_bits(vals), finite)
+    # rounding: halfway between 1.0 (0x38) and 1.125 (0x39) goes to the even code 0x38
+    assert workloads.f32_to_e4m3_bits(np.array([1.0625], np.float32))[0] == 0x38
+    assert workloads.f32_to_e4m3_bits(np.array([1.1875], np.float32))[0] == 0x3A
+    assert workloads.f32_to_e4m3_bits(np.array([1000.0], np.float32))[0] == 0x7E
+
+
+def test_e4m3_kv_split_matches_definition():
+    p = workloads.with_e4m3_kv(workloads.make_problem("fp8", 2, 8, 2, 16, [77, 40], 3, "f16", seed=3))
+    o1, l1 = oracle.decode_reference(p.q, p.k, p.v, p.seqlens, "f16", kv_dtype="e4m3")
+    o2, l2, _ = oracle.split_kv_decode(p.q, p.k, p.v, p.seqlens, 5, "f16", kv_dtype="e4m3")
+    assert _close(o1, o2, 1e-12) and _close(l1, l2, 1e-12)
+    # the brute force on the widened values agrees
+    ob, lb = brute_force(oracle.widen(p.q, "f16"), oracle.widen(p.k, "e4m3"),
+                         oracle.widen(p.v, "e4m3"), p.seqlens, 1 / math.sqrt(16))
+    assert _close(o1, ob, 1e-12) and _close(l1, lb, 1e-12)

@@ -50,6 +50,7 @@ class DecodeProblem:
     seed: int
     literal_w: bool = False      # run exactly W segments per sequence (no sub-chunks)
     notes: dict = field(default_factory=dict)
+    kv_dtype: str = ""           # K/V storage type when it differs from q's ("e4m3")
 
     @property
     def cu_seqlens(self) -> np.ndarray:
@@ -62,9 +63,13 @@ class DecodeProblem:
         return int(self.seqlens.astype(np.int64).sum())
 
     @property
+    def kv_type(self) -> str:
+        return self.kv_dtype or self.dtype
+
+    @property
     def kv_bytes(self) -> int:
-        """Bytes of K and V that one decode must read (2 bytes per element)."""
-        return 2 * self.n_tokens * self.Hkv * self.d * 2
+        """Bytes of K and V that one decode must read."""
+        return 2 * self.n_tokens * self.Hkv * self.d * (1 if self.kv_type == E4M3 else 2)
 
     def describe(self) -> dict:
         return {
@@ -76,7 +81,8 @@ class DecodeProblem:
             "W": (int(self.W[0]) if np.all(self.W == self.W[0]) else
                   {"min": int(self.W.min()), "max": int(self.W.max()),
                    "sum": int(self.W.sum())}),
-            "literal_w": self.literal_w, **self.notes,
+            "literal_w": self.literal_w, **({"kv_dtype": self.kv_dtype} if self.kv_dtype else {}),
+            **self.notes,
         }
 
 
@@ -97,11 +103,33 @@ def bf16_bits_to_f32(bits: np.ndarray) -> np.ndarray:
     return (np.asarray(bits, dtype=np.uint16).astype(np.uint32) << 16).view(np.float32)
 
 
+E4M3 = "e4m3"
+
+# The 127 non-negative finite values of OCP FP8 E4M3 (codes 0x00 .. 0x7E), in code order.
+_E4M3_POS = np.array(
+    [m / 8.0 * 2.0 ** -6 if e == 0 else (1.0 + m / 8.0) * 2.0 ** (e - 7)
+     for e in range(16) for m in range(8)][:127], dtype=np.float64)
+
+
+def f32_to_e4m3_bits(x: np.ndarray) -> np.ndarray:
+    """Round to OCP FP8 E4M3 (nearest, ties to even code; saturate at 448); return the codes."""
+    x = np.asarray(x, dtype=np.float32).astype(np.float64)
+    a = np.minimum(np.abs(x), 448.0)
+    hi = np.searchsorted(_E4M3_POS, a, side="left").clip(0, 126)
+    lo = (hi - 1).clip(0, 126)
+    dlo, dhi = a - _E4M3_POS[lo], _E4M3_POS[hi] - a
+    pick_hi = (dhi < dlo) | ((dhi == dlo) & (hi % 2 == 0))
+    code = np.where(pick_hi, hi, lo).astype(np.uint8)
+    return code | np.where(np.signbit(x), np.uint8(0x80), np.uint8(0))
+
+
 def to_storage(x32: np.ndarray, dtype: str) -> np.ndarray:
     if dtype == F16:
         return x32.astype(np.float16)
     if dtype == BF16:
         return f32_to_bf16_bits(x32)
+    if dtype == E4M3:
+        return f32_to_e4m3_bits(x32)
     raise ValueError(f"unknown dtype {dtype!r}")
 
 
@@ -158,6 +186,18 @@ def make_problem(name, B, Hq, Hkv, d, seqlens, W, dtype=F16, seed=0, literal_w=F
 _STREAM_PAGES = 6
 
 
+def with_e4m3_kv(problem: DecodeProblem) -> DecodeProblem:
+    """The same case with K and V rounded once to OCP FP8 E4M3 (q stays 16-bit).
+
+    Per-tensor scales are 1: standard-normal values sit well inside E4M3's range
+    (|x| <= 448).  A scaled cache folds its K scale into q and its V scale into out.
+    """
+    from dataclasses import replace
+    k = f32_to_e4m3_bits(storage_to_f32(problem.k, problem.dtype))
+    v = f32_to_e4m3_bits(storage_to_f32(problem.v, problem.dtype))
+    return replace(problem, name=problem.name + "_kv_e4m3", k=k, v=v, kv_dtype=E4M3)
+
+
 def to_paged(problem: DecodeProblem, page_size: int, spare_pages: int = 3, seed: int = None):
     """Scatter a problem's contiguous K/V into a shuffled page pool.
 
@@ -177,6 +217,9 @@ def to_paged(problem: DecodeProblem, page_size: int, spare_pages: int = 3, seed:
     shape = (total, page_size, problem.Hkv, problem.d)
     k_pool = normal(gen, shape, problem.dtype)
     v_pool = normal(gen, shape, problem.dtype)
+    if problem.kv_type == E4M3:
+        k_pool = f32_to_e4m3_bits(storage_to_f32(k_pool, problem.dtype))
+        v_pool = f32_to_e4m3_bits(storage_to_f32(v_pool, problem.dtype))
     table = np.full((problem.B, max_pages), -1, dtype=np.int32)
     cu = problem.cu_seqlens
     nxt = 0
