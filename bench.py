@@ -50,6 +50,8 @@ def parse_args(argv=None):
     ap.add_argument("--two-launch", action="store_true", help="split + combine as two kernels")
     ap.add_argument("--ffma", action="store_true", help="CUDA-core consumers even when G >= 4")
     ap.add_argument("--no-pdl", action="store_true", help="launch without programmatic dependent launch")
+    ap.add_argument("--kv", choices=["native", "e4m3"], default="native",
+                    help="K/V storage: the case's 16-bit type, or FP8 E4M3 (q stays 16-bit)")
     ap.add_argument("--paged", type=int, default=0, metavar="P",
                     help="K/V in a shuffled page pool with P tokens per page (block tables)")
     ap.add_argument("--waits", action="store_true",
@@ -67,10 +69,14 @@ def parse_args(argv=None):
 def make_problem(args):
     import workloads
     if args.workload.startswith("batch64"):
-        return workloads.batch64_gqa4_d128_L8k_bf16(W=args.W)
-    if args.workload in workloads.EXTRA:
-        return workloads.EXTRA[args.workload]()
-    return workloads.CASES[args.workload]()
+        prob = workloads.batch64_gqa4_d128_L8k_bf16(W=args.W)
+    elif args.workload in workloads.EXTRA:
+        prob = workloads.EXTRA[args.workload]()
+    else:
+        prob = workloads.CASES[args.workload]()
+    if getattr(args, "kv", "native") == "e4m3":
+        prob = workloads.with_e4m3_kv(prob)
+    return prob
 
 
 # ---------------------------------------------------------------------------
@@ -320,7 +326,7 @@ def load_peak():
 def to_device(x, dtype, device):
     import numpy as np
     import torch
-    if dtype == "f16":
+    if dtype == "f16" or x.dtype == np.uint8:
         t = torch.from_numpy(np.ascontiguousarray(x))
     else:
         t = torch.from_numpy(np.ascontiguousarray(x).view(np.int16)).view(torch.bfloat16)
@@ -350,7 +356,8 @@ def run_fd(args):
     flags = (fd.FD_PLAN_LITERAL_W if prob.literal_w else 0) | (
         fd.FD_PLAN_TWO_LAUNCH if args.two_launch else 0) | (fd.FD_PLAN_FFMA if args.ffma else 0) | (
         fd.FD_PLAN_NO_PDL if args.no_pdl else 0) | (fd.FD_PLAN_WAITS if args.waits else 0)
-    dec = fd.Decoder(prob.Hq, prob.Hkv, prob.d, prob.seqlens, prob.W, prob.dtype, flags=flags,
+    plan_dtype = "f16_e4m3kv" if prob.kv_type == "e4m3" else prob.dtype
+    dec = fd.Decoder(prob.Hq, prob.Hkv, prob.d, prob.seqlens, prob.W, plan_dtype, flags=flags,
                      chunks=args.chunks, device=device, page_size=args.paged)
     q = to_device(prob.q, prob.dtype, device)
     if args.paged:
@@ -496,6 +503,7 @@ def run_fd(args):
                 "chunks_per_segment": info["chunks"], "ctas": info["ctas"],
                 "partials_per_sequence_max": info["max_partials"],
                 "kv_bytes_per_step": kv_bytes, "two_launch": bool(args.two_launch),
+                "kv_storage": prob.kv_type,
                 "pdl": not args.no_pdl and not args.waits,
                 "kv_layout": f"paged ({args.paged} tokens per page, shuffled pool)" if args.paged
                              else "contiguous [N, Hkv, d]",
@@ -524,6 +532,7 @@ def run_fd(args):
                          "kernel": kernel_label},
             "e2e": e2e, "e2e_resident_kv": e2e_res,
             "gpu_launches": K * launches_per_step,
+            "kv_tokens_per_s": prob.n_tokens * K * world / agg["elapsed_s"],
             "clocks": clocks, "cpu_baseline": cpu,
             "gpu": props.name,
         }
@@ -539,7 +548,7 @@ def e2e_measure(fd, dec, prob, device, steps, stream, kv_resident, dev_kv=None):
     import numpy as np
     import torch
     def pinned(x):
-        if prob.dtype == "f16":
+        if prob.dtype == "f16" or x.dtype == np.uint8:
             t = torch.from_numpy(np.ascontiguousarray(x))
         else:
             t = torch.from_numpy(np.ascontiguousarray(x).view(np.int16)).view(torch.bfloat16)
@@ -556,7 +565,7 @@ def e2e_measure(fd, dec, prob, device, steps, stream, kv_resident, dev_kv=None):
     dlse = torch.empty((prob.B, prob.Hq), dtype=torch.float32, device=device)
     hout = torch.empty(dout.shape, dtype=dout.dtype).pin_memory()
     hlse = torch.empty(dlse.shape, dtype=dlse.dtype).pin_memory()
-    h2d = hq.numel() * 2 + (0 if kv_resident else 2 * prob.k.size * 2)
+    h2d = hq.numel() * 2 + (0 if kv_resident else 2 * prob.k.nbytes)
     d2h = hout.numel() * 2 + hlse.numel() * 4
 
     def one():

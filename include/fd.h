@@ -44,8 +44,13 @@ extern "C" {
 typedef struct fd_plan_s* fd_plan_t;
 
 enum fd_dtype {
-  FD_F16 = 0,  /* IEEE binary16 q, K, V and out */
-  FD_BF16 = 1  /* bfloat16 q, K, V and out */
+  FD_F16 = 0,        /* IEEE binary16 q, K, V and out */
+  FD_BF16 = 1,       /* bfloat16 q, K, V and out */
+  /* binary16 q and out over an FP8 cache: K and V are OCP FP8 E4M3 bytes (no
+   * per-tensor scale: a scaled cache folds its K scale into q and its V scale
+   * into out).  Needs d = 128 and G >= 4 (tensor-core path); the K/V bytes per
+   * token halve. */
+  FD_F16_E4M3KV = 2
 };
 
 enum fd_status {
@@ -93,7 +98,7 @@ enum fd_status {
  *            [w*S_b, min((w+1)*S_b, L_b)) with S_b = ceil(L_b / W_b); trailing
  *            segments may be empty (the pages shard the KV cache W ways; this
  *            split rule is the plan's reading).
- *   dtype    enum fd_dtype
+ *   dtype    enum fd_dtype (q / out type; K / V the same, or E4M3 bytes)
  *   flags    FD_PLAN_* bits
  *   chunks   chunks per segment C >= 1 (each segment is cut into C equal
  *            pieces, so W_b * C partials are combined); 0 = choose from the
@@ -138,7 +143,8 @@ int fd_workspace_init(fd_plan_t plan, void* workspace, cudaStream_t stream);
  * fd_decode -- the fused split-KV Flash Decode (one kernel launch on `stream`).
  *
  *   q          device [B, Hq, d] (dtype), contiguous
- *   k, v       device [N, Hkv, d] (dtype), contiguous, N = sum_b L_b
+ *   k, v       device [N, Hkv, d] (dtype; 1-byte E4M3 for FD_F16_E4M3KV), contiguous,
+ *              N = sum_b L_b
  *   out        device [B, Hq, d] (dtype), written
  *   lse        device [B, Hq] float, written (natural log); may be NULL
  *   workspace  device, fd_workspace_bytes(plan) bytes, zeroed once beforehand

@@ -18,6 +18,7 @@ from ._binding import (  # noqa: F401
     FD_ERR_TIMEOUT,
     FD_ERR_UNSUPPORTED,
     FD_F16,
+    FD_F16_E4M3KV,
     FD_MAX_BATCH,
     FD_MAX_PARTIALS,
     FD_NOALLOC_SCRATCH_BYTES,

@@ -24,6 +24,7 @@ FD_ERR_TIMEOUT = -7
 
 FD_F16 = 0
 FD_BF16 = 1
+FD_F16_E4M3KV = 2
 FD_PLAN_LITERAL_W = 0x1
 FD_PLAN_DEBUG = 0x2
 FD_PLAN_TWO_LAUNCH = 0x4
@@ -34,7 +35,7 @@ FD_PLAN_TEST_DROP_FLAG = 0x40
 FD_MAX_BATCH = 256
 FD_MAX_PARTIALS = 1024
 
-DTYPES = {"f16": FD_F16, "bf16": FD_BF16}
+DTYPES = {"f16": FD_F16, "bf16": FD_BF16, "f16_e4m3kv": FD_F16_E4M3KV}
 
 # Every symbol include/fd.h declares.
 EXPORTED = (

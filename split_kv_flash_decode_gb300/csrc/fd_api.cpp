@@ -51,15 +51,17 @@ int fd::encode_kv_map(CUtensorMap* map, const void* base, int64_t rows, int box_
                       const fd_plan_s* pl) {
   auto enc = tensor_map_encoder();
   if (!enc) return FD_ERR_CUDA;
+  const int es = fd::kv_elem_bytes(pl->path);
   const cuuint64_t dims[3] = {(cuuint64_t)pl->d, (cuuint64_t)pl->Hkv, (cuuint64_t)rows};
-  const cuuint64_t strides[2] = {(cuuint64_t)pl->d * 2, (cuuint64_t)pl->Hkv * pl->d * 2};
+  const cuuint64_t strides[2] = {(cuuint64_t)pl->d * es, (cuuint64_t)pl->Hkv * pl->d * es};
   const cuuint32_t box[3] = {(cuuint32_t)fd::box_cols_for(pl->path, pl->d), 1u,
                              (cuuint32_t)box_rows};
   const cuuint32_t estr[3] = {1u, 1u, 1u};
-  const CUtensorMapDataType ty =
-      pl->dtype == FD_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  const CUtensorMapDataType ty = pl->dtype == FD_F16    ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                                 : pl->dtype == FD_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                                        : CU_TENSOR_MAP_DATA_TYPE_UINT8;
   const CUtensorMapSwizzle swz =
-      pl->path == fd::kPathMma ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE;
+      fd::is_mma(pl->path) ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE;
   CUresult r = enc(map, ty, 3, const_cast<void*>(base), dims, strides, box, estr,
                    CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -70,8 +72,8 @@ namespace {
 
 cudaError_t launch(const fd_plan_s* pl, const fd::Params& p, int mode, int grid, cudaStream_t s) {
   const bool pdl = !(pl->flags & FD_PLAN_NO_PDL);
-  return pl->dtype == FD_F16 ? fd::launch_f16(p, pl->d, pl->G, pl->path, mode, pdl, grid, s)
-                             : fd::launch_bf16(p, pl->d, pl->G, pl->path, mode, pdl, grid, s);
+  return pl->dtype == FD_BF16 ? fd::launch_bf16(p, pl->d, pl->G, pl->path, mode, pdl, grid, s)
+                              : fd::launch_f16(p, pl->d, pl->G, pl->path, mode, pdl, grid, s);
 }
 
 }  // namespace
@@ -107,7 +109,7 @@ int plan_impl(int B, int Hq, int Hkv, int d, const int32_t* seqlens, const int32
   if (!seqlens || !W) return FD_ERR_INVALID;
   if (B < 1 || Hq < 1 || Hkv < 1 || d < 1 || chunks < 0 || num_sms < 0) return FD_ERR_INVALID;
   if (Hq % Hkv != 0) return FD_ERR_INVALID;
-  if (dtype != FD_F16 && dtype != FD_BF16) return FD_ERR_INVALID;
+  if (dtype != FD_F16 && dtype != FD_BF16 && dtype != FD_F16_E4M3KV) return FD_ERR_INVALID;
   if (flags & ~(FD_PLAN_LITERAL_W | FD_PLAN_DEBUG | FD_PLAN_TWO_LAUNCH | FD_PLAN_FFMA |
                 FD_PLAN_NO_PDL | FD_PLAN_WAITS | FD_PLAN_TEST_DROP_FLAG))
     return FD_ERR_INVALID;
@@ -120,6 +122,12 @@ int plan_impl(int B, int Hq, int Hkv, int d, const int32_t* seqlens, const int32
   if (d != 64 && d != 128) return FD_ERR_UNSUPPORTED;
   if (G != 1 && G != 2 && G != 4 && G != 8 && G != 16) return FD_ERR_UNSUPPORTED;
   if (G == 16 && (flags & FD_PLAN_FFMA)) return FD_ERR_UNSUPPORTED;  // tensor cores only
+  if (dtype == FD_F16_E4M3KV && (d != 128 || G < 4 || (flags & FD_PLAN_FFMA)))
+    return FD_ERR_UNSUPPORTED;
+  // Tensor cores whenever the GQA group covers at least half of the mma N = 8 tile.
+  const int path = dtype == FD_F16_E4M3KV                 ? fd::kPathMmaKv8
+                   : (G >= 4 && !(flags & FD_PLAN_FFMA)) ? fd::kPathMma
+                                                         : fd::kPathFfma;
 
   int64_t n_tokens = 0, sum_w = 0;
   int max_w = 0;
@@ -158,7 +166,6 @@ int plan_impl(int B, int Hq, int Hkv, int d, const int32_t* seqlens, const int32
   if ((int64_t)max_w * C > FD_MAX_PARTIALS) return FD_ERR_UNSUPPORTED;
   {
     // The combine's shared-memory scratch must fit in the ring it reuses.
-    const int path = (G >= 4 && !(flags & FD_PLAN_FFMA)) ? fd::kPathMma : fd::kPathFfma;
     const int64_t wt = (int64_t)max_w * C;
     int64_t need = (G * wt + 2 * G) * 4 + 16;                       // coefficients
     if (flags & FD_PLAN_WAITS)                                      // running state + lists
@@ -172,8 +179,7 @@ int plan_impl(int B, int Hq, int Hkv, int d, const int32_t* seqlens, const int32
   if (!pl) return FD_ERR_NOMEM;
   pl->B = B; pl->Hq = Hq; pl->Hkv = Hkv; pl->d = d; pl->G = G; pl->dtype = dtype;
   pl->flags = flags; pl->C = C; pl->num_sms = num_sms;
-  // Tensor cores whenever the GQA group covers at least half of the mma N = 8 tile.
-  pl->path = (G >= 4 && !(flags & FD_PLAN_FFMA)) ? fd::kPathMma : fd::kPathFfma;
+  pl->path = path;
   pl->page_size = page_size;
   pl->max_pages = 0;
   if (page_size)
@@ -249,7 +255,7 @@ int fd_plan_get_info(fd_plan_t pl, fd_plan_info* info) {
   info->num_sms = pl->num_sms; info->ctas = pl->ctas; info->max_partials = pl->max_partials;
   info->total_tokens = pl->n_tokens; info->total_partials = pl->total_partials;
   info->workspace_bytes = pl->ws_bytes;
-  info->kv_bytes = (uint64_t)pl->n_tokens * pl->Hkv * pl->d * 2 * 2;
+  info->kv_bytes = (uint64_t)pl->n_tokens * pl->Hkv * pl->d * 2 * fd::kv_elem_bytes(pl->path);
   info->path = pl->path;
   info->reserved = 0;
   return FD_OK;

@@ -24,20 +24,31 @@ constexpr int kThreads = (kConsumerWarps + 1) * 32;
 // Two consumer paths.  FFMA: CUDA-core dot products, unswizzled [tile][d] rows.
 // MMA: mma.sync m16n8k16 with tokens on M and the GQA heads on N, K/V staged as
 // 64-column half-tiles with the 128-byte TMA swizzle (conflict-free ldmatrix).
+// KV8: the MMA path over an FP8 (E4M3) cache, d = 128 only.  K/V land in the ring
+// as 128-byte swizzled rows of bytes; every thread loads its mma fragments from
+// there directly and widens them to f16 with integer ops.
 constexpr int kPathFfma = 0;
 constexpr int kPathMma = 1;
+constexpr int kPathMmaKv8 = 2;
 
+FD_HD constexpr bool is_mma(int path) { return path != kPathFfma; }
+// Bytes per stored K/V element.
+FD_HD constexpr int kv_elem_bytes(int path) { return path == kPathMmaKv8 ? 1 : 2; }
 // Tokens per pipeline stage.
-FD_HD constexpr int tile_for(int path) { return path == kPathMma ? 64 : 32; }
+FD_HD constexpr int tile_for(int path) { return is_mma(path) ? 64 : 32; }
 // Stages of the shared-memory ring.
 FD_HD constexpr int stages_for(int path, int d) {
-  return path == kPathMma ? (d == 128 ? 3 : 4) : (d == 128 ? 6 : 8);
+  return path == kPathMma ? (d == 128 ? 3 : 4)
+       : path == kPathMmaKv8 ? 6
+                             : (d == 128 ? 6 : 8);
 }
-// Columns (elements) of one TMA box row; MMA boxes are 128-byte swizzled rows.
-FD_HD constexpr int box_cols_for(int path, int d) { return path == kPathMma ? 64 : d; }
+// Columns (elements) of one TMA box row: 128-byte swizzled rows on the MMA paths.
+FD_HD constexpr int box_cols_for(int path, int d) {
+  return path == kPathMma ? 64 : path == kPathMmaKv8 ? 128 : d;
+}
 // Bytes of the K/V ring (also the scratch the combine reuses).
 FD_HD constexpr size_t ring_bytes_for(int path, int d) {
-  return (size_t)stages_for(path, d) * 2 * tile_for(path) * d * 2;
+  return (size_t)stages_for(path, d) * 2 * tile_for(path) * d * kv_elem_bytes(path);
 }
 // Dynamic shared memory of one CTA: the ring, the mbarriers and 1 KB of alignment slack.
 FD_HD constexpr size_t smem_bytes_for(int path, int d) { return ring_bytes_for(path, d) + 2048; }

@@ -35,6 +35,8 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include <type_traits>
+
 #include "fd_common.h"
 
 namespace fd {
@@ -220,6 +222,14 @@ __device__ __forceinline__ void mma16816<__nv_bfloat16>(float (&d)[4], const uin
       "{%8,%9}, {%0,%1,%2,%3};"
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// Two FP8 E4M3 values held in bits 8-15 and 24-31 of y (the other bits are
+// ignored) widened to an f16 pair equal to the E4M3 values times 2^-8, exactly:
+// the E4M3 exponent and mantissa bits become the low bits of the f16 exponent and
+// the top of its mantissa (exponent bias 7 vs 15), subnormals included.
+__device__ __forceinline__ uint32_t e4m3_hi_bytes_to_f16x2(uint32_t y) {
+  return ((y >> 1) & 0x3F803F80u) | (y & 0x80008000u);
 }
 
 // Two fp32 values rounded (RN) to one packed 16-bit pair: lo in bits 0-15.
@@ -677,10 +687,11 @@ __global__ void __launch_bounds__(kThreads, 2) fd_split_kernel(const __grid_cons
   constexpr int STAGES = stages_for(PATH, D);
   constexpr int BOXC = box_cols_for(PATH, D);   // columns per TMA box
   constexpr int NBOX = D / BOXC;                // boxes per tensor per stage
-  constexpr uint32_t kRowsBytes = TILE * D * sizeof(T);
+  constexpr int KVES = kv_elem_bytes(PATH);     // bytes per stored K/V element
+  constexpr uint32_t kRowsBytes = TILE * D * KVES;
   constexpr uint32_t kStageBytes = 2 * kRowsBytes;
   constexpr int NGRP_FFMA = kConsumerWarps * (32 / ((G * D > 512) ? 16 : 8));
-  constexpr int NGRP = PATH == kPathMma ? kConsumerWarps : NGRP_FFMA;
+  constexpr int NGRP = is_mma(PATH) ? kConsumerWarps : NGRP_FFMA;
   static_assert(PATH == kPathFfma || G >= 4, "the MMA path needs G >= 4 heads on N");
   static_assert(NGRP * G * D * 4 + 4 * NGRP * G * 4 <= STAGES * kStageBytes,
                 "group merge must fit in the ring");
@@ -738,11 +749,11 @@ __global__ void __launch_bounds__(kThreads, 2) fd_split_kernel(const __grid_cons
         if (p.block_table == nullptr) {
 #pragma unroll
           for (int bx = 0; bx < NBOX; ++bx)
-            tma_load_3d(dst + bx * (TILE * BOXC * 2), &p.tm_k, bx * BOXC, wk.kvh,
+            tma_load_3d(dst + bx * (TILE * BOXC * KVES), &p.tm_k, bx * BOXC, wk.kvh,
                         row0 + kt * TILE, full_bar(s), policy);
 #pragma unroll
           for (int bx = 0; bx < NBOX; ++bx)
-            tma_load_3d(dst + kRowsBytes + bx * (TILE * BOXC * 2), &p.tm_v, bx * BOXC, wk.kvh,
+            tma_load_3d(dst + kRowsBytes + bx * (TILE * BOXC * KVES), &p.tm_v, bx * BOXC, wk.kvh,
                         row0 + kt * TILE, full_bar(s), policy);
         } else {
           // Paged: one box per page piece of the tile.  Tiles start on multiples of
@@ -756,11 +767,11 @@ __global__ void __launch_bounds__(kThreads, 2) fd_split_kernel(const __grid_cons
             const int row = __ldg(bt + pg) * (1 << p.page_shift) + ((a + j) & ((1 << p.page_shift) - 1));
 #pragma unroll
             for (int bx = 0; bx < NBOX; ++bx)
-              tma_load_3d(dst + bx * (TILE * BOXC * 2) + j * BOXC * 2, &p.tm_k, bx * BOXC, wk.kvh,
+              tma_load_3d(dst + bx * (TILE * BOXC * KVES) + j * BOXC * KVES, &p.tm_k, bx * BOXC, wk.kvh,
                           row, full_bar(s), policy);
 #pragma unroll
             for (int bx = 0; bx < NBOX; ++bx)
-              tma_load_3d(dst + kRowsBytes + bx * (TILE * BOXC * 2) + j * BOXC * 2, &p.tm_v,
+              tma_load_3d(dst + kRowsBytes + bx * (TILE * BOXC * KVES) + j * BOXC * KVES, &p.tm_v,
                           bx * BOXC, wk.kvh, row, full_bar(s), policy);
           }
         }
@@ -771,6 +782,182 @@ __global__ void __launch_bounds__(kThreads, 2) fd_split_kernel(const __grid_cons
       }
     }
     __syncthreads();
+  } else if constexpr (PATH == kPathMmaKv8) {
+    // ---------------- MMA consumers over an FP8 (E4M3) cache ----------------
+    // Fragments are loaded straight from the 128-byte swizzled byte rows.  Two index
+    // permutations make each thread's fragment bytes contiguous: the reduction index
+    // of S = K q^T (k-step kk, thread quad t covers d = 16(2t + kk/4) + 4(kk%4) +
+    // {0,1} for a0/a1/b0 and + {2,3} for a2/a3/b1, applied to K and to q alike), and
+    // the rows of O^T (row g / g+8 of m-tile mi is dim 16g + 2mi / 16g + 2mi + 1,
+    // undone when the state is written).  Widened values are E4M3 * 2^-8: the 2^8
+    // folds exactly into the score scale (K) and into O (V).
+    static_assert(D == 128, "FP8 K/V rows are single 128-byte swizzle rows");
+    constexpr int KT = 8;                   // k-steps of S, m-tiles of O^T
+    constexpr int NT = G >= 8 ? G / 8 : 1;  // N tiles of 8 query heads
+    const int g = lane >> 2, t = lane & 3, qcol = 2 * t;
+    uint32_t qb[NT][KT][2];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      const int head = nt * 8 + g;
+      const T* qh = reinterpret_cast<const T*>(p.q) +
+                    ((int64_t)wk.b * p.Hq + wk.kvh * G + (head < G ? head : 0)) * D;
+#pragma unroll
+      for (int kk = 0; kk < KT; ++kk) {
+        const int dq = 16 * (2 * t + kk / 4) + 4 * (kk % 4);
+        qb[nt][kk][0] = head < G ? *reinterpret_cast<const uint32_t*>(qh + dq) : 0u;
+        qb[nt][kk][1] = head < G ? *reinterpret_cast<const uint32_t*>(qh + dq + 2) : 0u;
+      }
+    }
+    float o[NT][KT][4];
+    float mA[NT], mB[NT], lA[NT], lB[NT];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+#pragma unroll
+      for (int mi = 0; mi < KT; ++mi) o[nt][mi][0] = o[nt][mi][1] = o[nt][mi][2] = o[nt][mi][3] = 0.f;
+      mA[nt] = mB[nt] = -INFINITY;
+      lA[nt] = lB[nt] = 0.f;
+    }
+    const float scale = p.scale_log2 * 256.f;
+    const int tok0 = warp * 16;
+
+    for (int kt = 0; kt < ntiles; ++kt) {
+      const int s = kt % STAGES;
+      const bool ok = mbar_wait(full_bar(s), (kt / STAGES) & 1);
+      if (__any_sync(0xffffffffu, !ok || *(volatile int*)&sm_abort != 0)) {
+        if (!ok) {
+          atomicOr(p.status, kStatusTimeout);
+          *(volatile int*)&sm_abort = 1;
+        }
+        break;
+      }
+      const int ntok = min(TILE, wk.t1 - (wk.t0 + kt * TILE));
+      if (tok0 < ntok) {
+        // K: rows tok0 + g (+8), 16-byte chunks 2t and 2t + 1.
+        uint4 kw[2][2];
+#pragma unroll
+        for (int rh = 0; rh < 2; ++rh)
+#pragma unroll
+          for (int grp = 0; grp < 2; ++grp) {
+            const int r = tok0 + g + 8 * rh, c = 2 * t + grp;
+            kw[rh][grp] = *reinterpret_cast<const uint4*>(
+                smem + (size_t)s * kStageBytes + r * 128 + ((c ^ (r & 7)) << 4));
+          }
+        float sc[NT][4];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
+#pragma unroll
+        for (int kk = 0; kk < KT; ++kk) {
+          const uint4& w0 = kw[0][kk >> 2];
+          const uint4& w1 = kw[1][kk >> 2];
+          const int wi = kk & 3;
+          const uint32_t x0 = wi == 0 ? w0.x : wi == 1 ? w0.y : wi == 2 ? w0.z : w0.w;
+          const uint32_t x1 = wi == 0 ? w1.x : wi == 1 ? w1.y : wi == 2 ? w1.z : w1.w;
+          uint32_t a[4];
+          a[0] = e4m3_hi_bytes_to_f16x2(__byte_perm(x0, 0u, 0x1000u));  // bytes 0, 1
+          a[1] = e4m3_hi_bytes_to_f16x2(__byte_perm(x1, 0u, 0x1000u));
+          a[2] = e4m3_hi_bytes_to_f16x2(__byte_perm(x0, 0u, 0x3020u));  // bytes 2, 3
+          a[3] = e4m3_hi_bytes_to_f16x2(__byte_perm(x1, 0u, 0x3020u));
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt) mma16816<T>(sc[nt], a, qb[nt][kk][0], qb[nt][kk][1]);
+        }
+        const bool v0 = tok0 + g < ntok, v1 = tok0 + g + 8 < ntok;
+        uint32_t pb0[NT], pb1[NT];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+          const float sA0 = v0 ? sc[nt][0] * scale : -INFINITY;
+          const float sB0 = v0 ? sc[nt][1] * scale : -INFINITY;
+          const float sA1 = v1 ? sc[nt][2] * scale : -INFINITY;
+          const float sB1 = v1 ? sc[nt][3] * scale : -INFINITY;
+          float xA = fmaxf(sA0, sA1), xB = fmaxf(sB0, sB1);
+#pragma unroll
+          for (int off = 4; off < 32; off <<= 1) {
+            xA = fmaxf(xA, __shfl_xor_sync(0xffffffffu, xA, off));
+            xB = fmaxf(xB, __shfl_xor_sync(0xffffffffu, xB, off));
+          }
+          if (xA > mA[nt] + kRescaleThreshold) {
+            const float corr = ex2(mA[nt] - xA);
+            lA[nt] *= corr;
+#pragma unroll
+            for (int mi = 0; mi < KT; ++mi) { o[nt][mi][0] *= corr; o[nt][mi][2] *= corr; }
+            mA[nt] = xA;
+          }
+          if (xB > mB[nt] + kRescaleThreshold) {
+            const float corr = ex2(mB[nt] - xB);
+            lB[nt] *= corr;
+#pragma unroll
+            for (int mi = 0; mi < KT; ++mi) { o[nt][mi][1] *= corr; o[nt][mi][3] *= corr; }
+            mB[nt] = xB;
+          }
+          const float pA0 = ex2(sA0 - mA[nt]), pB0 = ex2(sB0 - mB[nt]);
+          const float pA1 = ex2(sA1 - mA[nt]), pB1 = ex2(sB1 - mB[nt]);
+          lA[nt] += pA0 + pA1;
+          lB[nt] += pB0 + pB1;
+          pb0[nt] = movmatrix_trans(pack2<T>(pA0, pB0));
+          pb1[nt] = movmatrix_trans(pack2<T>(pA1, pB1));
+        }
+        // V^T: token rows tok0 + 2t, +1, +8, +9; the 16-byte chunk g (dims 16g ..).
+        uint4 vw[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int r = tok0 + 2 * t + (i & 1) + 8 * (i >> 1);
+          vw[i] = *reinterpret_cast<const uint4*>(smem + (size_t)s * kStageBytes + kRowsBytes +
+                                                  r * 128 + ((g ^ (r & 7)) << 4));
+        }
+#pragma unroll
+        for (int mi = 0; mi < KT; ++mi) {
+          const int wi = mi >> 1;
+          const uint32_t k = 2u * (mi & 1);
+          const uint32_t y0 = wi == 0 ? vw[0].x : wi == 1 ? vw[0].y : wi == 2 ? vw[0].z : vw[0].w;
+          const uint32_t y1 = wi == 0 ? vw[1].x : wi == 1 ? vw[1].y : wi == 2 ? vw[1].z : vw[1].w;
+          const uint32_t y2 = wi == 0 ? vw[2].x : wi == 1 ? vw[2].y : wi == 2 ? vw[2].z : vw[2].w;
+          const uint32_t y3 = wi == 0 ? vw[3].x : wi == 1 ? vw[3].y : wi == 2 ? vw[3].z : vw[3].w;
+          // byte k (dim 16g + 2mi) and k + 1 (dim 16g + 2mi + 1) of two token rows
+          const uint32_t sel0 = ((4u + k) << 12) | (k << 4);
+          const uint32_t sel1 = ((5u + k) << 12) | ((k + 1u) << 4);
+          uint32_t a[4];
+          a[0] = e4m3_hi_bytes_to_f16x2(__byte_perm(y0, y1, sel0));
+          a[1] = e4m3_hi_bytes_to_f16x2(__byte_perm(y0, y1, sel1));
+          a[2] = e4m3_hi_bytes_to_f16x2(__byte_perm(y2, y3, sel0));
+          a[3] = e4m3_hi_bytes_to_f16x2(__byte_perm(y2, y3, sel1));
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt) mma16816<T>(o[nt][mi], a, pb0[nt], pb1[nt]);
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(empty_bar(s));
+    }
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+#pragma unroll
+      for (int off = 4; off < 32; off <<= 1) {
+        lA[nt] += __shfl_xor_sync(0xffffffffu, lA[nt], off);
+        lB[nt] += __shfl_xor_sync(0xffffffffu, lB[nt], off);
+      }
+    }
+    __syncthreads();  // ring drained: reuse it for the per-warp states
+    if (*(volatile int*)&sm_abort == 0) {
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        const int hA = nt * 8 + qcol;
+        if (hA < G) {
+          float* accA = sm_acc + (warp * G + hA) * D;
+          float* accB = accA + D;
+#pragma unroll
+          for (int mi = 0; mi < KT; ++mi) {
+            accA[16 * g + 2 * mi] = o[nt][mi][0] * 256.f;
+            accB[16 * g + 2 * mi] = o[nt][mi][1] * 256.f;
+            accA[16 * g + 2 * mi + 1] = o[nt][mi][2] * 256.f;
+            accB[16 * g + 2 * mi + 1] = o[nt][mi][3] * 256.f;
+          }
+          if (g == 0) {
+            sm_m[warp * G + hA] = mA[nt];
+            sm_m[warp * G + hA + 1] = mB[nt];
+            sm_l[warp * G + hA] = lA[nt];
+            sm_l[warp * G + hA + 1] = lB[nt];
+          }
+        }
+      }
+    }
   } else if constexpr (PATH == kPathMma) {
     // ---------------- MMA consumers ----------------
     constexpr int KT = D / 16;            // k-steps of S = K Q^T, m-tiles of O^T
@@ -1126,6 +1313,9 @@ cudaError_t launch_typed(const Params& p, int d, int G, int path, int mode, bool
   FD_CASE(128, 4, kPathFfma) FD_CASE(128, 8, kPathFfma)
   FD_CASE(64, 4, kPathMma) FD_CASE(64, 8, kPathMma) FD_CASE(64, 16, kPathMma)
   FD_CASE(128, 4, kPathMma) FD_CASE(128, 8, kPathMma) FD_CASE(128, 16, kPathMma)
+  if constexpr (std::is_same<T, __half>::value) {
+    FD_CASE(128, 4, kPathMmaKv8) FD_CASE(128, 8, kPathMmaKv8) FD_CASE(128, 16, kPathMmaKv8)
+  }
 #undef FD_CASE
   return cudaErrorInvalidValue;
 }

@@ -83,7 +83,7 @@ extern "C" int fd_decode_noalloc(fd_plan_t pl, const void* q, const void* k, con
   // arrival counters must start at zero, so clear them on the stream first.
   cudaError_t err = cudaMemsetAsync(ws, 0, pl->off_part, stream);
   if (err == cudaSuccess) {
-    auto launch = pl->dtype == FD_F16 ? fd::launch_f16 : fd::launch_bf16;
+    auto launch = pl->dtype == FD_BF16 ? fd::launch_bf16 : fd::launch_f16;
     const bool pdl = !(pl->flags & FD_PLAN_NO_PDL);
     if (pl->flags & FD_PLAN_TWO_LAUNCH) {
       err = launch(p, pl->d, pl->G, pl->path, 1, pdl, pl->ctas, stream);

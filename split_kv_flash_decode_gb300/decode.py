@@ -9,7 +9,9 @@ import torch
 
 from . import _binding as B
 
-_TORCH_DTYPE = {"f16": torch.float16, "bf16": torch.bfloat16}
+# q / out type and K / V storage type of each plan dtype.
+_TORCH_DTYPE = {"f16": torch.float16, "bf16": torch.bfloat16, "f16_e4m3kv": torch.float16}
+_KV_DTYPE = {"f16": torch.float16, "bf16": torch.bfloat16, "f16_e4m3kv": torch.uint8}
 
 
 class Decoder:
@@ -44,8 +46,9 @@ class Decoder:
     def _check(self, name, t, shape):
         if t.device != self.device:
             raise ValueError(f"{name} is on {t.device}, expected {self.device}")
-        if t.dtype != _TORCH_DTYPE[self.dtype]:
-            raise ValueError(f"{name} has dtype {t.dtype}, expected {_TORCH_DTYPE[self.dtype]}")
+        want = (_KV_DTYPE if name in ("k", "v", "k_pages", "v_pages") else _TORCH_DTYPE)[self.dtype]
+        if t.dtype != want:
+            raise ValueError(f"{name} has dtype {t.dtype}, expected {want}")
         if tuple(t.shape) != tuple(shape):
             raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
         if not t.is_contiguous():
@@ -96,6 +99,8 @@ class Decoder:
 def flash_decode(q, k, v, seqlens, W, flags=0, chunks=0):
     """One-shot decode: plan, allocate, run.  Returns (out, lse)."""
     dtype = {torch.float16: "f16", torch.bfloat16: "bf16"}[q.dtype]
+    if k.dtype == torch.uint8:
+        dtype = "f16_e4m3kv"
     dec = Decoder(q.shape[1], k.shape[1], q.shape[2], seqlens, W, dtype, flags, chunks,
                   device=q.device)
     return dec(q, k, v)

@@ -83,7 +83,8 @@ def test_plan_validation(args, code):
 
 
 def test_plan_bad_dtype_flags_chunks():
-    assert _raw_plan(1, 8, 8, 128, [10], [1], dtype=2) == fd.FD_ERR_INVALID
+    assert _raw_plan(1, 8, 8, 128, [10], [1], dtype=3) == fd.FD_ERR_INVALID
+    assert _raw_plan(1, 8, 8, 128, [10], [1], dtype=2) == fd.FD_ERR_UNSUPPORTED  # FP8 K/V: G >= 4
     assert _raw_plan(1, 8, 8, 128, [10], [1], flags=0x80) == fd.FD_ERR_INVALID
     assert _raw_plan(1, 8, 8, 128, [10], [1], chunks=-1) == fd.FD_ERR_INVALID
     assert _raw_plan(1, 8, 8, 128, [10], [600], chunks=2) == fd.FD_ERR_UNSUPPORTED
@@ -169,6 +170,15 @@ def test_consumer_path_choice():
     with pytest.raises(fd.FdError) as ei:
         fd.fd_plan(1, 128, 8, 128, [1000], 2, "f16", flags=fd.FD_PLAN_FFMA, num_sms=152)
     assert ei.value.status == fd.FD_ERR_UNSUPPORTED
+
+
+def test_fp8_kv_plan_rules():
+    p = fd.fd_plan(1, 32, 8, 128, [4096], 4, "f16_e4m3kv", num_sms=152)
+    assert p.info["path"] == 2 and p.info["kv_bytes"] == 4096 * 8 * 128 * 2
+    for Hq, d, flags in ((16, 128, 0), (32, 128, fd.FD_PLAN_FFMA), (32, 64, 0)):
+        with pytest.raises(fd.FdError) as ei:
+            fd.fd_plan(1, Hq, 8, d, [4096], 4, "f16_e4m3kv", flags=flags, num_sms=152)
+        assert ei.value.status == fd.FD_ERR_UNSUPPORTED
 
 
 def test_combine_scratch_limit():

@@ -32,11 +32,20 @@ def fd():
 
 def to_torch(x, dtype, device="cuda"):
     import torch
-    if dtype == "f16":
+    if x.dtype == np.uint8 or dtype in ("f16", "f16_e4m3kv"):   # uint8 = FP8 E4M3 codes
         t = torch.from_numpy(np.ascontiguousarray(x))
     else:
         t = torch.from_numpy(np.ascontiguousarray(x).view(np.int16)).view(torch.bfloat16)
     return t.to(device)
+
+
+def plan_dtype(p):
+    return "f16_e4m3kv" if p.kv_type == "e4m3" else p.dtype
+
+
+def reference(p):
+    return oracle.decode_reference(p.q, p.k, p.v, p.seqlens, p.dtype,
+                                   kv_dtype=p.kv_dtype or None)
 
 
 def out_to_f64(t):
@@ -45,7 +54,7 @@ def out_to_f64(t):
 
 
 def run_gpu(fd, p, chunks=0, flags=0, repeat=1):
-    dec = fd.Decoder(p.Hq, p.Hkv, p.d, p.seqlens, p.W, p.dtype,
+    dec = fd.Decoder(p.Hq, p.Hkv, p.d, p.seqlens, p.W, plan_dtype(p),
                      flags=flags | (fd.FD_PLAN_LITERAL_W if p.literal_w else 0), chunks=chunks)
     q, k, v = (to_torch(x, p.dtype) for x in (p.q, p.k, p.v))
     outs = []
@@ -279,7 +288,7 @@ def test_fine_grained_waits_needs_coresidency(fd):
 def run_paged(fd, p, page_size, flags=0, chunks=0):
     import torch
     kp, vp, table = workloads.to_paged(p, page_size)
-    dec = fd.Decoder(p.Hq, p.Hkv, p.d, p.seqlens, p.W, p.dtype, flags=flags, chunks=chunks,
+    dec = fd.Decoder(p.Hq, p.Hkv, p.d, p.seqlens, p.W, plan_dtype(p), flags=flags, chunks=chunks,
                      page_size=page_size)
     q = to_torch(p.q, p.dtype)
     out, lse = dec.decode_paged(q, to_torch(kp, p.dtype), to_torch(vp, p.dtype),
@@ -307,6 +316,30 @@ def test_paged_cache_full_32k_and_variants(fd):
     ref_out, ref_lse = oracle.decode_reference(p.q, p.k, p.v, p.seqlens, p.dtype)
     for flags in (0, fd.FD_PLAN_TWO_LAUNCH, fd.FD_PLAN_WAITS):
         out, lse, _, _ = run_paged(fd, p, 64, flags=flags)
+        check(out, lse, ref_out, ref_lse)
+
+
+@pytest.mark.parametrize("G", [4, 8, 16])
+def test_fp8_e4m3_kv_cache(fd, G):
+    """fp16 q over an FP8 (E4M3) cache, against the oracle on the same E4M3 values."""
+    base = workloads.make_problem("fp8kv", 3, 8 * G, 8, 128, [7000, 0, 2049], [4, 2, 3], "f16",
+                                  seed=70 + G)
+    p = workloads.with_e4m3_kv(base)
+    ref_out, ref_lse = reference(p)
+    for flags in (0, fd.FD_PLAN_TWO_LAUNCH, fd.FD_PLAN_WAITS):
+        (out, lse), dec = run_gpu(fd, p, flags=flags)
+        assert dec.info["path"] == 2 and dec.info["kv_bytes"] == p.kv_bytes
+        check(out, lse, ref_out, ref_lse, dtype="f16")
+    for page_size in (16, 128):
+        out, lse, _, _ = run_paged(fd, p, page_size)
+        check(out, lse, ref_out, ref_lse, dtype="f16")
+
+
+def test_fp8_e4m3_kv_full_cases(fd):
+    for make in (workloads.gqa4_d128_L32k_W8, workloads.gqa8_d128_L128k_W8_spiky):
+        p = workloads.with_e4m3_kv(make())
+        ref_out, ref_lse = reference(p)
+        (out, lse), _ = run_gpu(fd, p)
         check(out, lse, ref_out, ref_lse)
 
 
