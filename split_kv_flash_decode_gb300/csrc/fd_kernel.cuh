@@ -224,12 +224,18 @@ __device__ __forceinline__ void mma16816<__nv_bfloat16>(float (&d)[4], const uin
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
-// Two FP8 E4M3 values held in bits 8-15 and 24-31 of y (the other bits are
-// ignored) widened to an f16 pair equal to the E4M3 values times 2^-8, exactly:
-// the E4M3 exponent and mantissa bits become the low bits of the f16 exponent and
-// the top of its mantissa (exponent bias 7 vs 15), subnormals included.
-__device__ __forceinline__ uint32_t e4m3_hi_bytes_to_f16x2(uint32_t y) {
-  return ((y >> 1) & 0x3F803F80u) | (y & 0x80008000u);
+// Two FP8 E4M3 values widened to an f16 pair equal to the E4M3 values times 2^-8,
+// exactly: the E4M3 exponent and mantissa bits become the low bits of the f16
+// exponent and the top of its mantissa (exponent bias 7 vs 15), subnormals
+// included.  `sel` is a prmt selector over the bytes of {a, b} that puts, in each
+// 16-bit half, an E4M3 byte in the low byte and that byte sign-extended (selector
+// nibble bit 3) in the high byte.  Shifting left by 7 then moves the byte's
+// exponent and mantissa to bits 7-13 and the sign copy to bit 15; the mask clears
+// bit 14 (the byte's own sign bit) and the bits below 7.
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2_scaled(uint32_t a, uint32_t b, uint32_t sel) {
+  uint32_t y;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(y) : "r"(a), "r"(b), "r"(sel));
+  return (y * 128u) & 0xBF80BF80u;
 }
 
 // Two fp32 values rounded (RN) to one packed 16-bit pair: lo in bits 0-15.
@@ -853,10 +859,10 @@ __global__ void __launch_bounds__(kThreads, 2) fd_split_kernel(const __grid_cons
           const uint32_t x0 = wi == 0 ? w0.x : wi == 1 ? w0.y : wi == 2 ? w0.z : w0.w;
           const uint32_t x1 = wi == 0 ? w1.x : wi == 1 ? w1.y : wi == 2 ? w1.z : w1.w;
           uint32_t a[4];
-          a[0] = e4m3_hi_bytes_to_f16x2(__byte_perm(x0, 0u, 0x1000u));  // bytes 0, 1
-          a[1] = e4m3_hi_bytes_to_f16x2(__byte_perm(x1, 0u, 0x1000u));
-          a[2] = e4m3_hi_bytes_to_f16x2(__byte_perm(x0, 0u, 0x3020u));  // bytes 2, 3
-          a[3] = e4m3_hi_bytes_to_f16x2(__byte_perm(x1, 0u, 0x3020u));
+          a[0] = e4m3x2_to_f16x2_scaled(x0, 0u, 0x9180u);  // bytes 0, 1
+          a[1] = e4m3x2_to_f16x2_scaled(x1, 0u, 0x9180u);
+          a[2] = e4m3x2_to_f16x2_scaled(x0, 0u, 0xB3A2u);  // bytes 2, 3
+          a[3] = e4m3x2_to_f16x2_scaled(x1, 0u, 0xB3A2u);
 #pragma unroll
           for (int nt = 0; nt < NT; ++nt) mma16816<T>(sc[nt], a, qb[nt][kk][0], qb[nt][kk][1]);
         }
@@ -911,14 +917,15 @@ __global__ void __launch_bounds__(kThreads, 2) fd_split_kernel(const __grid_cons
           const uint32_t y1 = wi == 0 ? vw[1].x : wi == 1 ? vw[1].y : wi == 2 ? vw[1].z : vw[1].w;
           const uint32_t y2 = wi == 0 ? vw[2].x : wi == 1 ? vw[2].y : wi == 2 ? vw[2].z : vw[2].w;
           const uint32_t y3 = wi == 0 ? vw[3].x : wi == 1 ? vw[3].y : wi == 2 ? vw[3].z : vw[3].w;
-          // byte k (dim 16g + 2mi) and k + 1 (dim 16g + 2mi + 1) of two token rows
-          const uint32_t sel0 = ((4u + k) << 12) | (k << 4);
-          const uint32_t sel1 = ((5u + k) << 12) | ((k + 1u) << 4);
+          // byte k (dim 16g + 2mi) and k + 1 (dim 16g + 2mi + 1) of two token rows:
+          // low half <- row of the first word, high half <- row of the second
+          const uint32_t sel0 = ((12u + k) << 12) | ((4u + k) << 8) | ((8u + k) << 4) | k;
+          const uint32_t sel1 = ((13u + k) << 12) | ((5u + k) << 8) | ((9u + k) << 4) | (k + 1u);
           uint32_t a[4];
-          a[0] = e4m3_hi_bytes_to_f16x2(__byte_perm(y0, y1, sel0));
-          a[1] = e4m3_hi_bytes_to_f16x2(__byte_perm(y0, y1, sel1));
-          a[2] = e4m3_hi_bytes_to_f16x2(__byte_perm(y2, y3, sel0));
-          a[3] = e4m3_hi_bytes_to_f16x2(__byte_perm(y2, y3, sel1));
+          a[0] = e4m3x2_to_f16x2_scaled(y0, y1, sel0);
+          a[1] = e4m3x2_to_f16x2_scaled(y0, y1, sel1);
+          a[2] = e4m3x2_to_f16x2_scaled(y2, y3, sel0);
+          a[3] = e4m3x2_to_f16x2_scaled(y2, y3, sel1);
 #pragma unroll
           for (int nt = 0; nt < NT; ++nt) mma16816<T>(o[nt][mi], a, pb0[nt], pb1[nt]);
         }
