@@ -491,7 +491,7 @@ def run_fd(args):
 
     info = dec.info
     kernel_label = ("fd_split_kernel+fd_combine_kernel" if args.two_launch else "fd_split_kernel") + (
-        "/mma" if info["path"] == 1 else "/ffma") + ("/waits" if args.waits else "")
+        {0: "/ffma", 1: "/mma", 2: "/mma-fp8"}[info["path"]]) + ("/waits" if args.waits else "")
     if rank == 0:
         line = {
             "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": K,
@@ -510,8 +510,8 @@ def run_fd(args):
                 "combine": "fine-grained waits (slot 0 combines as flags arrive)" if args.waits
                            else ("separate combine kernel" if args.two_launch
                                  else "last arriver (atomic counter)"),
-                "consumer": "mma.sync m16n8k16 (tensor cores)" if info["path"] == 1
-                            else "FFMA (CUDA cores)",
+                "consumer": {0: "FFMA (CUDA cores)", 1: "mma.sync m16n8k16 (tensor cores)",
+                             2: "mma.sync m16n8k16 over E4M3 K/V widened in registers"}[info["path"]],
                 "l2_policy": f"K/V rotated over {copies} device copies ({copies * kv_bytes / 1e6:.0f} MB"
                              f" >= 4 x L2 {l2 / 1e6:.0f} MB)" if copies > 1 else
                              f"K/V {kv_bytes / 1e6:.0f} MB per step > 4 x L2 {l2 / 1e6:.0f} MB",
