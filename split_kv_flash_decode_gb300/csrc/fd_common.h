@@ -46,6 +46,10 @@ FD_HD constexpr int stages_for(int path, int d) {
 FD_HD constexpr int box_cols_for(int path, int d) {
   return path == kPathMma ? 64 : path == kPathMmaKv8 ? 128 : d;
 }
+// K/V tiles per CTA that the split kernel prefetches into L2 before it waits for
+// the previous kernel in the stream (4 measured best for fp16 and fp8 caches at
+// 32K and 128K tokens; 2 and 8 were slower).
+constexpr int kL2PrefetchTiles = 4;
 // Bytes of the K/V ring (also the scratch the combine reuses).
 FD_HD constexpr size_t ring_bytes_for(int path, int d) {
   return (size_t)stages_for(path, d) * 2 * tile_for(path) * d * kv_elem_bytes(path);

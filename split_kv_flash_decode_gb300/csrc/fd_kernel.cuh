@@ -116,6 +116,14 @@ __device__ __forceinline__ uint64_t l2_evict_first_policy() {
 }
 
 // 3-D tiled TMA load: box at coordinates (c0, c1, c2) of `map` into shared memory.
+// Bring one box of a tensor map into L2 (no shared-memory destination, no barrier).
+__device__ __forceinline__ void tma_prefetch_l2_3d(const CUtensorMap* map, int c0, int c1, int c2) {
+  asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(c0), "r"(c1), "r"(c2)
+               : "memory");
+}
+
 __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, int c0, int c1,
                                             int c2, uint32_t bar, uint64_t policy) {
   asm volatile(
@@ -310,7 +318,7 @@ __device__ __forceinline__ void fence_proxy_async_global() {
   asm volatile("fence.proxy.async.global;" ::: "memory");
 }
 
-// Write out[b, h, 4*c4 .. 4*c4+3] and, for c4 == 0, nothing else.
+// Write out[b, h, 4*c4 .. 4*c4+3] = a / lam (zero where lam == 0).
 template <typename T>
 __device__ __forceinline__ void store_out4(T* dst, float4 a, float lam) {
   dst[0] = Elem<T>::from_f(lam > 0.f ? a.x / lam : 0.f);
@@ -319,58 +327,84 @@ __device__ __forceinline__ void store_out4(T* dst, float4 a, float lam) {
   dst[3] = Elem<T>::from_f(lam > 0.f ? a.w / lam : 0.f);
 }
 
+__device__ __forceinline__ float warp_max(float x) {
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, off));
+  return x;
+}
+__device__ __forceinline__ float warp_sum(float x) {
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) x += __shfl_xor_sync(0xffffffffu, x, off);
+  return x;
+}
+
 // OnlineSoftmaxCombine of the Wtot partials of (b, kvh) for query heads
-// [g0, g0 + ng).  `rec` (shared memory) holds their records, head-major
-// [ng][wtot][D + 4]; `coef` holds ng * wtot + 2 * ng floats.  The summation order
-// is fixed (per-lane strides, a fixed shuffle tree, partial index order for O),
-// so the result does not depend on the order in which the partials arrived.
+// [g0, g0 + ng), from their records in shared memory, head-major
+// [ng][wtot][D + 4].  One warp per head: M is the max of the partial maxima,
+// Lambda = sum_w exp2(m_w - M) l_w, O = sum_w exp2(m_w - M) O_w; lane l owns the
+// D/32 output dimensions starting at (D/32) l, and receives each coefficient by
+// shuffle from the lane that computed it.  The order of every sum is fixed
+// (partial index order for O, a fixed shuffle tree for Lambda), so the result
+// does not depend on the order in which the partials arrived.
 template <typename T, int D, int G>
 __device__ __forceinline__ void combine_from_smem(const Params& p, int b, int kvh, int wtot,
-                                                  int g0, int ng, const float* rec, float* coef) {
+                                                  int g0, int ng, const float* rec) {
   constexpr int RS = record_floats(D);
-  float* ML = coef + ng * wtot;
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  constexpr int V = D / 32;  // 4 (d = 128) or 2 (d = 64)
+  static_assert(V == 2 || V == 4, "head dim must be 64 or 128");
+  constexpr int U = 8;       // records in flight per lane
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   constexpr int kWarps = kThreads / 32;
-  for (int g = warp; g < ng; g += kWarps) {
-    float M = -INFINITY, lam = 0.f;
-    for (int w = lane; w < wtot; w += 32) {
-      const float* r = rec + (size_t)(g * wtot + w) * RS + D;
-      ml_merge(M, lam, r[0], r[1]);
-    }
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) {
-      const float m2 = __shfl_xor_sync(0xffffffffu, M, off);
-      const float l2 = __shfl_xor_sync(0xffffffffu, lam, off);
-      ml_merge(M, lam, m2, l2);
-    }
-    for (int w = lane; w < wtot; w += 32)
-      coef[g * wtot + w] =
-          (M == -INFINITY) ? 0.f : ex2(rec[(size_t)(g * wtot + w) * RS + D] - M);
-    if (lane == 0) {
-      ML[2 * g] = M;
-      ML[2 * g + 1] = lam;
-    }
-  }
-  __syncthreads();
   T* out = reinterpret_cast<T*>(p.out);
-  for (int v = tid; v < ng * (D / 4); v += kThreads) {
-    const int g = v / (D / 4), c4 = v - (v / (D / 4)) * (D / 4);
-    const float4* r = reinterpret_cast<const float4*>(rec + (size_t)g * wtot * RS) + c4;
-    const float* cg = coef + g * wtot;
-    float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int w = 0; w < wtot; ++w) {
-      const float4 x = r[(size_t)w * (RS / 4)];
-      const float c = cg[w];
-      a.x = fmaf(c, x.x, a.x);
-      a.y = fmaf(c, x.y, a.y);
-      a.z = fmaf(c, x.z, a.z);
-      a.w = fmaf(c, x.w, a.w);
+  for (int g = warp; g < ng; g += kWarps) {
+    const float* rg = rec + (size_t)g * wtot * RS;
+    float M = -INFINITY;
+    for (int w = lane; w < wtot; w += 32) M = fmaxf(M, rg[(size_t)w * RS + D]);
+    M = warp_max(M);
+    float lam = 0.f;
+    float acc[V];
+#pragma unroll
+    for (int j = 0; j < V; ++j) acc[j] = 0.f;
+    for (int w0 = 0; w0 < wtot; w0 += 32) {
+      const int n = min(32, wtot - w0);
+      float cl = 0.f;
+      if (lane < n && M != -INFINITY) {
+        const float2 ml = *reinterpret_cast<const float2*>(rg + (size_t)(w0 + lane) * RS + D);
+        cl = ex2(ml.x - M);  // exp2(-inf) = 0 for an empty partial
+        lam = fmaf(cl, ml.y, lam);
+      }
+      const float* base = rg + (size_t)w0 * RS + V * lane;
+      int i = 0;
+      for (; i + U <= n; i += U) {
+        float x[U][V], c[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+          if constexpr (V == 4) {
+            const float4 t = *reinterpret_cast<const float4*>(base + (size_t)(i + u) * RS);
+            x[u][0] = t.x; x[u][1] = t.y; x[u][2] = t.z; x[u][3] = t.w;
+          } else {
+            const float2 t = *reinterpret_cast<const float2*>(base + (size_t)(i + u) * RS);
+            x[u][0] = t.x; x[u][1] = t.y;
+          }
+          c[u] = __shfl_sync(0xffffffffu, cl, i + u);
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u)
+#pragma unroll
+          for (int j = 0; j < V; ++j) acc[j] = fmaf(c[u], x[u][j], acc[j]);
+      }
+      for (; i < n; ++i) {
+        const float c = __shfl_sync(0xffffffffu, cl, i);
+#pragma unroll
+        for (int j = 0; j < V; ++j) acc[j] = fmaf(c, base[(size_t)i * RS + j], acc[j]);
+      }
     }
-    store_out4<T>(out + ((int64_t)b * p.Hq + kvh * G + g0 + g) * D + 4 * c4, a, ML[2 * g + 1]);
-  }
-  if (tid < ng && p.lse != nullptr) {
-    const float M = ML[2 * tid], lam = ML[2 * tid + 1];
-    p.lse[(int64_t)b * p.Hq + kvh * G + g0 + tid] = lam > 0.f ? (M + log2f(lam)) * kLn2 : -INFINITY;
+    lam = warp_sum(lam);
+    T* dst = out + ((int64_t)b * p.Hq + kvh * G + g0 + g) * D + V * lane;
+#pragma unroll
+    for (int j = 0; j < V; ++j) dst[j] = Elem<T>::from_f(lam > 0.f ? acc[j] / lam : 0.f);
+    if (lane == 0 && p.lse != nullptr)
+      p.lse[(int64_t)b * p.Hq + kvh * G + g0 + g] = lam > 0.f ? (M + log2f(lam)) * kLn2 : -INFINITY;
   }
 }
 
@@ -451,15 +485,12 @@ __device__ __forceinline__ void combine_partials(const Params& p, int b, int kvh
                                                  uint32_t bar, uint32_t& phase) {
   constexpr int RS = record_floats(D);
   const uint32_t head_bytes = (uint32_t)wtot * RS * 4;
-  const uint32_t coef_bytes = ((uint32_t)(G * wtot + 2 * G) * 4 + 15u) & ~15u;
-  const uint32_t avail = smem_bytes > coef_bytes ? smem_bytes - coef_bytes : 0u;
-  const int hpp = head_bytes > 0 ? (int)min((uint32_t)G, avail / head_bytes) : 0;
+  const int hpp = head_bytes > 0 ? (int)min((uint32_t)G, smem_bytes / head_bytes) : 0;
   if (hpp == 0) {
     combine_from_global<T, D, G>(p, b, kvh, wtot, pbase, reinterpret_cast<float*>(smem));
     return;
   }
   float* rec = reinterpret_cast<float*>(smem);
-  float* coef = reinterpret_cast<float*>(smem + avail);
   for (int g0 = 0; g0 < G; g0 += hpp) {
     const int ng = min(hpp, G - g0);
     if (threadIdx.x == 0) {
@@ -474,7 +505,7 @@ __device__ __forceinline__ void combine_partials(const Params& p, int b, int kvh
     }
     if (!mbar_wait(bar, phase)) atomicOr(p.status, kStatusTimeout);
     phase ^= 1u;
-    combine_from_smem<T, D, G>(p, b, kvh, wtot, g0, ng, rec, coef);
+    combine_from_smem<T, D, G>(p, b, kvh, wtot, g0, ng, rec);
     __syncthreads();  // the next pass overwrites the records
   }
 }
@@ -728,6 +759,22 @@ __global__ void __launch_bounds__(kThreads, 2) fd_split_kernel(const __grid_cons
   if (warp == kConsumerWarps && lane == 0 && ntiles > 0) {
     prefetch_tensormap(&p.tm_k);
     prefetch_tensormap(&p.tm_v);
+    // Warm L2 with the first tiles of the chunk while the previous kernel drains
+    // (its combine tail leaves HBM idle).  An L2 prefetch hands no data to this
+    // SM, and L2 is where every global write becomes visible, so it cannot expose
+    // K/V that the previous kernel is still writing.  The paged layout would have
+    // to read the block table first, which may be such a write: it skips this.
+    if (p.block_table == nullptr) {
+      const int row0 = p.cu[wk.b] + wk.t0;
+      const int npf = min(ntiles, kL2PrefetchTiles);
+      for (int kt = 0; kt < npf; ++kt) {
+#pragma unroll
+        for (int bx = 0; bx < NBOX; ++bx) {
+          tma_prefetch_l2_3d(&p.tm_k, bx * BOXC, wk.kvh, row0 + kt * TILE);
+          tma_prefetch_l2_3d(&p.tm_v, bx * BOXC, wk.kvh, row0 + kt * TILE);
+        }
+      }
+    }
   }
   pdl_wait();  // q, K, V, the workspace and out may come from earlier kernels
   __syncthreads();
