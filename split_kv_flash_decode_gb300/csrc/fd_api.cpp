@@ -194,6 +194,9 @@ int plan_impl(int B, int Hq, int Hkv, int d, const int32_t* seqlens, const int32
   std::memset(&p, 0, sizeof(p));
   p.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)d));
   p.B = B; p.Hq = Hq; p.Hkv = Hkv; p.C = C;
+  // Only the first wave can start before the previous kernel ends; later CTAs
+  // would only queue prefetches ahead of their own loads.
+  p.prefetch_ctas = (int32_t)std::min<int64_t>(ctas, (int64_t)num_sms * kCtasPerSm);
   // Paged caches: boundaries on whole tiles, so that every TMA box stays in one page.
   p.align = page_size ? fd::tile_for(pl->path) : 1;
   p.box_rows = page_size ? std::min(fd::tile_for(pl->path), page_size) : fd::tile_for(pl->path);

@@ -764,7 +764,8 @@ __global__ void __launch_bounds__(kThreads, 2) fd_split_kernel(const __grid_cons
     // SM, and L2 is where every global write becomes visible, so it cannot expose
     // K/V that the previous kernel is still writing.  The paged layout would have
     // to read the block table first, which may be such a write: it skips this.
-    if (p.block_table == nullptr) {
+    // So do CTAs past the first wave, which start after the previous kernel.
+    if (p.block_table == nullptr && (int)blockIdx.x < p.prefetch_ctas) {
       const int row0 = p.cu[wk.b] + wk.t0;
       const int npf = min(ntiles, kL2PrefetchTiles);
       for (int kt = 0; kt < npf; ++kt) {
