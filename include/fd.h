@@ -154,7 +154,9 @@ int fd_workspace_init(fd_plan_t plan, void* workspace, cudaStream_t stream);
  * caller owns every buffer and the stream.  Kernels are launched with
  * programmatic dependent launch (unless FD_PLAN_NO_PDL): their prologue may
  * overlap the previous kernel on the stream, but they read and write global
- * memory only after every earlier kernel has completed.  Asynchronous: returns after the
+ * memory only after every earlier kernel has completed.  The prologue does
+ * prefetch the first K/V tiles of each chunk into L2 (contiguous layout only); a
+ * prefetch returns no data, so it cannot observe a K/V write still in flight.  Asynchronous: returns after the
  * launch; with FD_PLAN_DEBUG it synchronises and reports FD_ERR_TIMEOUT or
  * FD_ERR_STATE from the device status word.  Decodes that share a workspace
  * must not overlap in time.
