@@ -50,6 +50,10 @@ def parse_args(argv=None):
     ap.add_argument("--two-launch", action="store_true", help="split + combine as two kernels")
     ap.add_argument("--ffma", action="store_true", help="CUDA-core consumers even when G >= 4")
     ap.add_argument("--no-pdl", action="store_true", help="launch without programmatic dependent launch")
+    ap.add_argument("--no-cluster", action="store_true",
+                    help="one partial record per chunk (no in-cluster segment merge)")
+    ap.add_argument("--cluster", action="store_true",
+                    help="always merge chunk partials per segment inside a cluster")
     ap.add_argument("--kv", choices=["native", "e4m3"], default="native",
                     help="K/V storage: the case's 16-bit type, or FP8 E4M3 (q stays 16-bit)")
     ap.add_argument("--paged", type=int, default=0, metavar="P",
@@ -355,7 +359,8 @@ def run_fd(args):
 
     flags = (fd.FD_PLAN_LITERAL_W if prob.literal_w else 0) | (
         fd.FD_PLAN_TWO_LAUNCH if args.two_launch else 0) | (fd.FD_PLAN_FFMA if args.ffma else 0) | (
-        fd.FD_PLAN_NO_PDL if args.no_pdl else 0) | (fd.FD_PLAN_WAITS if args.waits else 0)
+        fd.FD_PLAN_NO_PDL if args.no_pdl else 0) | (fd.FD_PLAN_WAITS if args.waits else 0) | (
+        fd.FD_PLAN_NO_CLUSTER if args.no_cluster else 0) | (fd.FD_PLAN_CLUSTER if args.cluster else 0)
     plan_dtype = "f16_e4m3kv" if prob.kv_type == "e4m3" else prob.dtype
     dec = fd.Decoder(prob.Hq, prob.Hkv, prob.d, prob.seqlens, prob.W, plan_dtype, flags=flags,
                      chunks=args.chunks, device=device, page_size=args.paged)
@@ -501,6 +506,7 @@ def run_fd(args):
             "config": {
                 "workload": prob.name, **prob.describe(), "accumulate": "f32",
                 "chunks_per_segment": info["chunks"], "ctas": info["ctas"],
+                "records_per_segment": info["records_per_segment"],
                 "partials_per_sequence_max": info["max_partials"],
                 "kv_bytes_per_step": kv_bytes, "two_launch": bool(args.two_launch),
                 "kv_storage": prob.kv_type,

@@ -79,6 +79,14 @@ enum fd_status {
  * sets its flag, so that combiner's bounded wait runs out (~1 s) and the status
  * word reports FD_ERR_TIMEOUT.  Its out/lse are left unwritten. */
 #define FD_PLAN_TEST_DROP_FLAG 0x40u
+/* Segment merge.  When the planner cuts each segment into 2..8 chunks, the chunk
+ * CTAs of a segment can run as one thread-block cluster and merge their partials
+ * through distributed shared memory, so that the combine reads one record per
+ * segment, as in the pages.  By default this happens when one (sequence, KV head)'s
+ * chunk records would not fit the combine's shared memory in one pass.
+ * FD_PLAN_NO_CLUSTER never merges; FD_PLAN_CLUSTER always does (both: invalid). */
+#define FD_PLAN_NO_CLUSTER 0x80u
+#define FD_PLAN_CLUSTER 0x100u
 
 /* Compiled limits. */
 #define FD_MAX_BATCH 256       /* sequences per plan */
@@ -236,8 +244,10 @@ typedef struct fd_plan_info {
   int64_t total_partials;  /* P */
   uint64_t workspace_bytes;
   uint64_t kv_bytes;       /* bytes of K and V one decode reads */
-  int32_t path;            /* 0: CUDA-core (FFMA) consumers, 1: tensor-core (mma.sync) */
-  int32_t reserved;
+  int32_t path;            /* 0: CUDA-core (FFMA) consumers, 1: tensor-core (mma.sync),
+                              2: tensor-core over an E4M3 cache */
+  int32_t records_per_segment; /* partial records per segment: 1 (chunks merged in a
+                                  cluster) or chunks */
 } fd_plan_info;
 
 int fd_plan_get_info(fd_plan_t plan, fd_plan_info* info);

@@ -26,6 +26,8 @@ from ._binding import (  # noqa: F401
     FD_PLAN_DEBUG,
     FD_PLAN_FFMA,
     FD_PLAN_LITERAL_W,
+    FD_PLAN_CLUSTER,
+    FD_PLAN_NO_CLUSTER,
     FD_PLAN_NO_PDL,
     FD_PLAN_TEST_DROP_FLAG,
     FD_PLAN_WAITS,

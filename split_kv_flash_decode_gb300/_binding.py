@@ -32,6 +32,8 @@ FD_PLAN_FFMA = 0x8
 FD_PLAN_NO_PDL = 0x10
 FD_PLAN_WAITS = 0x20
 FD_PLAN_TEST_DROP_FLAG = 0x40
+FD_PLAN_NO_CLUSTER = 0x80
+FD_PLAN_CLUSTER = 0x100
 FD_MAX_BATCH = 256
 FD_MAX_PARTIALS = 1024
 
@@ -60,7 +62,7 @@ class PlanInfo(ctypes.Structure):
         ("ctas", ctypes.c_int32), ("max_partials", ctypes.c_int32),
         ("total_tokens", ctypes.c_int64), ("total_partials", ctypes.c_int64),
         ("workspace_bytes", ctypes.c_uint64), ("kv_bytes", ctypes.c_uint64),
-        ("path", ctypes.c_int32), ("reserved", ctypes.c_int32),
+        ("path", ctypes.c_int32), ("records_per_segment", ctypes.c_int32),
     ]
 
 

@@ -18,6 +18,7 @@ namespace {
 constexpr int kVersion = 0x000100;
 constexpr size_t kAlign = 256;
 constexpr int kMinChunkTokens = 256;  // auto chunking never cuts segments below this
+constexpr int kMaxCluster = 8;        // portable thread-block cluster size
 constexpr int kCtasPerSm = 2;         // resident CTAs per SM (launch bounds + shared memory)
 
 size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
@@ -111,7 +112,10 @@ int plan_impl(int B, int Hq, int Hkv, int d, const int32_t* seqlens, const int32
   if (Hq % Hkv != 0) return FD_ERR_INVALID;
   if (dtype != FD_F16 && dtype != FD_BF16 && dtype != FD_F16_E4M3KV) return FD_ERR_INVALID;
   if (flags & ~(FD_PLAN_LITERAL_W | FD_PLAN_DEBUG | FD_PLAN_TWO_LAUNCH | FD_PLAN_FFMA |
-                FD_PLAN_NO_PDL | FD_PLAN_WAITS | FD_PLAN_TEST_DROP_FLAG))
+                FD_PLAN_NO_PDL | FD_PLAN_WAITS | FD_PLAN_TEST_DROP_FLAG |
+                FD_PLAN_NO_CLUSTER | FD_PLAN_CLUSTER))
+    return FD_ERR_INVALID;
+  if ((flags & FD_PLAN_CLUSTER) && (flags & (FD_PLAN_NO_CLUSTER | FD_PLAN_WAITS)))
     return FD_ERR_INVALID;
   if ((flags & FD_PLAN_WAITS) && (flags & FD_PLAN_TWO_LAUNCH)) return FD_ERR_INVALID;
   if ((flags & FD_PLAN_TEST_DROP_FLAG) && !(flags & FD_PLAN_WAITS)) return FD_ERR_INVALID;
@@ -197,6 +201,16 @@ int plan_impl(int B, int Hq, int Hkv, int d, const int32_t* seqlens, const int32
   // Only the first wave can start before the previous kernel ends; later CTAs
   // would only queue prefetches ahead of their own loads.
   p.prefetch_ctas = (int32_t)std::min<int64_t>(ctas, (int64_t)num_sms * kCtasPerSm);
+  // When the chunk records of one (sequence, KV head) would need several passes
+  // through the combine's shared memory (at least 2; 3 over an FP8 cache, whose
+  // shorter CTAs gain less than the cluster barriers cost), segments cut into 2..8
+  // chunks merge them inside a cluster (one record per segment).  Not in the
+  // fine-grained-waits variant, which combines chunk records as they arrive.
+  const int64_t rec_bytes = (int64_t)G * max_w * C * fd::record_floats(d) * 4;
+  const int64_t ring = (int64_t)fd::ring_bytes_for(pl->path, d);
+  const bool multi_pass = rec_bytes > (pl->path == fd::kPathMmaKv8 ? 2 : 1) * ring;
+  p.rps = ((multi_pass || (flags & FD_PLAN_CLUSTER)) && C > 1 && C <= kMaxCluster &&
+           !(flags & (FD_PLAN_WAITS | FD_PLAN_NO_CLUSTER))) ? 1 : C;
   // Paged caches: boundaries on whole tiles, so that every TMA box stays in one page.
   p.align = page_size ? fd::tile_for(pl->path) : 1;
   p.box_rows = page_size ? std::min(fd::tile_for(pl->path), page_size) : fd::tile_for(pl->path);
@@ -260,7 +274,7 @@ int fd_plan_get_info(fd_plan_t pl, fd_plan_info* info) {
   info->workspace_bytes = pl->ws_bytes;
   info->kv_bytes = (uint64_t)pl->n_tokens * pl->Hkv * pl->d * 2 * fd::kv_elem_bytes(pl->path);
   info->path = pl->path;
-  info->reserved = 0;
+  info->records_per_segment = pl->params.rps;
   return FD_OK;
 }
 

@@ -83,6 +83,9 @@ struct Params {
   int32_t box_rows;    // token rows per TMA box (the tile, or one page when pages are smaller)
   int32_t align;       // segment / chunk boundaries are multiples of this many tokens
   int32_t prefetch_ctas;  // CTAs [0, prefetch_ctas) warm L2 before the programmatic-launch wait
+  // Partial records per segment: C, or 1 when the C chunk CTAs of a segment form a
+  // thread-block cluster and merge their partials through distributed shared memory.
+  int32_t rps;
   float scale_log2;    // log2(e) / sqrt(d)
   int32_t B, Hq, Hkv, C;
   int32_t cu[FD_MAX_BATCH + 1];         // token prefix sums

@@ -274,24 +274,51 @@ __device__ __forceinline__ uint32_t swz_addr(uint32_t base, int rows, int row, i
 // Work item of CTA `cta` in the flattened (sequence, slot, KV head) order.
 struct Work {
   int b, kvh, slot, wtot, t0, t1;
-  int64_t pbase;  // index of the first partial of sequence b
+  int w, c;       // segment, and chunk within the segment (slot = w * C + c)
+  int nrec;       // partial records per query head of sequence b (W_b * rps)
+  int rslot;      // this CTA's record slot (slot, or w when segments merge in-cluster)
+  int64_t pbase;  // index of the first partial record of sequence b
 };
 
-__device__ __forceinline__ Work decode_work(const Params& p, int cta) {
+// First partial record of sequence b, and the ready flag of partial `slot` of
+// (b, kvh) (fine-grained-waits variant).
+__device__ __forceinline__ int64_t rec_base(const Params& p, int b) {
+  return (int64_t)(p.unit_base[b] / (p.Hkv * p.C)) * p.rps * p.Hq;
+}
+__device__ __forceinline__ int flag_index(const Params& p, int b, int kvh, int slot) {
+  return p.unit_base[b] + kvh * p.wseg[b] * p.C + slot;
+}
+
+// `seg`: the plan merges each segment's chunks in a cluster (rps == 1 < C).
+__device__ __forceinline__ Work decode_work(const Params& p, int cta, bool seg) {
   int lo = 0, hi = p.B;
   while (hi - lo > 1) {
     const int mid = (lo + hi) >> 1;
     if (p.unit_base[mid] <= cta) lo = mid; else hi = mid;
   }
+  // CTA order within a sequence: KV head fastest, then partial slot; with the
+  // segment merge, chunk fastest, then KV head, then segment, so that the C chunks
+  // of one segment are consecutive (one cluster).
   Work w;
   w.b = lo;
   const int r = cta - p.unit_base[lo];
-  w.kvh = r % p.Hkv;
-  w.slot = r / p.Hkv;
-  w.wtot = (p.unit_base[lo + 1] - p.unit_base[lo]) / p.Hkv;
+  if (!seg) {
+    w.kvh = r % p.Hkv;
+    w.slot = r / p.Hkv;
+    w.w = w.slot / p.C;
+    w.c = w.slot - w.w * p.C;
+  } else {
+    w.c = r % p.C;
+    w.kvh = (r / p.C) % p.Hkv;
+    w.w = r / (p.C * p.Hkv);
+    w.slot = w.w * p.C + w.c;
+  }
+  w.wtot = p.wseg[lo] * p.C;
+  w.nrec = p.wseg[lo] * (seg ? 1 : p.C);
+  w.rslot = seg ? w.w : w.slot;
   const int L = p.cu[lo + 1] - p.cu[lo];
   chunk_range(L, p.wseg[lo], p.C, w.slot, p.align, &w.t0, &w.t1);
-  w.pbase = (int64_t)(p.unit_base[lo] / p.Hkv) * p.Hq;
+  w.pbase = rec_base(p, lo);
   return w;
 }
 
@@ -310,6 +337,34 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
       "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
       "l"(src), "r"(bytes), "r"(bar)
       : "memory");
+}
+
+// Distributed shared memory of a thread-block cluster: the address of the same
+// shared-memory location in CTA `rank` of this cluster, loads from it, and the
+// cluster-wide barrier (split into arrive and wait).
+__device__ __forceinline__ uint32_t cluster_map(uint32_t addr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ float4 ld_cluster_f4(uint32_t addr) {
+  float4 v;
+  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(addr)
+               : "memory");
+  return v;
+}
+__device__ __forceinline__ float2 ld_cluster_f2(uint32_t addr) {
+  float2 v;
+  asm volatile("ld.shared::cluster.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(addr) : "memory");
+  return v;
+}
+__device__ __forceinline__ void cluster_arrive() {
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() {
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
 // Order this thread's view of generic-proxy global writes before its later
@@ -530,7 +585,7 @@ __device__ __forceinline__ void combine_as_arrived(const Params& p, const Work& 
   int* ctl = done + wtot;                  // [0] batch size, [1] stop
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   constexpr int kWarps = kThreads / 32;
-  const int fbase = p.unit_base[wk.b] + wk.kvh;  // flag of slot w: fbase + w * Hkv
+  const int fbase = flag_index(p, wk.b, wk.kvh, 0);  // flag of slot w: fbase + w
   for (int i = tid; i < G * D; i += kThreads) run_O[i] = 0.f;
   for (int g = tid; g < G; g += kThreads) { run_M[g] = -INFINITY; run_L[g] = 0.f; }
   for (int w = tid; w < wtot; w += kThreads) done[w] = 0;
@@ -542,7 +597,7 @@ __device__ __forceinline__ void combine_as_arrived(const Params& p, const Work& 
     if (tid == 0) ctl[0] = 0;
     __syncthreads();
     for (int w = tid; w < wtot; w += kThreads) {
-      if (!done[w] && (w == wk.slot || ld_acquire_gpu(p.flags + fbase + w * p.Hkv) != 0u)) {
+      if (!done[w] && (w == wk.slot || ld_acquire_gpu(p.flags + fbase + w) != 0u)) {
         done[w] = 1;
         ready[atomicAdd(&ctl[0], 1)] = w;
       }
@@ -605,7 +660,7 @@ __device__ __forceinline__ void combine_as_arrived(const Params& p, const Work& 
   }
   // Flags go back to zero for the next decode (the ones that were set).
   for (int w = tid; w < wtot; w += kThreads)
-    if (done[w] && w != wk.slot) p.flags[fbase + w * p.Hkv] = 0u;
+    if (done[w] && w != wk.slot) p.flags[fbase + w] = 0u;
   if (merged < wtot) return;  // timed out: status is set, out is not written
   T* out = reinterpret_cast<T*>(p.out);
   for (int v = tid; v < G * (D / 4); v += kThreads) {
@@ -619,12 +674,69 @@ __device__ __forceinline__ void combine_as_arrived(const Params& p, const Work& 
   }
 }
 
+// Segment merge inside a thread-block cluster (the C chunk CTAs of one segment):
+// every CTA holds its chunk record in shared memory (`crec`, [G][D + 4]); after a
+// cluster barrier each CTA reads all C records through distributed shared memory
+// and writes its share of the columns of the segment's record (fixed chunk
+// order; CTA 0 also writes M and Lambda).  Ends with this CTA's arrival at the
+// closing cluster barrier; the caller waits on it before the CTA exits, so no
+// CTA leaves while another still reads its shared memory.  `cf` is scratch for
+// G * (C + 2) floats.
+template <int D, int G>
+__device__ __forceinline__ void merge_segment(const Params& p, const Work& wk, const float* crec,
+                                              float* cf) {
+  constexpr int RS = record_floats(D);
+  const int tid = threadIdx.x, C = p.C;
+  cluster_arrive();
+  cluster_wait();  // every chunk record of the segment is in place
+  const uint32_t crec_a = smem_addr(crec);
+  if (tid < G) {
+    const uint32_t ml_a = crec_a + (uint32_t)(tid * RS + D) * 4u;
+    float M = -INFINITY;
+    for (int j = 0; j < C; ++j) M = fmaxf(M, ld_cluster_f2(cluster_map(ml_a, j)).x);
+    float lam = 0.f;
+    for (int j = 0; j < C; ++j) {
+      const float2 ml = ld_cluster_f2(cluster_map(ml_a, j));
+      const float f = (M == -INFINITY) ? 0.f : ex2(ml.x - M);  // an empty chunk has m = -inf
+      cf[tid * C + j] = f;
+      lam = fmaf(f, ml.y, lam);
+    }
+    cf[G * C + tid] = M;
+    cf[G * C + G + tid] = lam;
+  }
+  __syncthreads();
+  constexpr int Q = D / 4;
+  const int lo4 = wk.c * Q / C, n4 = (wk.c + 1) * Q / C - lo4;
+  const int64_t rec0 = wk.pbase + (int64_t)(wk.kvh * G) * wk.nrec + wk.w;  // head g: + g * nrec
+  for (int i = tid; i < G * n4; i += kThreads) {
+    const int g = i / n4, c4 = lo4 + (i - (i / n4) * n4);
+    const uint32_t src = crec_a + (uint32_t)(g * RS + 4 * c4) * 4u;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int j = 0; j < C; ++j) {
+      const float4 x = ld_cluster_f4(cluster_map(src, j));
+      const float f = cf[g * C + j];
+      acc.x = fmaf(f, x.x, acc.x);
+      acc.y = fmaf(f, x.y, acc.y);
+      acc.z = fmaf(f, x.z, acc.z);
+      acc.w = fmaf(f, x.w, acc.w);
+    }
+    __stcg(reinterpret_cast<float4*>(p.part + (rec0 + (int64_t)g * wk.nrec) * RS) + c4, acc);
+  }
+  if (wk.c == 0 && tid < G)
+    __stcg(reinterpret_cast<float4*>(p.part + (rec0 + (int64_t)tid * wk.nrec) * RS + D),
+           make_float4(cf[G * C + tid], cf[G * C + G + tid], 0.f, 0.f));
+  cluster_arrive();  // done reading the other CTAs' shared memory
+}
+
 // Merge NGRP running states (sm_acc [NGRP][G][D], sm_m / sm_l [NGRP][G], all in
 // shared memory) into this CTA's partial; then either finish directly (a single
-// partial), or publish the partial, arrive, and combine if this CTA arrived last.
-template <typename T, int D, int G, int NGRP, int MODE>
+// partial), or publish the partial (merged per segment inside the cluster when
+// rps == 1), arrive, and combine if this CTA arrived last.  An `aborted` CTA (its
+// pipeline timed out; the status word says so) contributes an empty partial so
+// that its cluster and its (b, kvh) counter still complete.
+template <typename T, int D, int G, int NGRP, int MODE, bool SEG>
 __device__ __forceinline__ void finish_cta(const Params& p, const Work& wk, float* sm_acc,
-                                           int& sm_last, uint8_t* combine_smem,
+                                           int& sm_last, bool aborted, uint8_t* combine_smem,
                                            uint32_t combine_bytes, uint32_t combine_bar) {
   float* sm_m = sm_acc + NGRP * G * D;  // [NGRP][G]
   float* sm_l = sm_m + NGRP * G;        // [NGRP][G]
@@ -641,8 +753,8 @@ __device__ __forceinline__ void finish_cta(const Params& p, const Work& wk, floa
       sm_fac[q * G + g] = f;
       lam = fmaf(sm_l[q * G + g], f, lam);
     }
-    sm_ML[2 * g] = M;
-    sm_ML[2 * g + 1] = lam;
+    sm_ML[2 * g] = aborted ? -INFINITY : M;
+    sm_ML[2 * g + 1] = aborted ? 0.f : lam;
   }
   __syncthreads();
 
@@ -665,8 +777,13 @@ __device__ __forceinline__ void finish_cta(const Params& p, const Work& wk, floa
     return;
   }
 
-  // Publish this CTA's partial record (O unnormalised w.r.t. M, then M, Lambda).
+  // Publish this CTA's partial record (O unnormalised w.r.t. M, then M, Lambda):
+  // to global memory, or to `crec` at the end of the ring for the segment merge.
   constexpr int RS = record_floats(D);
+  constexpr bool merge_seg = SEG;
+  static_assert(!SEG || MODE == 0 || MODE == 1, "segment merge: fused or split-only kernels");
+  const uint32_t crec_bytes = merge_seg ? (uint32_t)(G * RS * 4) : 0u;
+  float* crec = reinterpret_cast<float*>(combine_smem + combine_bytes - G * RS * 4);
   for (int idx = tid; idx < G * D / 4; idx += kThreads) {
     const int g = idx / (D / 4), c4 = idx - (idx / (D / 4)) * (D / 4);
     float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -679,20 +796,33 @@ __device__ __forceinline__ void finish_cta(const Params& p, const Work& wk, floa
       a.z = fmaf(x.z, f, a.z);
       a.w = fmaf(x.w, f, a.w);
     }
-    const int64_t pidx = wk.pbase + (int64_t)(h0 + g) * wk.wtot + wk.slot;
-    __stcg(reinterpret_cast<float4*>(p.part + pidx * RS) + c4, a);
+    if (aborted) a = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (merge_seg) {
+      reinterpret_cast<float4*>(crec + g * RS)[c4] = a;
+    } else {
+      const int64_t pidx = wk.pbase + (int64_t)(h0 + g) * wk.nrec + wk.rslot;
+      __stcg(reinterpret_cast<float4*>(p.part + pidx * RS) + c4, a);
+    }
   }
   if (tid < G) {
-    const int64_t pidx = wk.pbase + (int64_t)(h0 + tid) * wk.wtot + wk.slot;
-    __stcg(reinterpret_cast<float4*>(p.part + pidx * RS + D),
-           make_float4(sm_ML[2 * tid], sm_ML[2 * tid + 1], 0.f, 0.f));
+    const float4 ml = make_float4(sm_ML[2 * tid], sm_ML[2 * tid + 1], 0.f, 0.f);
+    if (merge_seg) {
+      *reinterpret_cast<float4*>(crec + tid * RS + D) = ml;
+    } else {
+      const int64_t pidx = wk.pbase + (int64_t)(h0 + tid) * wk.nrec + wk.rslot;
+      __stcg(reinterpret_cast<float4*>(p.part + pidx * RS + D), ml);
+    }
   }
-  if (MODE == 1) return;
+  if (merge_seg) merge_segment<D, G>(p, wk, crec, sm_acc);
+  if (MODE == 1) {
+    if (merge_seg) cluster_wait();
+    return;
+  }
   if (MODE == 3) {
     __syncthreads();
     if (wk.slot != 0) {
       const bool dropped = p.drop_flag && wk.b == 0 && wk.kvh == 0 && wk.slot == 1;
-      if (tid == 0 && !dropped) st_release_gpu(p.flags + blockIdx.x, 1u);
+      if (tid == 0 && !dropped) st_release_gpu(p.flags + flag_index(p, wk.b, wk.kvh, wk.slot), 1u);
       return;
     }
     combine_as_arrived<T, D, G>(p, wk, reinterpret_cast<float*>(combine_smem));
@@ -710,16 +840,23 @@ __device__ __forceinline__ void finish_cta(const Params& p, const Work& wk, floa
     sm_last = (old == (uint32_t)(wk.wtot - 1));
   }
   __syncthreads();
-  if (!sm_last) return;
-  uint32_t phase = 0;
-  combine_partials<T, D, G>(p, wk.b, wk.kvh, wk.wtot, wk.pbase, combine_smem, combine_bytes,
-                            combine_bar, phase);
-  if (tid == 0) *cnt = 0u;
+  if (sm_last) {
+    // The records end before `crec`, which other CTAs of the cluster may still read.
+    uint32_t phase = 0;
+    combine_partials<T, D, G>(p, wk.b, wk.kvh, wk.nrec, wk.pbase, combine_smem,
+                              combine_bytes - crec_bytes, combine_bar, phase);
+    if (tid == 0) *cnt = 0u;
+  }
+  if (merge_seg) cluster_wait();
 }
 
 // MODE 0: fused split + last-arriver combine.  MODE 1: split only (partials).
+// MODE 3: fused split + fine-grained waits.  MODE 4 / 5: MODE 0 / 1 with each
+// segment's chunk partials merged inside a thread-block cluster (rps == 1).
 template <typename T, int D, int G, int PATH, int MODE>
 __global__ void __launch_bounds__(kThreads, 2) fd_split_kernel(const __grid_constant__ Params p) {
+  constexpr bool kSeg = MODE >= 4;
+  constexpr int kMode = kSeg ? MODE - 4 : MODE;
   constexpr int TILE = tile_for(PATH);
   constexpr int STAGES = stages_for(PATH, D);
   constexpr int BOXC = box_cols_for(PATH, D);   // columns per TMA box
@@ -730,8 +867,9 @@ __global__ void __launch_bounds__(kThreads, 2) fd_split_kernel(const __grid_cons
   constexpr int NGRP_FFMA = kConsumerWarps * (32 / ((G * D > 512) ? 16 : 8));
   constexpr int NGRP = is_mma(PATH) ? kConsumerWarps : NGRP_FFMA;
   static_assert(PATH == kPathFfma || G >= 4, "the MMA path needs G >= 4 heads on N");
-  static_assert(NGRP * G * D * 4 + 4 * NGRP * G * 4 <= STAGES * kStageBytes,
-                "group merge must fit in the ring");
+  static_assert(NGRP * G * D * 4 + 4 * NGRP * G * 4 + G * record_floats(D) * 4 <=
+                    STAGES * kStageBytes,
+                "group merge and the segment-merge record must fit in the ring");
 
   extern __shared__ uint8_t smem_raw[];
   // 1024-byte aligned base: the 128-byte swizzle pattern repeats every 1024 bytes.
@@ -745,7 +883,7 @@ __global__ void __launch_bounds__(kThreads, 2) fd_split_kernel(const __grid_cons
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   pdl_launch_dependents();
   // Prologue that touches no global memory: it may overlap the previous kernel.
-  const Work wk = decode_work(p, blockIdx.x);
+  const Work wk = decode_work(p, blockIdx.x, kSeg);
   const int ntiles = (wk.t1 - wk.t0 + TILE - 1) / TILE;
   if (tid == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -1285,8 +1423,11 @@ __global__ void __launch_bounds__(kThreads, 2) fd_split_kernel(const __grid_cons
     }
   }
   __syncthreads();
-  if (sm_abort) return;
-  finish_cta<T, D, G, NGRP, MODE>(p, wk, sm_acc, sm_last, smem, STAGES * kStageBytes,
+  // A CTA of a cluster must still reach the cluster barriers: it finishes with an
+  // empty partial instead.
+  if (sm_abort && !kSeg) return;
+  finish_cta<T, D, G, NGRP, kMode, kSeg>(p, wk, sm_acc, sm_last, sm_abort != 0, smem,
+                                         STAGES * kStageBytes,
                                   smem_addr(bars + 2 * STAGES));
 }
 
@@ -1306,10 +1447,9 @@ __global__ void __launch_bounds__(kThreads, 2) fd_combine_kernel(const __grid_co
   pdl_wait();
   __syncthreads();
   const int b = blockIdx.x / p.Hkv, kvh = blockIdx.x - (blockIdx.x / p.Hkv) * p.Hkv;
-  const int wtot = (p.unit_base[b + 1] - p.unit_base[b]) / p.Hkv;
-  const int64_t pbase = (int64_t)(p.unit_base[b] / p.Hkv) * p.Hq;
   uint32_t phase = 0;
-  combine_partials<T, D, G>(p, b, kvh, wtot, pbase, smem, kBytes, smem_addr(bar), phase);
+  combine_partials<T, D, G>(p, b, kvh, p.wseg[b] * p.rps, rec_base(p, b), smem, kBytes,
+                            smem_addr(bar), phase);
 }
 
 }  // namespace dev
@@ -1317,24 +1457,33 @@ __global__ void __launch_bounds__(kThreads, 2) fd_combine_kernel(const __grid_co
 template <typename T, int D, int G, int PATH>
 cudaError_t launch_dgp(const Params& p, int mode, bool pdl, int grid, cudaStream_t stream) {
   const size_t smem = smem_bytes_for(PATH, D);
+  // The split kernels of plans that merge segments in clusters are separate
+  // instantiations (kernel modes 4 and 5).
+  const bool seg = mode <= 1 && p.rps != p.C;
+  const int kmode = seg ? mode + 4 : mode;
   const void* fn;
-  if (mode == 0) fn = reinterpret_cast<const void*>(&dev::fd_split_kernel<T, D, G, PATH, 0>);
-  else if (mode == 1) fn = reinterpret_cast<const void*>(&dev::fd_split_kernel<T, D, G, PATH, 1>);
-  else if (mode == 2) fn = reinterpret_cast<const void*>(&dev::fd_combine_kernel<T, D, G, PATH>);
-  else fn = reinterpret_cast<const void*>(&dev::fd_split_kernel<T, D, G, PATH, 3>);
+  switch (kmode) {
+    case 0: fn = reinterpret_cast<const void*>(&dev::fd_split_kernel<T, D, G, PATH, 0>); break;
+    case 1: fn = reinterpret_cast<const void*>(&dev::fd_split_kernel<T, D, G, PATH, 1>); break;
+    case 2: fn = reinterpret_cast<const void*>(&dev::fd_combine_kernel<T, D, G, PATH>); break;
+    case 3: fn = reinterpret_cast<const void*>(&dev::fd_split_kernel<T, D, G, PATH, 3>); break;
+    case 4: fn = reinterpret_cast<const void*>(&dev::fd_split_kernel<T, D, G, PATH, 4>); break;
+    default: fn = reinterpret_cast<const void*>(&dev::fd_split_kernel<T, D, G, PATH, 5>); break;
+  }
   int dev_id = 0;
   cudaError_t err = cudaGetDevice(&dev_id);
   if (err != cudaSuccess) return err;
   // The opt-in shared-memory size is a per-device function attribute.
-  static uint64_t done_mask[4] = {0, 0, 0, 0};
+  static uint64_t done_mask[6] = {0, 0, 0, 0, 0, 0};
   const uint64_t bit = 1ull << (dev_id & 63);
-  if (!(__atomic_load_n(&done_mask[mode], __ATOMIC_ACQUIRE) & bit)) {
+  if (!(__atomic_load_n(&done_mask[kmode], __ATOMIC_ACQUIRE) & bit)) {
     err = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (err != cudaSuccess) return err;
-    __atomic_fetch_or(&done_mask[mode], bit, __ATOMIC_RELEASE);
+    __atomic_fetch_or(&done_mask[kmode], bit, __ATOMIC_RELEASE);
   }
   void* args[] = {const_cast<Params*>(&p)};
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
+  unsigned int nattr = 1;
   if (mode == 3) {
     // The designated combiners wait for other CTAs: the whole grid must be resident.
     int per_sm = 0, sms = 0;
@@ -1347,6 +1496,14 @@ cudaError_t launch_dgp(const Params& p, int mode, bool pdl, int grid, cudaStream
   } else {
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
+    if (seg) {
+      // The C chunk CTAs of a segment (consecutive block indices) form one cluster.
+      attr[1].id = cudaLaunchAttributeClusterDimension;
+      attr[1].val.clusterDim.x = (unsigned)p.C;
+      attr[1].val.clusterDim.y = 1;
+      attr[1].val.clusterDim.z = 1;
+      nattr = 2;
+    }
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
@@ -1354,7 +1511,7 @@ cudaError_t launch_dgp(const Params& p, int mode, bool pdl, int grid, cudaStream
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = nattr;
   return cudaLaunchKernelExC(&cfg, fn, args);
 }
 

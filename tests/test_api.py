@@ -85,7 +85,9 @@ def test_plan_validation(args, code):
 def test_plan_bad_dtype_flags_chunks():
     assert _raw_plan(1, 8, 8, 128, [10], [1], dtype=3) == fd.FD_ERR_INVALID
     assert _raw_plan(1, 8, 8, 128, [10], [1], dtype=2) == fd.FD_ERR_UNSUPPORTED  # FP8 K/V: G >= 4
-    assert _raw_plan(1, 8, 8, 128, [10], [1], flags=0x80) == fd.FD_ERR_INVALID
+    assert _raw_plan(1, 8, 8, 128, [10], [1], flags=0x200) == fd.FD_ERR_INVALID
+    assert _raw_plan(1, 8, 8, 128, [10], [1], flags=fd.FD_PLAN_CLUSTER | fd.FD_PLAN_NO_CLUSTER) == fd.FD_ERR_INVALID
+    assert _raw_plan(1, 8, 8, 128, [10], [1], flags=fd.FD_PLAN_CLUSTER | fd.FD_PLAN_WAITS) == fd.FD_ERR_INVALID
     assert _raw_plan(1, 8, 8, 128, [10], [1], chunks=-1) == fd.FD_ERR_INVALID
     assert _raw_plan(1, 8, 8, 128, [10], [600], chunks=2) == fd.FD_ERR_UNSUPPORTED
     # flag combinations
@@ -157,6 +159,30 @@ def test_literal_w_and_auto_chunks():
     assert p.info["chunks"] == 4  # 1024-token segments -> 256-token chunks
     p = fd.fd_plan(1, 8, 8, 64, [100], 4, "f16", num_sms=152)
     assert p.info["chunks"] == 1
+
+
+def test_records_per_segment():
+    ring = {128: 3 * 2 * 64 * 128 * 2, 64: 4 * 2 * 64 * 64 * 2}   # tensor-core rings (bytes)
+    # Auto: chunk records merge per segment (in a cluster of 2..8 CTAs) exactly when one
+    # (sequence, KV head)'s records, G * W * C * (d + 4) * 4 bytes, exceed the ring
+    # (twice the ring over an FP8 cache).
+    for Hq, W, chunks in ((32, 8, 2), (32, 8, 5), (32, 8, 8), (64, 8, 4), (128, 8, 4),
+                          (128, 8, 9), (32, 8, 1), (64, 8, 16)):
+        p = fd.fd_plan(1, Hq, 8, 128, [32768], W, "f16", chunks=chunks, num_sms=152)
+        G = Hq // 8
+        multi = G * W * chunks * 132 * 4 > ring[128]
+        want = 1 if (multi and 2 <= chunks <= 8) else chunks
+        assert p.info["chunks"] == chunks and p.info["records_per_segment"] == want, (Hq, chunks)
+    # the default 32K GQA-4 plan fits one pass; GQA-8 at 128K does not
+    assert fd.fd_plan(1, 32, 8, 128, [32768], 8, "f16", num_sms=152).info["records_per_segment"] == 4
+    assert fd.fd_plan(1, 64, 8, 128, [131072], 8, "f16", num_sms=152).info["records_per_segment"] == 1
+    fp8 = lambda Hq: fd.fd_plan(1, Hq, 8, 128, [131072], 8, "f16_e4m3kv", num_sms=152)  # noqa: E731
+    assert fp8(64).info["records_per_segment"] == 4 and fp8(128).info["records_per_segment"] == 1
+    p = fd.fd_plan(1, 32, 8, 128, [32768], 8, "f16", flags=fd.FD_PLAN_CLUSTER, num_sms=152)
+    assert p.info["chunks"] == 4 and p.info["records_per_segment"] == 1
+    for flags in (fd.FD_PLAN_NO_CLUSTER, fd.FD_PLAN_WAITS):
+        p = fd.fd_plan(1, 64, 8, 128, [131072], 8, "f16", flags=flags, num_sms=152)
+        assert p.info["chunks"] == 4 and p.info["records_per_segment"] == 4
 
 
 def test_consumer_path_choice():

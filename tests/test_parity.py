@@ -222,6 +222,28 @@ def test_two_launch_matches_fused(fd):
     assert np.array_equal(o1, o2) and np.array_equal(l1, l2)
 
 
+@pytest.mark.parametrize("dtype,G,d", [("f16", 4, 128), ("bf16", 8, 128), ("f16", 16, 128),
+                                       ("bf16", 1, 64), ("f16", 2, 128), ("bf16", 16, 64)])
+def test_cluster_segment_merge(fd, dtype, G, d):
+    """Chunks merged per segment inside a cluster (forced) agree with the oracle, with
+    one record per chunk (FD_PLAN_NO_CLUSTER), and between runs bitwise."""
+    p = workloads.make_problem("cluster", 3, 4 * G, 4, d, [9000, 1, 2500], [4, 1, 3], dtype,
+                               seed=80 + G + d)
+    ref_out, ref_lse = oracle.decode_reference(p.q, p.k, p.v, p.seqlens, p.dtype)
+    for chunks in (2, 3, 8):
+        runs, dec = run_gpu(fd, p, chunks=chunks, repeat=3, flags=fd.FD_PLAN_CLUSTER)
+        assert dec.info["chunks"] == chunks and dec.info["records_per_segment"] == 1
+        for o, l in runs[1:]:
+            assert np.array_equal(o, runs[0][0]) and np.array_equal(l, runs[0][1])
+        check(*runs[0], ref_out, ref_lse, dtype=p.dtype)
+        (o2, l2), dec2 = run_gpu(fd, p, chunks=chunks, flags=fd.FD_PLAN_NO_CLUSTER)
+        assert dec2.info["records_per_segment"] == chunks
+        check(o2, l2, ref_out, ref_lse, dtype=p.dtype)
+        (o3, l3), _ = run_gpu(fd, p, chunks=chunks,
+                              flags=fd.FD_PLAN_TWO_LAUNCH | fd.FD_PLAN_CLUSTER)
+        assert np.array_equal(o3, runs[0][0]) and np.array_equal(l3, runs[0][1])
+
+
 def test_pdl_off_matches_pdl_on(fd):
     """Programmatic dependent launch changes scheduling only, never the numbers."""
     p = workloads.make_problem("pdl", 2, 32, 8, 128, [6000, 999], [4, 3], "f16", seed=18)
