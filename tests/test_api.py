@@ -152,11 +152,11 @@ def test_literal_w_and_auto_chunks():
     p = fd.fd_plan(64, 32, 8, 128, [8192] * 64, 16, "bf16", flags=fd.FD_PLAN_LITERAL_W,
                    chunks=5, num_sms=152)
     assert p.info["chunks"] == 1 and p.info["ctas"] == 64 * 8 * 16
-    # auto: one wave of two CTAs per SM, segments not cut below 256 tokens
+    # auto: one wave of two CTAs per SM, segments not cut below 128 tokens
     p = fd.fd_plan(1, 32, 8, 128, [32768], 8, "f16", num_sms=152)
     assert p.info["chunks"] == 4 and p.info["ctas"] == 256
     p = fd.fd_plan(1, 8, 8, 64, [4096], 4, "f16", num_sms=152)
-    assert p.info["chunks"] == 4  # 1024-token segments -> 256-token chunks
+    assert p.info["chunks"] == 8  # 1024-token segments -> 128-token chunks, 256 CTAs
     p = fd.fd_plan(1, 8, 8, 64, [100], 4, "f16", num_sms=152)
     assert p.info["chunks"] == 1
 
