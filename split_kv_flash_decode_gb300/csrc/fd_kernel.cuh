@@ -10,8 +10,10 @@
 // (Push-model flag ordering, correctness check #4).
 //
 // GB300 mapping (one CTA = one chunk of one segment of one (sequence, KV head)):
-//   * warp 4, lane 0: TMA producer.  Per stage it issues 3-D tensor loads of a
-//     tile of K rows and of V rows of one KV head into an mbarrier ring.
+//   * warp 4, lane 0: TMA producer.  Before the programmatic-launch wait, CTAs
+//     of the first wave prefetch the first tiles of their chunk into L2 (HBM is
+//     idle while the previous decode combines).  Per stage it issues 3-D tensor
+//     loads of a tile of K rows and of V rows of one KV head into an mbarrier ring.
 //   * warps 0-3: consumers; every K/V byte loaded serves all G query heads that
 //     share the KV head (GQA packing).  Two consumer paths:
 //       MMA  (G >= 4): mma.sync m16n8k16 with 16 tokens on M and the G heads on
@@ -19,17 +21,22 @@
 //            O^T += V^T P^T with P moved from the accumulator layout to the
 //            operand layout by movmatrix.  K/V tiles are 64-column half-tiles
 //            with the 128-byte swizzle, so ldmatrix is conflict-free.
+//       MMA over an E4M3 cache (fp16 q/out): the same mma.sync, fragments
+//            loaded straight from the byte rows and widened in registers.
 //       FFMA (G <= 2, or forced): lanes form groups of LPT lanes, a group owns
 //            one token at a time, scores use FFMA plus an xor-shuffle reduction.
 //     Each warp (MMA) or token group (FFMA) keeps its own running (m, l, acc)
 //     in the log2 domain with a lazy rescale (only when the max grows by > 2^8).
 //   * end of CTA: groups merge through shared memory into one fp32 partial,
-//     which is written to the workspace; one thread then does
+//     which is written to the workspace (or, in the segment-merge modes, merged
+//     with the other chunks of its segment through distributed shared memory
+//     first, one record per segment); one thread then does
 //     fence + atom.add.acq_rel.gpu on the (sequence, KV head) arrival counter.
-//     The CTA that sees count == Wtot - 1 is the last arriver: it combines the
-//     Wtot partials in index order (deterministic), writes out and lse, and
-//     resets the counter.  No CTA ever waits for another, so the kernel cannot
-//     deadlock; the only waits are bounded mbarrier waits on its own loads.
+//     The CTA that sees count == Wtot - 1 is the last arriver: it bulk-copies
+//     the records into shared memory, combines them in index order
+//     (deterministic), writes out and lse, and resets the counter.  No CTA waits
+//     for another CTA's progress outside its own cluster, whose CTAs run
+//     together; every other wait is a bounded mbarrier wait on its own loads.
 #pragma once
 
 #include <cuda_bf16.h>

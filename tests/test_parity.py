@@ -336,7 +336,7 @@ def test_paged_cache(fd, page_size, dtype, G):
 def test_paged_cache_full_32k_and_variants(fd):
     p = workloads.gqa4_d128_L32k_W8()
     ref_out, ref_lse = oracle.decode_reference(p.q, p.k, p.v, p.seqlens, p.dtype)
-    for flags in (0, fd.FD_PLAN_TWO_LAUNCH, fd.FD_PLAN_WAITS):
+    for flags in (0, fd.FD_PLAN_TWO_LAUNCH, fd.FD_PLAN_WAITS, fd.FD_PLAN_CLUSTER):
         out, lse, _, _ = run_paged(fd, p, 64, flags=flags)
         check(out, lse, ref_out, ref_lse)
 
@@ -348,12 +348,14 @@ def test_fp8_e4m3_kv_cache(fd, G):
                                   seed=70 + G)
     p = workloads.with_e4m3_kv(base)
     ref_out, ref_lse = reference(p)
-    for flags in (0, fd.FD_PLAN_TWO_LAUNCH, fd.FD_PLAN_WAITS):
+    for flags in (0, fd.FD_PLAN_TWO_LAUNCH, fd.FD_PLAN_WAITS, fd.FD_PLAN_CLUSTER):
         (out, lse), dec = run_gpu(fd, p, flags=flags)
         assert dec.info["path"] == 2 and dec.info["kv_bytes"] == p.kv_bytes
         check(out, lse, ref_out, ref_lse, dtype="f16")
-    for page_size in (16, 128):
-        out, lse, _, _ = run_paged(fd, p, page_size)
+    for page_size, flags in ((16, 0), (128, 0), (64, fd.FD_PLAN_CLUSTER)):
+        out, lse, dec, _ = run_paged(fd, p, page_size, flags=flags)
+        if flags:
+            assert dec.info["records_per_segment"] == 1
         check(out, lse, ref_out, ref_lse, dtype="f16")
 
 
