@@ -36,12 +36,6 @@ FD_HD constexpr bool is_mma(int path) { return path != kPathFfma; }
 FD_HD constexpr int kv_elem_bytes(int path) { return path == kPathMmaKv8 ? 1 : 2; }
 // Tokens per pipeline stage.
 FD_HD constexpr int tile_for(int path) { return is_mma(path) ? 64 : 32; }
-// Stages of the shared-memory ring.
-FD_HD constexpr int stages_for(int path, int d) {
-  return path == kPathMma ? (d == 128 ? 3 : 4)
-       : path == kPathMmaKv8 ? 6
-                             : (d == 128 ? 6 : 8);
-}
 // Columns (elements) of one TMA box row: 128-byte swizzled rows on the MMA paths.
 FD_HD constexpr int box_cols_for(int path, int d) {
   return path == kPathMma ? 64 : path == kPathMmaKv8 ? 128 : d;
@@ -50,12 +44,27 @@ FD_HD constexpr int box_cols_for(int path, int d) {
 // the previous kernel in the stream (4 measured best for fp16 and fp8 caches at
 // 32K and 128K tokens; 2 and 8 were slower).
 constexpr int kL2PrefetchTiles = 4;
+// The K/V ring, 96 KB.  On the fp16/bf16 tensor-core path a slot holds one tile of
+// K rows or of V rows of one KV head (tile kt: K in slot 2 kt mod S, V in slot
+// 2 kt + 1 mod S), so that loads are issued and waited for per 16 KB; on the other
+// paths a slot holds a tile of K rows followed by the tile of V rows.  (A 112 KB
+// ring, the most two CTAs per SM can hold, was slower on every path; 16 KB slots
+// were slower on the FP8 path, whose consumers are latency-bound.)
+constexpr int kRingBytes = 96 * 1024;
+FD_HD constexpr bool split_kv_slots(int path) { return path == kPathMma; }
+FD_HD constexpr int slot_bytes_for(int path, int d) {
+  return tile_for(path) * d * kv_elem_bytes(path) * (split_kv_slots(path) ? 1 : 2);
+}
+FD_HD constexpr int ring_slots_for(int path, int d) { return kRingBytes / slot_bytes_for(path, d); }
 // Bytes of the K/V ring (also the scratch the combine reuses).
 FD_HD constexpr size_t ring_bytes_for(int path, int d) {
-  return (size_t)stages_for(path, d) * 2 * tile_for(path) * d * kv_elem_bytes(path);
+  return (size_t)ring_slots_for(path, d) * slot_bytes_for(path, d);
 }
-// Dynamic shared memory of one CTA: the ring, the mbarriers and 1 KB of alignment slack.
-FD_HD constexpr size_t smem_bytes_for(int path, int d) { return ring_bytes_for(path, d) + 2048; }
+// Bytes after the ring: 2 mbarriers per slot, the combine's mbarrier, two flags,
+// and up to 1 KB of slack for aligning the ring to 1024 bytes.
+constexpr int kRingMetaBytes = 2048;
+// Dynamic shared memory of one CTA: the ring and its metadata.
+FD_HD constexpr size_t smem_bytes_for(int path, int d) { return ring_bytes_for(path, d) + kRingMetaBytes; }
 // Floats per partial record: O[0..d), m, l and two pad words (16-byte records).
 FD_HD constexpr int record_floats(int d) { return d + 4; }
 

@@ -865,27 +865,32 @@ __global__ void __launch_bounds__(kThreads, 2) fd_split_kernel(const __grid_cons
   constexpr bool kSeg = MODE >= 4;
   constexpr int kMode = kSeg ? MODE - 4 : MODE;
   constexpr int TILE = tile_for(PATH);
-  constexpr int STAGES = stages_for(PATH, D);
+  constexpr int NSLOT = ring_slots_for(PATH, D);
+  constexpr bool kSplitKV = split_kv_slots(PATH);  // a slot holds K or V rows, not both
+  constexpr int kFills = kSplitKV ? 2 : 1;         // slot fills per tile
   constexpr int BOXC = box_cols_for(PATH, D);   // columns per TMA box
   constexpr int NBOX = D / BOXC;                // boxes per tensor per stage
   constexpr int KVES = kv_elem_bytes(PATH);     // bytes per stored K/V element
-  constexpr uint32_t kRowsBytes = TILE * D * KVES;
-  constexpr uint32_t kStageBytes = 2 * kRowsBytes;
+  constexpr uint32_t kRowsBytes = TILE * D * KVES;  // one tile of K (or V) rows
+  constexpr uint32_t kSlotBytes = kFills == 2 ? kRowsBytes : 2 * kRowsBytes;
+  constexpr uint32_t kRing = NSLOT * kSlotBytes;
+  constexpr uint32_t kVOff = kFills == 2 ? 0u : kRowsBytes;  // V rows within their slot
+  static_assert(NSLOT >= 2 && kRowsBytes % 1024 == 0, "slots hold whole swizzle atoms");
+  static_assert((2 * NSLOT + 1) * 8 + 8 + 1024 <= kRingMetaBytes, "ring metadata must fit");
   constexpr int NGRP_FFMA = kConsumerWarps * (32 / ((G * D > 512) ? 16 : 8));
   constexpr int NGRP = is_mma(PATH) ? kConsumerWarps : NGRP_FFMA;
   static_assert(PATH == kPathFfma || G >= 4, "the MMA path needs G >= 4 heads on N");
-  static_assert(NGRP * G * D * 4 + 4 * NGRP * G * 4 + G * record_floats(D) * 4 <=
-                    STAGES * kStageBytes,
+  static_assert(NGRP * G * D * 4 + 4 * NGRP * G * 4 + G * record_floats(D) * 4 <= kRing,
                 "group merge and the segment-merge record must fit in the ring");
 
+  // 1024-byte aligned ring: the 128-byte swizzle pattern repeats every 1024 bytes.
   extern __shared__ uint8_t smem_raw[];
-  // 1024-byte aligned base: the 128-byte swizzle pattern repeats every 1024 bytes.
   uint8_t* smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + (size_t)STAGES * kStageBytes);
-  int& sm_abort = *reinterpret_cast<int*>(bars + 2 * STAGES + 1);
-  int& sm_last = *(reinterpret_cast<int*>(bars + 2 * STAGES + 1) + 1);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kRing);
+  int& sm_abort = *reinterpret_cast<int*>(bars + 2 * NSLOT + 1);
+  int& sm_last = *(reinterpret_cast<int*>(bars + 2 * NSLOT + 1) + 1);
   auto full_bar = [&](int s) { return smem_addr(bars + s); };
-  auto empty_bar = [&](int s) { return smem_addr(bars + STAGES + s); };
+  auto empty_bar = [&](int s) { return smem_addr(bars + NSLOT + s); };
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   pdl_launch_dependents();
@@ -893,11 +898,11 @@ __global__ void __launch_bounds__(kThreads, 2) fd_split_kernel(const __grid_cons
   const Work wk = decode_work(p, blockIdx.x, kSeg);
   const int ntiles = (wk.t1 - wk.t0 + TILE - 1) / TILE;
   if (tid == 0) {
-    for (int s = 0; s < STAGES; ++s) {
+    for (int s = 0; s < NSLOT; ++s) {
       mbar_init(full_bar(s), 1);
       mbar_init(empty_bar(s), kConsumerWarps);
     }
-    mbar_init(smem_addr(bars + 2 * STAGES), 1);  // combine copies
+    mbar_init(smem_addr(bars + 2 * NSLOT), 1);  // combine copies
     fence_mbar_init();
     sm_abort = 0;
   }
@@ -934,26 +939,30 @@ __global__ void __launch_bounds__(kThreads, 2) fd_split_kernel(const __grid_cons
     if (lane == 0 && ntiles > 0) {
       const uint64_t policy = l2_evict_first_policy();
       const int row0 = p.cu[wk.b] + wk.t0;
-      int kt = 0;
-      for (; kt < ntiles; ++kt) {
-        const int s = kt % STAGES;
-        if (kt >= STAGES && !mbar_wait(empty_bar(s), ((kt / STAGES) - 1) & 1)) {
+      // Slot fill i carries tile kt = i / kFills: its K rows, then its V rows (split
+      // slots: fill 2 kt holds K, fill 2 kt + 1 holds V).
+      const int nfills = kFills * ntiles;
+      int i = 0;
+      for (; i < nfills; ++i) {
+        const int s = i % NSLOT, kt = i / kFills;
+        if (i >= NSLOT && !mbar_wait(empty_bar(s), ((i / NSLOT) - 1) & 1)) {
           atomicOr(p.status, kStatusTimeout);
           *(volatile int*)&sm_abort = 1;
           break;
         }
         if (*(volatile int*)&sm_abort) break;
-        const uint32_t dst = smem_addr(smem + (size_t)s * kStageBytes);
-        mbar_arrive_expect_tx(full_bar(s), kStageBytes);
+        const uint32_t dst = smem_addr(smem + (size_t)s * kSlotBytes);
+        mbar_arrive_expect_tx(full_bar(s), kSlotBytes);
         if (p.block_table == nullptr) {
 #pragma unroll
-          for (int bx = 0; bx < NBOX; ++bx)
-            tma_load_3d(dst + bx * (TILE * BOXC * KVES), &p.tm_k, bx * BOXC, wk.kvh,
-                        row0 + kt * TILE, full_bar(s), policy);
+          for (int h = 0; h < 2; ++h) {
+            if (kFills == 2 && h != (i & 1)) continue;
+            const uint32_t d0 = dst + (kFills == 2 ? 0u : h * kRowsBytes);
 #pragma unroll
-          for (int bx = 0; bx < NBOX; ++bx)
-            tma_load_3d(dst + kRowsBytes + bx * (TILE * BOXC * KVES), &p.tm_v, bx * BOXC, wk.kvh,
-                        row0 + kt * TILE, full_bar(s), policy);
+            for (int bx = 0; bx < NBOX; ++bx)
+              tma_load_3d(d0 + bx * (TILE * BOXC * KVES), h ? &p.tm_v : &p.tm_k, bx * BOXC, wk.kvh,
+                          row0 + kt * TILE, full_bar(s), policy);
+          }
         } else {
           // Paged: one box per page piece of the tile.  Tiles start on multiples of
           // the tile size, so each box stays inside one page; boxes past the end of
@@ -965,19 +974,20 @@ __global__ void __launch_bounds__(kThreads, 2) fd_split_kernel(const __grid_cons
             const int pg = min((a + j) >> p.page_shift, last_pg);
             const int row = __ldg(bt + pg) * (1 << p.page_shift) + ((a + j) & ((1 << p.page_shift) - 1));
 #pragma unroll
-            for (int bx = 0; bx < NBOX; ++bx)
-              tma_load_3d(dst + bx * (TILE * BOXC * KVES) + j * BOXC * KVES, &p.tm_k, bx * BOXC, wk.kvh,
-                          row, full_bar(s), policy);
+            for (int h = 0; h < 2; ++h) {
+              if (kFills == 2 && h != (i & 1)) continue;
+              const uint32_t d0 = dst + (kFills == 2 ? 0u : h * kRowsBytes);
 #pragma unroll
-            for (int bx = 0; bx < NBOX; ++bx)
-              tma_load_3d(dst + kRowsBytes + bx * (TILE * BOXC * KVES) + j * BOXC * KVES, &p.tm_v,
-                          bx * BOXC, wk.kvh, row, full_bar(s), policy);
+              for (int bx = 0; bx < NBOX; ++bx)
+                tma_load_3d(d0 + bx * (TILE * BOXC * KVES) + j * BOXC * KVES, h ? &p.tm_v : &p.tm_k,
+                            bx * BOXC, wk.kvh, row, full_bar(s), policy);
+            }
           }
         }
       }
       // Every load issued must land before shared memory is reused or released.
-      for (int t = (kt > STAGES ? kt - STAGES : 0); t < kt; ++t) {
-        if (!mbar_wait(full_bar(t % STAGES), (t / STAGES) & 1)) atomicOr(p.status, kStatusTimeout);
+      for (int f = (i > NSLOT ? i - NSLOT : 0); f < i; ++f) {
+        if (!mbar_wait(full_bar(f % NSLOT), (f / NSLOT) & 1)) atomicOr(p.status, kStatusTimeout);
       }
     }
     __syncthreads();
@@ -1020,8 +1030,10 @@ __global__ void __launch_bounds__(kThreads, 2) fd_split_kernel(const __grid_cons
     const int tok0 = warp * 16;
 
     for (int kt = 0; kt < ntiles; ++kt) {
-      const int s = kt % STAGES;
-      const bool ok = mbar_wait(full_bar(s), (kt / STAGES) & 1);
+      // K and V slots of tile kt (the same slot unless K and V are split)
+      const int sk = (kFills * kt) % NSLOT, sv = (kFills * kt + kFills - 1) % NSLOT;
+      const bool ok = mbar_wait(full_bar(sk), ((kFills * kt) / NSLOT) & 1) &&
+                      (kFills == 1 || mbar_wait(full_bar(sv), ((kFills * kt + 1) / NSLOT) & 1));
       if (__any_sync(0xffffffffu, !ok || *(volatile int*)&sm_abort != 0)) {
         if (!ok) {
           atomicOr(p.status, kStatusTimeout);
@@ -1039,7 +1051,7 @@ __global__ void __launch_bounds__(kThreads, 2) fd_split_kernel(const __grid_cons
           for (int grp = 0; grp < 2; ++grp) {
             const int r = tok0 + g + 8 * rh, c = 2 * t + grp;
             kw[rh][grp] = *reinterpret_cast<const uint4*>(
-                smem + (size_t)s * kStageBytes + r * 128 + ((c ^ (r & 7)) << 4));
+                smem + (size_t)sk * kSlotBytes + r * 128 + ((c ^ (r & 7)) << 4));
           }
         float sc[NT][4];
 #pragma unroll
@@ -1099,8 +1111,8 @@ __global__ void __launch_bounds__(kThreads, 2) fd_split_kernel(const __grid_cons
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           const int r = tok0 + 2 * t + (i & 1) + 8 * (i >> 1);
-          vw[i] = *reinterpret_cast<const uint4*>(smem + (size_t)s * kStageBytes + kRowsBytes +
-                                                  r * 128 + ((g ^ (r & 7)) << 4));
+          vw[i] = *reinterpret_cast<const uint4*>(smem + (size_t)sv * kSlotBytes + kVOff + r * 128 +
+                                                  ((g ^ (r & 7)) << 4));
         }
 #pragma unroll
         for (int mi = 0; mi < KT; ++mi) {
@@ -1124,7 +1136,10 @@ __global__ void __launch_bounds__(kThreads, 2) fd_split_kernel(const __grid_cons
         }
       }
       __syncwarp();
-      if (lane == 0) mbar_arrive(empty_bar(s));
+      if (lane == 0) {
+        mbar_arrive(empty_bar(sk));
+        if (kFills == 2) mbar_arrive(empty_bar(sv));
+      }
     }
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
@@ -1193,8 +1208,10 @@ __global__ void __launch_bounds__(kThreads, 2) fd_split_kernel(const __grid_cons
     const int vrow = tok0 + (mj >> 1) * 8 + mr;  // V rows this lane addresses (A = V^T)
 
     for (int kt = 0; kt < ntiles; ++kt) {
-      const int s = kt % STAGES;
-      const bool ok = mbar_wait(full_bar(s), (kt / STAGES) & 1);
+      // K and V slots of tile kt (the same slot unless K and V are split)
+      const int sk = (kFills * kt) % NSLOT, sv = (kFills * kt + kFills - 1) % NSLOT;
+      const bool ok = mbar_wait(full_bar(sk), ((kFills * kt) / NSLOT) & 1) &&
+                      (kFills == 1 || mbar_wait(full_bar(sv), ((kFills * kt + 1) / NSLOT) & 1));
       if (__any_sync(0xffffffffu, !ok || *(volatile int*)&sm_abort != 0)) {
         if (!ok) {
           atomicOr(p.status, kStatusTimeout);
@@ -1204,8 +1221,8 @@ __global__ void __launch_bounds__(kThreads, 2) fd_split_kernel(const __grid_cons
       }
       const int ntok = min(TILE, wk.t1 - (wk.t0 + kt * TILE));
       if (tok0 < ntok) {
-        const uint32_t kbase = smem_addr(smem + (size_t)s * kStageBytes);
-        const uint32_t vbase = kbase + kRowsBytes;
+        const uint32_t kbase = smem_addr(smem + (size_t)sk * kSlotBytes);
+        const uint32_t vbase = smem_addr(smem + (size_t)sv * kSlotBytes + kVOff);
         float sc[NT][4];
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
@@ -1262,7 +1279,10 @@ __global__ void __launch_bounds__(kThreads, 2) fd_split_kernel(const __grid_cons
         }
       }
       __syncwarp();
-      if (lane == 0) mbar_arrive(empty_bar(s));
+      if (lane == 0) {
+        mbar_arrive(empty_bar(sk));
+        if (kFills == 2) mbar_arrive(empty_bar(sv));
+      }
     }
     // Row sums: lanes sharing a head pair hold partial sums over their tokens.
 #pragma unroll
@@ -1330,9 +1350,11 @@ __global__ void __launch_bounds__(kThreads, 2) fd_split_kernel(const __grid_cons
     }
 
     for (int kt = 0; kt < ntiles; ++kt) {
-      const int s = kt % STAGES;
+      // K and V slots of tile kt (the same slot unless K and V are split)
+      const int sk = (kFills * kt) % NSLOT, sv = (kFills * kt + kFills - 1) % NSLOT;
       // Every lane waits; the warp leaves together so shuffles never see a partial warp.
-      const bool ok = mbar_wait(full_bar(s), (kt / STAGES) & 1);
+      const bool ok = mbar_wait(full_bar(sk), ((kFills * kt) / NSLOT) & 1) &&
+                      (kFills == 1 || mbar_wait(full_bar(sv), ((kFills * kt + 1) / NSLOT) & 1));
       if (__any_sync(0xffffffffu, !ok || *(volatile int*)&sm_abort != 0)) {
         if (!ok) {
           atomicOr(p.status, kStatusTimeout);
@@ -1341,8 +1363,8 @@ __global__ void __launch_bounds__(kThreads, 2) fd_split_kernel(const __grid_cons
         break;
       }
       const int ntok = min(TILE, wk.t1 - (wk.t0 + kt * TILE));
-      const T* Ks = reinterpret_cast<const T*>(smem + (size_t)s * kStageBytes);
-      const T* Vs = Ks + TILE * D;
+      const T* Ks = reinterpret_cast<const T*>(smem + (size_t)sk * kSlotBytes);
+      const T* Vs = reinterpret_cast<const T*>(smem + (size_t)sv * kSlotBytes + kVOff);
 
       float sc[TPG][G];
 #pragma unroll
@@ -1408,7 +1430,10 @@ __global__ void __launch_bounds__(kThreads, 2) fd_split_kernel(const __grid_cons
         }
       }
       __syncwarp();
-      if (lane == 0) mbar_arrive(empty_bar(s));
+      if (lane == 0) {
+        mbar_arrive(empty_bar(sk));
+        if (kFills == 2) mbar_arrive(empty_bar(sv));
+      }
     }
     __syncthreads();  // ring drained: reuse it for the per-group states
     if (*(volatile int*)&sm_abort == 0) {
@@ -1433,9 +1458,8 @@ __global__ void __launch_bounds__(kThreads, 2) fd_split_kernel(const __grid_cons
   // A CTA of a cluster must still reach the cluster barriers: it finishes with an
   // empty partial instead.
   if (sm_abort && !kSeg) return;
-  finish_cta<T, D, G, NGRP, kMode, kSeg>(p, wk, sm_acc, sm_last, sm_abort != 0, smem,
-                                         STAGES * kStageBytes,
-                                  smem_addr(bars + 2 * STAGES));
+  finish_cta<T, D, G, NGRP, kMode, kSeg>(p, wk, sm_acc, sm_last, sm_abort != 0, smem, kRing,
+                                         smem_addr(bars + 2 * NSLOT));
 }
 
 // Two-launch ablation, second kernel: one CTA per (sequence, KV head) combines
@@ -1443,7 +1467,7 @@ __global__ void __launch_bounds__(kThreads, 2) fd_split_kernel(const __grid_cons
 template <typename T, int D, int G, int PATH>
 __global__ void __launch_bounds__(kThreads, 2) fd_combine_kernel(const __grid_constant__ Params p) {
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
+  uint8_t* smem = smem_raw;  // bulk copies need 16-byte alignment only
   constexpr uint32_t kBytes = (uint32_t)ring_bytes_for(PATH, D);
   uint64_t* bar = reinterpret_cast<uint64_t*>(smem + kBytes);
   pdl_launch_dependents();

@@ -162,7 +162,7 @@ def test_literal_w_and_auto_chunks():
 
 
 def test_records_per_segment():
-    ring = {128: 3 * 2 * 64 * 128 * 2, 64: 4 * 2 * 64 * 64 * 2}   # tensor-core rings (bytes)
+    ring = {128: 96 * 1024, 64: 96 * 1024}   # K/V rings (bytes)
     # Auto: chunk records merge per segment (in a cluster of 2..8 CTAs) exactly when one
     # (sequence, KV head)'s records, G * W * C * (d + 4) * 4 bytes, exceed the ring
     # (twice the ring over an FP8 cache).
@@ -208,11 +208,15 @@ def test_fp8_kv_plan_rules():
 
 
 def test_combine_scratch_limit():
-    # G = 16 with 1024 partials needs more combine scratch than the d = 64 ring holds
-    with pytest.raises(fd.FdError) as ei:
-        fd.fd_plan(1, 128, 8, 64, [100000], 1024, "f16", flags=fd.FD_PLAN_LITERAL_W, num_sms=152)
+    # The combine's coefficient scratch, (G * partials + 2 G) * 4 bytes, must fit the ring
+    # it reuses; with a 96 KB ring even G = 16 with 1024 partials fits (66 KB), for the
+    # fine-grained-waits variant too.
+    fd.fd_plan(1, 128, 8, 64, [100000], 1024, "f16", flags=fd.FD_PLAN_LITERAL_W, num_sms=152)
+    fd.fd_plan(1, 128, 8, 128, [100000], 1024, "f16", flags=fd.FD_PLAN_LITERAL_W | fd.FD_PLAN_WAITS,
+               num_sms=152)
+    with pytest.raises(fd.FdError) as ei:          # beyond the partial-record limit
+        fd.fd_plan(1, 128, 8, 64, [100000], 1025, "f16", flags=fd.FD_PLAN_LITERAL_W, num_sms=152)
     assert ei.value.status == fd.FD_ERR_UNSUPPORTED
-    fd.fd_plan(1, 128, 8, 128, [100000], 1024, "f16", flags=fd.FD_PLAN_LITERAL_W, num_sms=152)
 
 
 def test_workspace_layout():
