@@ -44,17 +44,13 @@ FD_HD constexpr int box_cols_for(int path, int d) {
 // the previous kernel in the stream (4 measured best for fp16 and fp8 caches at
 // 32K and 128K tokens; 2 and 8 were slower).
 constexpr int kL2PrefetchTiles = 4;
-// The K/V ring, 96 KB.  On the fp16/bf16 tensor-core path a slot holds one tile of
-// K rows or of V rows of one KV head (tile kt: K in slot 2 kt mod S, V in slot
-// 2 kt + 1 mod S), so that loads are issued and waited for per 16 KB; on the other
-// paths a slot holds a tile of K rows followed by the tile of V rows.  (A 112 KB
-// ring, the most two CTAs per SM can hold, was slower on every path; 16 KB slots
-// were slower on the FP8 path, whose consumers are latency-bound.)
+// The K/V ring, 96 KB on every path: slots of one tile of K rows followed by the
+// tile of V rows of one KV head.  (At d = 64 the ring used to be 64 KB; 96 KB is
+// 14% faster at 32K tokens.  A 112 KB ring, the most two CTAs per SM can hold,
+// was slower on every path, and so were separate K and V slots with their own
+// barriers on the multi-wave and FP8 cases.)
 constexpr int kRingBytes = 96 * 1024;
-FD_HD constexpr bool split_kv_slots(int path) { return path == kPathMma; }
-FD_HD constexpr int slot_bytes_for(int path, int d) {
-  return tile_for(path) * d * kv_elem_bytes(path) * (split_kv_slots(path) ? 1 : 2);
-}
+FD_HD constexpr int slot_bytes_for(int path, int d) { return 2 * tile_for(path) * d * kv_elem_bytes(path); }
 FD_HD constexpr int ring_slots_for(int path, int d) { return kRingBytes / slot_bytes_for(path, d); }
 // Bytes of the K/V ring (also the scratch the combine reuses).
 FD_HD constexpr size_t ring_bytes_for(int path, int d) {

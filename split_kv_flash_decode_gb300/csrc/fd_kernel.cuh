@@ -865,16 +865,13 @@ __global__ void __launch_bounds__(kThreads, 2) fd_split_kernel(const __grid_cons
   constexpr bool kSeg = MODE >= 4;
   constexpr int kMode = kSeg ? MODE - 4 : MODE;
   constexpr int TILE = tile_for(PATH);
-  constexpr int NSLOT = ring_slots_for(PATH, D);
-  constexpr bool kSplitKV = split_kv_slots(PATH);  // a slot holds K or V rows, not both
-  constexpr int kFills = kSplitKV ? 2 : 1;         // slot fills per tile
+  constexpr int NSLOT = ring_slots_for(PATH, D);  // ring slots (one K + V tile each)
   constexpr int BOXC = box_cols_for(PATH, D);   // columns per TMA box
   constexpr int NBOX = D / BOXC;                // boxes per tensor per stage
   constexpr int KVES = kv_elem_bytes(PATH);     // bytes per stored K/V element
   constexpr uint32_t kRowsBytes = TILE * D * KVES;  // one tile of K (or V) rows
-  constexpr uint32_t kSlotBytes = kFills == 2 ? kRowsBytes : 2 * kRowsBytes;
+  constexpr uint32_t kSlotBytes = 2 * kRowsBytes;   // K rows, then V rows
   constexpr uint32_t kRing = NSLOT * kSlotBytes;
-  constexpr uint32_t kVOff = kFills == 2 ? 0u : kRowsBytes;  // V rows within their slot
   static_assert(NSLOT >= 2 && kRowsBytes % 1024 == 0, "slots hold whole swizzle atoms");
   static_assert((2 * NSLOT + 1) * 8 + 8 + 1024 <= kRingMetaBytes, "ring metadata must fit");
   constexpr int NGRP_FFMA = kConsumerWarps * (32 / ((G * D > 512) ? 16 : 8));
@@ -939,13 +936,11 @@ __global__ void __launch_bounds__(kThreads, 2) fd_split_kernel(const __grid_cons
     if (lane == 0 && ntiles > 0) {
       const uint64_t policy = l2_evict_first_policy();
       const int row0 = p.cu[wk.b] + wk.t0;
-      // Slot fill i carries tile kt = i / kFills: its K rows, then its V rows (split
-      // slots: fill 2 kt holds K, fill 2 kt + 1 holds V).
-      const int nfills = kFills * ntiles;
-      int i = 0;
-      for (; i < nfills; ++i) {
-        const int s = i % NSLOT, kt = i / kFills;
-        if (i >= NSLOT && !mbar_wait(empty_bar(s), ((i / NSLOT) - 1) & 1)) {
+      // Tile kt goes to slot kt mod NSLOT: its K rows, then its V rows.
+      int kt = 0;
+      for (; kt < ntiles; ++kt) {
+        const int s = kt % NSLOT;
+        if (kt >= NSLOT && !mbar_wait(empty_bar(s), ((kt / NSLOT) - 1) & 1)) {
           atomicOr(p.status, kStatusTimeout);
           *(volatile int*)&sm_abort = 1;
           break;
@@ -955,13 +950,11 @@ __global__ void __launch_bounds__(kThreads, 2) fd_split_kernel(const __grid_cons
         mbar_arrive_expect_tx(full_bar(s), kSlotBytes);
         if (p.block_table == nullptr) {
 #pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            if (kFills == 2 && h != (i & 1)) continue;
-            const uint32_t d0 = dst + (kFills == 2 ? 0u : h * kRowsBytes);
+          for (int h = 0; h < 2; ++h) {  // K rows, then V rows
 #pragma unroll
             for (int bx = 0; bx < NBOX; ++bx)
-              tma_load_3d(d0 + bx * (TILE * BOXC * KVES), h ? &p.tm_v : &p.tm_k, bx * BOXC, wk.kvh,
-                          row0 + kt * TILE, full_bar(s), policy);
+              tma_load_3d(dst + h * kRowsBytes + bx * (TILE * BOXC * KVES), h ? &p.tm_v : &p.tm_k,
+                          bx * BOXC, wk.kvh, row0 + kt * TILE, full_bar(s), policy);
           }
         } else {
           // Paged: one box per page piece of the tile.  Tiles start on multiples of
@@ -974,20 +967,18 @@ __global__ void __launch_bounds__(kThreads, 2) fd_split_kernel(const __grid_cons
             const int pg = min((a + j) >> p.page_shift, last_pg);
             const int row = __ldg(bt + pg) * (1 << p.page_shift) + ((a + j) & ((1 << p.page_shift) - 1));
 #pragma unroll
-            for (int h = 0; h < 2; ++h) {
-              if (kFills == 2 && h != (i & 1)) continue;
-              const uint32_t d0 = dst + (kFills == 2 ? 0u : h * kRowsBytes);
+            for (int h = 0; h < 2; ++h) {  // K rows, then V rows
 #pragma unroll
               for (int bx = 0; bx < NBOX; ++bx)
-                tma_load_3d(d0 + bx * (TILE * BOXC * KVES) + j * BOXC * KVES, h ? &p.tm_v : &p.tm_k,
-                            bx * BOXC, wk.kvh, row, full_bar(s), policy);
+                tma_load_3d(dst + h * kRowsBytes + bx * (TILE * BOXC * KVES) + j * BOXC * KVES,
+                            h ? &p.tm_v : &p.tm_k, bx * BOXC, wk.kvh, row, full_bar(s), policy);
             }
           }
         }
       }
       // Every load issued must land before shared memory is reused or released.
-      for (int f = (i > NSLOT ? i - NSLOT : 0); f < i; ++f) {
-        if (!mbar_wait(full_bar(f % NSLOT), (f / NSLOT) & 1)) atomicOr(p.status, kStatusTimeout);
+      for (int t = (kt > NSLOT ? kt - NSLOT : 0); t < kt; ++t) {
+        if (!mbar_wait(full_bar(t % NSLOT), (t / NSLOT) & 1)) atomicOr(p.status, kStatusTimeout);
       }
     }
     __syncthreads();
@@ -1030,10 +1021,8 @@ __global__ void __launch_bounds__(kThreads, 2) fd_split_kernel(const __grid_cons
     const int tok0 = warp * 16;
 
     for (int kt = 0; kt < ntiles; ++kt) {
-      // K and V slots of tile kt (the same slot unless K and V are split)
-      const int sk = (kFills * kt) % NSLOT, sv = (kFills * kt + kFills - 1) % NSLOT;
-      const bool ok = mbar_wait(full_bar(sk), ((kFills * kt) / NSLOT) & 1) &&
-                      (kFills == 1 || mbar_wait(full_bar(sv), ((kFills * kt + 1) / NSLOT) & 1));
+      const int s = kt % NSLOT;
+      const bool ok = mbar_wait(full_bar(s), (kt / NSLOT) & 1);
       if (__any_sync(0xffffffffu, !ok || *(volatile int*)&sm_abort != 0)) {
         if (!ok) {
           atomicOr(p.status, kStatusTimeout);
@@ -1051,7 +1040,7 @@ __global__ void __launch_bounds__(kThreads, 2) fd_split_kernel(const __grid_cons
           for (int grp = 0; grp < 2; ++grp) {
             const int r = tok0 + g + 8 * rh, c = 2 * t + grp;
             kw[rh][grp] = *reinterpret_cast<const uint4*>(
-                smem + (size_t)sk * kSlotBytes + r * 128 + ((c ^ (r & 7)) << 4));
+                smem + (size_t)s * kSlotBytes + r * 128 + ((c ^ (r & 7)) << 4));
           }
         float sc[NT][4];
 #pragma unroll
@@ -1111,8 +1100,8 @@ __global__ void __launch_bounds__(kThreads, 2) fd_split_kernel(const __grid_cons
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           const int r = tok0 + 2 * t + (i & 1) + 8 * (i >> 1);
-          vw[i] = *reinterpret_cast<const uint4*>(smem + (size_t)sv * kSlotBytes + kVOff + r * 128 +
-                                                  ((g ^ (r & 7)) << 4));
+          vw[i] = *reinterpret_cast<const uint4*>(smem + (size_t)s * kSlotBytes + kRowsBytes +
+                                                  r * 128 + ((g ^ (r & 7)) << 4));
         }
 #pragma unroll
         for (int mi = 0; mi < KT; ++mi) {
@@ -1136,10 +1125,7 @@ __global__ void __launch_bounds__(kThreads, 2) fd_split_kernel(const __grid_cons
         }
       }
       __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(empty_bar(sk));
-        if (kFills == 2) mbar_arrive(empty_bar(sv));
-      }
+      if (lane == 0) mbar_arrive(empty_bar(s));
     }
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
@@ -1208,10 +1194,8 @@ __global__ void __launch_bounds__(kThreads, 2) fd_split_kernel(const __grid_cons
     const int vrow = tok0 + (mj >> 1) * 8 + mr;  // V rows this lane addresses (A = V^T)
 
     for (int kt = 0; kt < ntiles; ++kt) {
-      // K and V slots of tile kt (the same slot unless K and V are split)
-      const int sk = (kFills * kt) % NSLOT, sv = (kFills * kt + kFills - 1) % NSLOT;
-      const bool ok = mbar_wait(full_bar(sk), ((kFills * kt) / NSLOT) & 1) &&
-                      (kFills == 1 || mbar_wait(full_bar(sv), ((kFills * kt + 1) / NSLOT) & 1));
+      const int s = kt % NSLOT;
+      const bool ok = mbar_wait(full_bar(s), (kt / NSLOT) & 1);
       if (__any_sync(0xffffffffu, !ok || *(volatile int*)&sm_abort != 0)) {
         if (!ok) {
           atomicOr(p.status, kStatusTimeout);
@@ -1221,8 +1205,8 @@ __global__ void __launch_bounds__(kThreads, 2) fd_split_kernel(const __grid_cons
       }
       const int ntok = min(TILE, wk.t1 - (wk.t0 + kt * TILE));
       if (tok0 < ntok) {
-        const uint32_t kbase = smem_addr(smem + (size_t)sk * kSlotBytes);
-        const uint32_t vbase = smem_addr(smem + (size_t)sv * kSlotBytes + kVOff);
+        const uint32_t kbase = smem_addr(smem + (size_t)s * kSlotBytes);
+        const uint32_t vbase = kbase + kRowsBytes;
         float sc[NT][4];
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
@@ -1279,10 +1263,7 @@ __global__ void __launch_bounds__(kThreads, 2) fd_split_kernel(const __grid_cons
         }
       }
       __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(empty_bar(sk));
-        if (kFills == 2) mbar_arrive(empty_bar(sv));
-      }
+      if (lane == 0) mbar_arrive(empty_bar(s));
     }
     // Row sums: lanes sharing a head pair hold partial sums over their tokens.
 #pragma unroll
@@ -1350,11 +1331,9 @@ __global__ void __launch_bounds__(kThreads, 2) fd_split_kernel(const __grid_cons
     }
 
     for (int kt = 0; kt < ntiles; ++kt) {
-      // K and V slots of tile kt (the same slot unless K and V are split)
-      const int sk = (kFills * kt) % NSLOT, sv = (kFills * kt + kFills - 1) % NSLOT;
+      const int s = kt % NSLOT;
       // Every lane waits; the warp leaves together so shuffles never see a partial warp.
-      const bool ok = mbar_wait(full_bar(sk), ((kFills * kt) / NSLOT) & 1) &&
-                      (kFills == 1 || mbar_wait(full_bar(sv), ((kFills * kt + 1) / NSLOT) & 1));
+      const bool ok = mbar_wait(full_bar(s), (kt / NSLOT) & 1);
       if (__any_sync(0xffffffffu, !ok || *(volatile int*)&sm_abort != 0)) {
         if (!ok) {
           atomicOr(p.status, kStatusTimeout);
@@ -1363,8 +1342,8 @@ __global__ void __launch_bounds__(kThreads, 2) fd_split_kernel(const __grid_cons
         break;
       }
       const int ntok = min(TILE, wk.t1 - (wk.t0 + kt * TILE));
-      const T* Ks = reinterpret_cast<const T*>(smem + (size_t)sk * kSlotBytes);
-      const T* Vs = reinterpret_cast<const T*>(smem + (size_t)sv * kSlotBytes + kVOff);
+      const T* Ks = reinterpret_cast<const T*>(smem + (size_t)s * kSlotBytes);
+      const T* Vs = Ks + TILE * D;
 
       float sc[TPG][G];
 #pragma unroll
@@ -1430,10 +1409,7 @@ __global__ void __launch_bounds__(kThreads, 2) fd_split_kernel(const __grid_cons
         }
       }
       __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(empty_bar(sk));
-        if (kFills == 2) mbar_arrive(empty_bar(sv));
-      }
+      if (lane == 0) mbar_arrive(empty_bar(s));
     }
     __syncthreads();  // ring drained: reuse it for the per-group states
     if (*(volatile int*)&sm_abort == 0) {
