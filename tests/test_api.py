@@ -159,6 +159,8 @@ def test_literal_w_and_auto_chunks():
     assert p.info["chunks"] == 8  # 1024-token segments -> 128-token chunks, 256 CTAs
     p = fd.fd_plan(1, 8, 8, 64, [100], 4, "f16", num_sms=152)
     assert p.info["chunks"] == 1
+    p = fd.fd_plan(1, 8, 8, 64, [2048], 4, "f16", num_sms=152)
+    assert p.info["chunks"] == 4  # 512-token segments -> 128-token chunks, not 9 slots' worth
 
 
 def test_records_per_segment():
@@ -183,6 +185,16 @@ def test_records_per_segment():
     for flags in (fd.FD_PLAN_NO_CLUSTER, fd.FD_PLAN_WAITS):
         p = fd.fd_plan(1, 64, 8, 128, [131072], 8, "f16", flags=flags, num_sms=152)
         assert p.info["chunks"] == 4 and p.info["records_per_segment"] == 4
+    # paged plans follow the same rule; one chunk per segment never forms a cluster
+    p = fd.fd_plan_paged(1, 64, 8, 128, [131072], 8, 64, "f16", num_sms=152)
+    assert p.info["chunks"] == 4 and p.info["records_per_segment"] == 1
+    p = fd.fd_plan(1, 32, 8, 128, [32768], 8, "f16", flags=fd.FD_PLAN_CLUSTER | fd.FD_PLAN_LITERAL_W,
+                   num_sms=152)
+    assert p.info["chunks"] == 1 and p.info["records_per_segment"] == 1
+    # more than 8 chunks per segment cannot form a (portable) cluster
+    p = fd.fd_plan(1, 32, 8, 128, [32768], 8, "f16", flags=fd.FD_PLAN_CLUSTER, chunks=12,
+                   num_sms=152)
+    assert p.info["records_per_segment"] == 12
 
 
 def test_consumer_path_choice():
