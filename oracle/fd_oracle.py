@@ -20,7 +20,7 @@ follows the split method step by step (segment rule, per-segment partial,
 OnlineSoftmaxCombine fold, final normalisation) and is pinned against the
 definition by the tests.
 
-Readings where the pages are silent (each is also listed in the design doc):
+Readings where the pages are silent:
   * logit scale 1/sqrt(d); lse is the natural log of sum_j exp(s_j) over the
     *scaled* logits s_j;
   * GQA: query head h reads KV head h // G with G = Hq / Hkv;
