@@ -3,16 +3,22 @@
 
 Prints ONE JSON line on rank 0.  A step is one fused decode (all of the hot
 path: KV streaming, scores, online softmax, P.V, partial write, arrival and the
-last-arriver combine) over one batch of synthetic input.
+last-arriver combine) over one batch of synthetic input.  The default workload is
+the largest decode case: B=64 sequences of 8192 tokens, GQA 32/8, d=128, bf16,
+W=16 segments each (2.15 GB of K/V per decode).
 
   value     KV-read GB/s over exactly --steps steps replayed from a CUDA graph,
-            inputs resident in HBM; K/V rotate over enough copies that every
-            step reads from HBM (copies x bytes >= 4 x L2).
+            inputs resident in HBM, launched back to back; K/V rotate over
+            enough copies that every step reads from HBM (copies x bytes >= 4 x L2).
   latency   per-launch device time (CUDA events around every launch).
+  isolated  one decode alone: an L2 flush (a read of a 2 x L2 buffer, an unrelated
+            kernel) runs before every decode, and events bracket the decode only.
   roofline  KV bytes per launch / mean launch time vs the measured HBM peak.
+  extra_cases  the 32K and 128K single-sequence cases, step and isolated figures.
   e2e       the same metric through fd_decode with pinned HOST buffers: every
             step copies q, K, V in and out, lse back.
-  cpu_baseline  the fp64 oracle on the host cores (1 thread), bounded sample.
+  cpu_baseline  the fp64 oracle on all host cores (a process per core, split over
+            (sequence, query head)) and on 1 core, bounded sample.
 
 ``--impl reference`` times the fp64 oracle instead (rank 0 only).
 Multi-GPU: N independent replicas (the decode has no cross-GPU exchange).
@@ -33,7 +39,10 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
-DEFAULT_WORKLOAD = "gqa4_d128_L32k_W8"
+DEFAULT_WORKLOAD = "batch64_gqa4_d128_L8k_bf16"
+DEFAULT_W = 16
+# Reported beside the headline: the 32K and 128K single-sequence decode cases.
+EXTRA_CASES = ("gqa4_d128_L32k_W8", "gqa8_d128_L128k_W8_spiky")
 METRIC = "decode latency (µs) and achieved KV-read HBM GB/s (% of GB300 peak), 1 GPU"
 FALLBACK_HBM_GBS = 6800.0
 
@@ -45,10 +54,11 @@ def parse_args(argv=None):
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["fd", "reference"], default="fd")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
-    ap.add_argument("--W", type=int, default=1, help="segments for the batch64 W-sweep workload")
+    ap.add_argument("--W", type=int, default=DEFAULT_W, help="segments for the batch64 W-sweep workload")
     ap.add_argument("--chunks", type=int, default=0, help="chunks per segment (0 = planner)")
     ap.add_argument("--two-launch", action="store_true", help="split + combine as two kernels")
     ap.add_argument("--ffma", action="store_true", help="CUDA-core consumers even when G >= 4")
+    ap.add_argument("--tcgen05", action="store_true", help="tcgen05 tensor cores (d = 128, G >= 4)")
     ap.add_argument("--no-pdl", action="store_true", help="launch without programmatic dependent launch")
     ap.add_argument("--no-cluster", action="store_true",
                     help="one partial record per chunk (no in-cluster segment merge)")
@@ -66,6 +76,8 @@ def parse_args(argv=None):
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--ref-budget-s", type=float, default=120.0)
     ap.add_argument("--no-graph", action="store_true", help="launch each step from Python")
+    ap.add_argument("--no-extra", action="store_true", help="skip the 32K / 128K extra cases")
+    ap.add_argument("--extra-steps", type=int, default=500)
     ap.add_argument("--cpu-baseline-only", action="store_true", help=argparse.SUPPRESS)
     return ap.parse_args(argv)
 
@@ -198,6 +210,10 @@ class ClockSampler:
 # CPU side: the fp64 oracle (cpu_baseline and the reference arm).
 # ---------------------------------------------------------------------------
 
+def _kv_elem_bytes(problem):
+    return 1 if problem.kv_type == "e4m3" else 2
+
+
 def _oracle_sample(problem, n_tokens):
     """The first n_tokens of every sequence (all heads) as a standalone problem."""
     import numpy as np
@@ -207,44 +223,98 @@ def _oracle_sample(problem, n_tokens):
     vs = [problem.v[cu[b]:cu[b] + lens[b]] for b in range(problem.B)]
     k = np.concatenate(ks) if ks else problem.k[:0]
     v = np.concatenate(vs) if vs else problem.v[:0]
-    return lens, k, v, int(lens.sum()) * problem.Hkv * problem.d * 2 * 2
+    nbytes = int(lens.sum()) * problem.Hkv * problem.d * 2 * _kv_elem_bytes(problem)
+    return lens, k, v, nbytes
 
 
 def time_oracle_step(problem, n_tokens):
     import oracle
     lens, k, v, nbytes = _oracle_sample(problem, n_tokens)
     t = time.perf_counter()
-    oracle.decode_reference(problem.q, k, v, lens, problem.dtype)
+    oracle.decode_reference(problem.q, k, v, lens, problem.dtype, kv_dtype=problem.kv_dtype or None)
     return time.perf_counter() - t, nbytes
 
 
-def cpu_baseline_only(args):
-    """Runs in a 1-thread subprocess: the oracle on a bounded sample for ~cpu_seconds."""
-    prob = make_problem(args)
+# The sample the worker processes decode: set before the pool forks, so that every
+# worker inherits it (this process never touches the GPU, so forking is safe).
+_SAMPLE = None
+
+
+def _oracle_heads(heads):
+    import oracle
+    q, k, v, lens, dtype, kv_dtype = _SAMPLE
+    oracle.decode_reference(q, k, v, lens, dtype, heads=heads, kv_dtype=kv_dtype)
+    return len(heads)
+
+
+class ParallelOracle:
+    """The fp64 oracle on every host core: one process per core, each decoding a
+    contiguous share of the (sequence, query head) pairs of the same sample."""
+
+    def __init__(self, problem, n_tokens, cores=None):
+        import multiprocessing as mp
+        global _SAMPLE
+        lens, k, v, self.nbytes = _oracle_sample(problem, n_tokens)
+        _SAMPLE = (problem.q, k, v, lens, problem.dtype, problem.kv_dtype or None)
+        self.cores = int(cores or os.cpu_count() or 1)
+        pairs = [(b, h) for b in range(problem.B) for h in range(problem.Hq)]
+        n = min(self.cores, len(pairs))
+        self.shares = [pairs[i * len(pairs) // n:(i + 1) * len(pairs) // n] for i in range(n)]
+        self.pool = mp.get_context("fork").Pool(self.cores)
+
+    def step(self):
+        t = time.perf_counter()
+        self.pool.map(_oracle_heads, self.shares, chunksize=1)
+        return time.perf_counter() - t, self.nbytes
+
+    def close(self):
+        self.pool.close()
+        self.pool.join()
+
+
+def _choose_sample(prob, budget_s):
+    """Tokens per sequence such that one 1-thread oracle decode takes about budget_s."""
     n = int(prob.seqlens.max())
-    # Calibrate on a small prefix, then size the sample to ~cpu_seconds / 3 per call.
     dt, nb = time_oracle_step(prob, min(n, 2048))
     per_byte = dt / max(nb, 1)
-    full_bytes = prob.kv_bytes
-    target = args.cpu_seconds / 3.0
-    n_tok = n if per_byte * full_bytes <= target else max(256, int(n * target / (per_byte * full_bytes)))
-    total_t, total_b, calls = 0.0, 0, 0
-    while total_t < args.cpu_seconds and calls < 1000:
-        dt, nb = time_oracle_step(prob, n_tok)
-        total_t += dt
-        total_b += nb
-        calls += 1
+    full = prob.kv_bytes
+    return n if per_byte * full <= budget_s else max(256, int(n * budget_s / (per_byte * full)))
+
+
+def cpu_baseline_only(args):
+    """Runs in a subprocess that never touches the GPU: the oracle on a bounded sample,
+    about cpu_seconds on all cores, then about cpu_seconds on one core."""
+    prob = make_problem(args)
+    n = int(prob.seqlens.max())
+    n_tok = _choose_sample(prob, args.cpu_seconds / 3.0)
     frac = "all" if n_tok >= n else f"first {n_tok}"
-    return {"value": total_b / total_t / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
-            "sample": f"{calls} x fp64 oracle decode of {prob.name} ({frac} tokens of every "
-                      f"sequence, all heads), {total_t:.1f} s, 1 thread"}
+    what = f"fp64 oracle decode of {prob.name} ({frac} tokens of every sequence, all heads)"
+
+    par = ParallelOracle(prob, n_tok)
+    par.step()                                         # warm the workers
+    pt, pb, pcalls = 0.0, 0, 0
+    while pt < args.cpu_seconds and pcalls < 1000:
+        dt, nb = par.step()
+        pt, pb, pcalls = pt + dt, pb + nb, pcalls + 1
+    par.close()
+
+    st, sb, scalls = 0.0, 0, 0
+    while st < args.cpu_seconds and scalls < 1000:
+        dt, nb = time_oracle_step(prob, n_tok)
+        st, sb, scalls = st + dt, sb + nb, scalls + 1
+    return {"value": pb / pt / 1e9, "unit": "GB/s", "cores": par.cores, "kind": "oracle",
+            "sample": f"{pcalls} x {what}, {pt:.1f} s wall on {par.cores} processes (one per "
+                      f"host core, split over (sequence, query head)), 1 BLAS thread each",
+            "single_core": {"value": sb / st / 1e9, "unit": "GB/s", "cores": 1,
+                            "sample": f"{scalls} x the same decode, {st:.1f} s, 1 thread"}}
 
 
 def run_cpu_baseline_subprocess(args):
     env = dict(os.environ, **_ONE_THREAD)
     cmd = [sys.executable, os.path.abspath(__file__), "--cpu-baseline-only", "--workload",
-           args.workload, "--W", str(args.W), "--cpu-seconds", str(args.cpu_seconds)]
-    res = subprocess.run(cmd, env=env, capture_output=True, text=True, timeout=600)
+           args.workload, "--W", str(args.W), "--cpu-seconds", str(args.cpu_seconds),
+           "--kv", args.kv]
+    res = subprocess.run(cmd, env=env, capture_output=True, text=True, timeout=900)
     if res.returncode != 0:
         return {"value": None, "unit": "GB/s", "cores": 1, "kind": "oracle",
                 "sample": "failed: " + res.stderr.strip().splitlines()[-1] if res.stderr else "failed"}
@@ -258,18 +328,18 @@ def run_reference(args):
     prob = make_problem(args)
     n = int(prob.seqlens.max())
     steps, warm = max(1, args.steps), max(0, args.warmup)
-    dt, nb = time_oracle_step(prob, min(n, 2048))
-    per_byte = dt / max(nb, 1)
-    per_step = args.ref_budget_s / (steps + warm)
-    n_tok = n if per_byte * prob.kv_bytes <= per_step else max(
-        32, int(n * per_step / (per_byte * prob.kv_bytes)))
+    cores = os.cpu_count() or 1
+    # Budget per step on all cores; the calibration runs on one.
+    n_tok = _choose_sample(prob, cores * args.ref_budget_s / (steps + warm))
+    par = ParallelOracle(prob, n_tok, cores)
     for _ in range(warm):
-        time_oracle_step(prob, n_tok)
+        par.step()
     total_t, total_b = 0.0, 0
     for _ in range(steps):
-        dt, nb = time_oracle_step(prob, n_tok)
+        dt, nb = par.step()
         total_t += dt
         total_b += nb
+    par.close()
     value = total_b / total_t / 1e9
     frac = "all" if n_tok >= n else f"first {n_tok}"
     line = {
@@ -278,9 +348,9 @@ def run_reference(args):
         "ms_per_step": total_t / steps * 1e3, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded N(0,1))",
         "config": {"workload": prob.name, **prob.describe()},
-        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle",
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": par.cores, "kind": "oracle",
                          "sample": f"each step: fp64 oracle decode of {prob.name} ({frac} tokens "
-                                   f"of every sequence, all heads), 1 thread"},
+                                   f"of every sequence, all heads), {par.cores} processes"},
         "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -337,6 +407,173 @@ def to_device(x, dtype, device):
     return t.to(device)
 
 
+def plan_flags(fd, args, prob):
+    return (fd.FD_PLAN_LITERAL_W if prob.literal_w else 0) | (
+        fd.FD_PLAN_TWO_LAUNCH if args.two_launch else 0) | (fd.FD_PLAN_FFMA if args.ffma else 0) | (
+        fd.FD_PLAN_NO_PDL if args.no_pdl else 0) | (fd.FD_PLAN_WAITS if args.waits else 0) | (
+        fd.FD_PLAN_NO_CLUSTER if args.no_cluster else 0) | (fd.FD_PLAN_CLUSTER if args.cluster else 0) | (
+        fd.FD_PLAN_TCGEN05 if args.tcgen05 else 0)
+
+
+class CaseRun:
+    """One workload on the device: plan, rotated K/V copies, and three CUDA graphs
+    over the same K steps: back to back (the timed region), one event pair around
+    every launch, and every launch alone after an L2 flush."""
+
+    def __init__(self, fd, args, prob, device, stream, steps):
+        import torch
+        self.fd, self.args, self.prob, self.stream, self.K = fd, args, prob, stream, steps
+        props = torch.cuda.get_device_properties(device)
+        self.l2 = int(getattr(props, "L2_cache_size", 126 * 1024 * 1024))
+        kv_bytes = prob.kv_bytes
+        # Rotate K/V copies so consecutive steps never find their K/V in L2.
+        copies = 1 if kv_bytes == 0 else max(1, math.ceil(4 * self.l2 / kv_bytes))
+        self.copies = min(copies, max(1, int(40e9 // max(kv_bytes, 1))))
+        plan_dtype = "f16_e4m3kv" if prob.kv_type == "e4m3" else prob.dtype
+        self.dec = fd.Decoder(prob.Hq, prob.Hkv, prob.d, prob.seqlens, prob.W, plan_dtype,
+                              flags=plan_flags(fd, args, prob), chunks=args.chunks, device=device,
+                              page_size=args.paged)
+        self.q = to_device(prob.q, prob.dtype, device)
+        if args.paged:
+            import workloads
+            kp, vp, table = workloads.to_paged(prob, args.paged)
+            k0, v0 = to_device(kp, prob.dtype, device), to_device(vp, prob.dtype, device)
+            self.bt = torch.from_numpy(table).to(device)
+            self.num_pages = kp.shape[0]
+        else:
+            k0 = to_device(prob.k, prob.dtype, device)
+            v0 = to_device(prob.v, prob.dtype, device)
+        self.k0, self.v0 = k0, v0
+        self.ks = [k0] + [k0.clone() for _ in range(self.copies - 1)]
+        self.vs = [v0] + [v0.clone() for _ in range(self.copies - 1)]
+        self.out = torch.empty_like(self.q)
+        self.lse = torch.empty((prob.B, prob.Hq), dtype=torch.float32, device=device)
+        # An unrelated kernel between isolated decodes: a read of twice the L2 size
+        # (a read leaves clean lines, as a weight-streaming GEMM before attention
+        # would; a write would leave dirty lines for the decode to write back).
+        self.flush = torch.ones(2 * self.l2 // 4, dtype=torch.float32, device=device)
+        self.launches_per_step = 2 if args.two_launch else 1
+        with torch.cuda.stream(stream):
+            for i in range(max(3, args.warmup)):
+                self.step(i)
+        stream.synchronize()
+        self.use_graph = not args.no_graph
+        try:
+            torch.cuda.Event(enable_timing=True, external=True)
+        except TypeError:
+            self.use_graph = False
+        K = self.K
+        self.ev = [(self._event(), self._event()) for _ in range(K)]
+        self.ev_iso = [(self._event(), self._event()) for _ in range(K)]
+        self.ev_all = (self._event(), self._event())
+        self.graphs = {}
+        if self.use_graph:
+            for name, fn in (("a", self._record_a), ("b", self._record_b), ("c", self._record_c)):
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g, stream=stream):
+                    fn()
+                self.graphs[name] = g
+            stream.synchronize()
+
+    def _event(self):
+        import torch
+        # Inside a CUDA graph the events must be "external" to become timing records.
+        if self.use_graph:
+            return torch.cuda.Event(enable_timing=True, external=True)
+        return torch.cuda.Event(enable_timing=True)
+
+    def step(self, i):
+        fd, a = self.fd, self.args
+        c = i % self.copies
+        if a.paged:
+            fd.fd_decode_paged(self.dec.plan, self.q, self.ks[c], self.vs[c], self.num_pages, self.bt,
+                               self.bt.shape[1], self.out, self.lse, self.dec.workspace, self.stream)
+        else:
+            fd.fd_decode(self.dec.plan, self.q, self.ks[c], self.vs[c], self.out, self.lse,
+                         self.dec.workspace, self.stream)
+
+    def _record_a(self):
+        self.ev_all[0].record(self.stream)
+        for i in range(self.K):
+            self.step(i)
+        self.ev_all[1].record(self.stream)
+
+    def _record_b(self):
+        for i in range(self.K):
+            self.ev[i][0].record(self.stream)
+            self.step(i)
+            self.ev[i][1].record(self.stream)
+
+    def _record_c(self):
+        for i in range(self.K):
+            self.flush_sum = self.flush.sum()
+            self.ev_iso[i][0].record(self.stream)
+            self.step(i)
+            self.ev_iso[i][1].record(self.stream)
+
+    def run(self, name):
+        import torch
+        # A graph replays on torch's current stream: make that the decode stream.
+        with torch.cuda.stream(self.stream):
+            if self.use_graph:
+                self.graphs[name].replay()
+            else:
+                {"a": self._record_a, "b": self._record_b, "c": self._record_c}[name]()
+
+    def timed_ms(self):
+        return self.ev_all[0].elapsed_time(self.ev_all[1])
+
+    def per_launch_us(self, which):
+        evs = self.ev if which == "b" else self.ev_iso
+        return [x.elapsed_time(y) * 1e3 for x, y in evs]
+
+
+def stats_us(xs):
+    qs = sorted(xs)
+
+    def pct(p):
+        return qs[min(len(qs) - 1, max(0, int(round(p / 100 * (len(qs) - 1)))))]
+    return {"mean": statistics.fmean(qs), "median": statistics.median(qs), "p10": pct(10),
+            "p90": pct(90), "min": qs[0], "max": qs[-1]}
+
+
+def extra_case(fd, args, name, device, stream, peak):
+    """Step (back to back) and isolated (after an L2 flush) figures of one more case."""
+    import copy
+    import workloads
+    a = copy.copy(args)
+    a.workload = name
+    prob = make_problem(a)
+    run = CaseRun(fd, a, prob, device, stream, max(1, args.extra_steps))
+    run.run("a")
+    stream.synchronize()
+    run.run("a")
+    stream.synchronize()
+    step_us = run.timed_ms() * 1e3 / run.K
+    run.run("b")
+    stream.synchronize()
+    lat = stats_us(run.per_launch_us("b"))
+    run.run("c")
+    stream.synchronize()
+    iso = stats_us(run.per_launch_us("c"))
+    if run.dec.status() != fd.FD_OK:
+        raise RuntimeError(f"device status word reported an error on {name}")
+    kv = prob.kv_bytes
+    out = {"workload": prob.name, "kv_bytes_per_step": kv, "steps": run.K,
+           "ctas": run.dec.info["ctas"], "chunks_per_segment": run.dec.info["chunks"],
+           "step_us": step_us, "step_gbs": kv / (step_us * 1e-6) / 1e9,
+           "frac_step": kv / (step_us * 1e-6) / 1e9 / peak,
+           "latency_us": lat,
+           "frac_latency": kv / (lat["median"] * 1e-6) / 1e9 / peak,
+           "isolated_us": iso,
+           "isolated_gbs": kv / (iso["median"] * 1e-6) / 1e9,
+           "frac_isolated": kv / (iso["median"] * 1e-6) / 1e9 / peak}
+    del run
+    import torch
+    torch.cuda.empty_cache()
+    return out
+
+
 def run_fd(args):
     import torch
 
@@ -351,99 +588,10 @@ def run_fd(args):
     build.build()
     prob = make_problem(args)
     props = torch.cuda.get_device_properties(device)
-    l2 = int(getattr(props, "L2_cache_size", 126 * 1024 * 1024))
-    kv_bytes = prob.kv_bytes
-    # Rotate K/V copies so consecutive steps never find their K/V in L2.
-    copies = 1 if kv_bytes == 0 else max(1, math.ceil(4 * l2 / kv_bytes))
-    copies = min(copies, max(1, int(40e9 // max(kv_bytes, 1))))
-
-    flags = (fd.FD_PLAN_LITERAL_W if prob.literal_w else 0) | (
-        fd.FD_PLAN_TWO_LAUNCH if args.two_launch else 0) | (fd.FD_PLAN_FFMA if args.ffma else 0) | (
-        fd.FD_PLAN_NO_PDL if args.no_pdl else 0) | (fd.FD_PLAN_WAITS if args.waits else 0) | (
-        fd.FD_PLAN_NO_CLUSTER if args.no_cluster else 0) | (fd.FD_PLAN_CLUSTER if args.cluster else 0)
-    plan_dtype = "f16_e4m3kv" if prob.kv_type == "e4m3" else prob.dtype
-    dec = fd.Decoder(prob.Hq, prob.Hkv, prob.d, prob.seqlens, prob.W, plan_dtype, flags=flags,
-                     chunks=args.chunks, device=device, page_size=args.paged)
-    q = to_device(prob.q, prob.dtype, device)
-    if args.paged:
-        import workloads
-        kp, vp, table = workloads.to_paged(prob, args.paged)
-        k0, v0 = to_device(kp, prob.dtype, device), to_device(vp, prob.dtype, device)
-        bt = torch.from_numpy(table).to(device)
-        num_pages = kp.shape[0]
-    else:
-        k0 = to_device(prob.k, prob.dtype, device)
-        v0 = to_device(prob.v, prob.dtype, device)
-    ks = [k0] + [k0.clone() for _ in range(copies - 1)]
-    vs = [v0] + [v0.clone() for _ in range(copies - 1)]
-    out = torch.empty_like(q)
-    lse = torch.empty((prob.B, prob.Hq), dtype=torch.float32, device=device)
     stream = torch.cuda.Stream(device)
-    launches_per_step = 2 if args.two_launch else 1
-
-    def step(i):
-        if args.paged:
-            fd.fd_decode_paged(dec.plan, q, ks[i % copies], vs[i % copies], num_pages, bt,
-                               bt.shape[1], out, lse, dec.workspace, stream)
-        else:
-            fd.fd_decode(dec.plan, q, ks[i % copies], vs[i % copies], out, lse, dec.workspace,
-                         stream)
-
-    K, Wm = max(1, args.steps), max(3, args.warmup)
-    with torch.cuda.stream(stream):
-        for i in range(Wm):
-            step(i)
-    stream.synchronize()
-
-    # Two graphs over exactly K steps: A (the timed region) launches the K decodes
-    # back to back between one event pair; B puts an event pair around every launch
-    # to give the latency of a single decode.  Inside a CUDA graph the events must be
-    # "external" so that they become timing records.
-    use_graph = not args.no_graph
-    try:
-        torch.cuda.Event(enable_timing=True, external=True)
-    except TypeError:
-        use_graph = False
-
-    def timing_event():
-        if use_graph:
-            return torch.cuda.Event(enable_timing=True, external=True)
-        return torch.cuda.Event(enable_timing=True)
-
-    ev = [(timing_event(), timing_event()) for _ in range(K)]
-    ev_all = (timing_event(), timing_event())
-    ev_b = (timing_event(), timing_event())
-
-    def record_a():
-        ev_all[0].record(stream)
-        for i in range(K):
-            step(i)
-        ev_all[1].record(stream)
-
-    def record_b():
-        ev_b[0].record(stream)
-        for i in range(K):
-            ev[i][0].record(stream)
-            step(i)
-            ev[i][1].record(stream)
-        ev_b[1].record(stream)
-
-    graphs = {}
-    if use_graph:
-        for name, fn in (("a", record_a), ("b", record_b)):
-            g = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(g, stream=stream):
-                fn()
-            graphs[name] = g
-        stream.synchronize()
-
-    def run(name):
-        # A graph replays on torch's current stream: make that the decode stream.
-        with torch.cuda.stream(stream):
-            if use_graph:
-                graphs[name].replay()
-            else:
-                (record_a if name == "a" else record_b)()
+    K = max(1, args.steps)
+    run = CaseRun(fd, args, prob, device, stream, K)
+    dec, kv_bytes, copies, l2 = run.dec, prob.kv_bytes, run.copies, run.l2
 
     gpu_id = getattr(props, "uuid", None)
     gpu_id = f"GPU-{gpu_id}" if gpu_id is not None and not str(gpu_id).startswith("GPU-") else str(gpu_id or local)
@@ -451,36 +599,35 @@ def run_fd(args):
     t_soak = time.time()
     # Soak: the same replay, untimed, so clocks settle and the sampler sees the load.
     while time.time() - t_soak < args.soak_s:
-        run("a")
+        run.run("a")
         stream.synchronize()
     barrier(world)
     torch.cuda.synchronize(device)
-    run("a")                      # the timed region: exactly K steps
+    run.run("a")                  # the timed region: exactly K steps
     stream.synchronize()
     torch.cuda.synchronize(device)
     t_end = time.time()
     barrier(world)
-    total_ms = ev_all[0].elapsed_time(ev_all[1])
-    run("b")                      # per-launch latency of the same K steps
+    total_ms = run.timed_ms()
+    run.run("b")                  # per-launch latency of the same K steps
+    stream.synchronize()
+    run.run("c")                  # each decode alone, after an L2 flush
     stream.synchronize()
     sampler.stop()
     clocks = sampler.summary(t_soak, t_end)
     if dec.status() != fd.FD_OK:
         raise RuntimeError("device status word reported an error during the timed region")
 
-    per_launch = [a.elapsed_time(b) * 1e3 for a, b in ev]  # microseconds
     agg = aggregate_throughput(kv_bytes * K / 1e9, total_ms / 1e3, world, device)
     value = agg["throughput"]  # GB/s, whole job
     step_us = total_ms * 1e3 / K
-    mean_us = statistics.fmean(per_launch)
-    qs = sorted(per_launch)
-
-    def pct(p):
-        return qs[min(len(qs) - 1, max(0, int(round(p / 100 * (len(qs) - 1)))))]
+    lat = stats_us(run.per_launch_us("b"))
+    iso = stats_us(run.per_launch_us("c"))
 
     peak, peak_kind = load_peak()
     # Average device time per launch over the timed region (back-to-back launches).
     achieved = kv_bytes / (step_us * 1e-6) / 1e9
+    achieved_iso = kv_bytes / (iso["median"] * 1e-6) / 1e9
 
     # e2e through the public API with pinned host buffers.
     if args.paged:
@@ -488,19 +635,28 @@ def run_fd(args):
     else:
         e2e = e2e_measure(fd, dec, prob, device, args.e2e_steps, stream, kv_resident=False)
         e2e_res = e2e_measure(fd, dec, prob, device, max(args.e2e_steps, 200), stream,
-                              kv_resident=True, dev_kv=(k0, v0))
+                              kv_resident=True, dev_kv=(run.k0, run.v0))
+    info = dec.info
+    del run
+    torch.cuda.empty_cache()
+
+    extras = {}
+    if not args.no_extra and world == 1 and not args.paged:
+        for name in EXTRA_CASES:
+            if name != prob.name:
+                extras[name] = extra_case(fd, args, name, device, stream, peak)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = run_cpu_baseline_subprocess(args)
 
-    info = dec.info
     kernel_label = ("fd_split_kernel+fd_combine_kernel" if args.two_launch else "fd_split_kernel") + (
-        {0: "/ffma", 1: "/mma", 2: "/mma-fp8"}[info["path"]]) + ("/waits" if args.waits else "")
+        {0: "/ffma", 1: "/mma", 2: "/mma-fp8", 3: "/tcgen05"}[info["path"]]) + ("/waits" if args.waits else "")
     if rank == 0:
         line = {
             "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": K,
-            "warmup": Wm, "ms_per_step": agg["elapsed_s"] * 1e3 / K, "higher_is_better": True,
+            "warmup": max(3, args.warmup), "ms_per_step": agg["elapsed_s"] * 1e3 / K,
+            "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": prob.dtype,
             "data": "synthetic (seeded N(0,1) per tensor)",
             "config": {
@@ -517,16 +673,20 @@ def run_fd(args):
                            else ("separate combine kernel" if args.two_launch
                                  else "last arriver (atomic counter)"),
                 "consumer": {0: "FFMA (CUDA cores)", 1: "mma.sync m16n8k16 (tensor cores)",
-                             2: "mma.sync m16n8k16 over E4M3 K/V widened in registers"}[info["path"]],
+                             2: "mma.sync m16n8k16 over E4M3 K/V widened in registers",
+                             3: "tcgen05.mma (accumulators in tensor memory)"}[info["path"]],
                 "l2_policy": f"K/V rotated over {copies} device copies ({copies * kv_bytes / 1e6:.0f} MB"
                              f" >= 4 x L2 {l2 / 1e6:.0f} MB)" if copies > 1 else
-                             f"K/V {kv_bytes / 1e6:.0f} MB per step > 4 x L2 {l2 / 1e6:.0f} MB",
-                "launch": "CUDA graph replay of the K steps" if use_graph else "eager",
+                             f"inputs larger than L2: K/V {kv_bytes / 1e6:.0f} MB per step >= 4 x L2"
+                             f" {l2 / 1e6:.0f} MB",
+                "launch": "CUDA graph replay of the K steps" if run_graph_ok(args) else "eager",
                 "parallelism": f"replicas x{world}",
             },
-            "latency_us": {"mean": mean_us, "median": statistics.median(per_launch),
-                           "p10": pct(10), "p90": pct(90), "min": qs[0], "max": qs[-1],
-                           "what": "one decode, CUDA events around each launch (second replay)"},
+            "latency_us": {**lat, "what": "one decode, CUDA events around each launch, "
+                                         "launched back to back (second replay)"},
+            "isolated_us": {**iso, "what": "one decode alone: a sum over a 2 x L2 buffer (an "
+                                          "unrelated kernel) before each, events around the "
+                                          "decode only (third replay)"},
             "step_us": step_us,
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak,
@@ -534,10 +694,13 @@ def run_fd(args):
                          "traffic_unit": "bytes per launch (ncu dram read + write)",
                          "algorithmic_bytes": kv_bytes,
                          "achieved_from": "KV bytes per launch / (timed-region time / K)",
+                         "achieved_isolated": achieved_iso,
+                         "frac_isolated": achieved_iso / peak,
                          "peak_kind": f"{peak_kind} (hbm_gbs copy, burst)",
                          "kernel": kernel_label},
+            "extra_cases": extras,
             "e2e": e2e, "e2e_resident_kv": e2e_res,
-            "gpu_launches": K * launches_per_step,
+            "gpu_launches": K * (2 if args.two_launch else 1),
             "kv_tokens_per_s": prob.n_tokens * K * world / agg["elapsed_s"],
             "clocks": clocks, "cpu_baseline": cpu,
             "gpu": props.name,
@@ -547,6 +710,17 @@ def run_fd(args):
         import torch.distributed as dist
         dist.destroy_process_group()
     return 0
+
+
+def run_graph_ok(args):
+    import torch
+    if args.no_graph:
+        return False
+    try:
+        torch.cuda.Event(enable_timing=True, external=True)
+    except TypeError:
+        return False
+    return True
 
 
 def e2e_measure(fd, dec, prob, device, steps, stream, kv_resident, dev_kv=None):

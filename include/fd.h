@@ -87,6 +87,22 @@ enum fd_status {
  * FD_PLAN_NO_CLUSTER never merges; FD_PLAN_CLUSTER always does (both: invalid). */
 #define FD_PLAN_NO_CLUSTER 0x80u
 #define FD_PLAN_CLUSTER 0x100u
+/* Test hook for the pipeline's bounded waits: the producer of partial slot 0 of
+ * (sequence 0, KV head 0) never loads that partial's second tile, so its
+ * consumers give up after ~1 s.  That CTA then publishes an empty partial and
+ * still arrives, so every arrival counter returns to zero; the status word
+ * reports FD_ERR_TIMEOUT and the out/lse of (sequence 0, KV head 0) lack that
+ * partial.  Needs L_0 large enough for slot 0 to span two tiles (128 tokens with
+ * FD_PLAN_TCGEN05, 64 on the other tensor-core paths, 32 on CUDA cores); otherwise
+ * nothing is skipped.  Not with
+ * FD_PLAN_TEST_DROP_FLAG. */
+#define FD_PLAN_TEST_SKIP_TILE 0x200u
+/* Fifth-generation tensor cores (tcgen05.mma with accumulators in tensor memory)
+ * for the scores and P.V: 128-token tiles, d = 128, G in {4, 8, 16}, fp16 or bf16
+ * (FD_ERR_UNSUPPORTED otherwise).  S^T = K Q^T runs with the tokens on M and the
+ * heads, padded to 16, on N, straight from the TMA-swizzled K tile; P^T is staged
+ * in shared memory; O^T = V^T P^T accumulates in tensor memory. */
+#define FD_PLAN_TCGEN05 0x400u
 
 /* Compiled limits. */
 #define FD_MAX_BATCH 256       /* sequences per plan */
@@ -138,7 +154,7 @@ int fd_plan_destroy(fd_plan_t plan);
 
 /* Bytes of device workspace fd_decode needs for this plan: a status word, one
  * uint32 arrival counter per (sequence, KV head), one uint32 ready flag per CTA,
- * and the fp32 partial records [P][d + 4] (O, m, l; P = Hq * sum_b W_b * C).
+ * and the fp32 partial records [P][d + 4] (O, m, l, l~; P = Hq * sum_b W_b * C).
  * 0 for a NULL plan. */
 size_t fd_workspace_bytes(fd_plan_t plan);
 
@@ -212,17 +228,31 @@ int fd_decode_paged(fd_plan_t plan, const void* q, const void* k_pages, const vo
  *
  * Returns FD_ERR_UNSUPPORTED when fd_workspace_bytes(plan) exceeds
  * FD_NOALLOC_SCRATCH_BYTES (the plan needs more scratch than the array holds).
- * The first call on each device looks up the array's device address
- * (cudaGetSymbolAddress, with that device current); make that first call
- * before any stream capture.  Each call clears the array's counters and status
- * word on `stream` before its launch; the array keeps the last call's
- * partials.  Every call in the process shares the one array per device, so
- * fd_decode_noalloc calls that overlap on the GPU (other streams, other
- * threads) race and must be serialised by the caller.  FD_PLAN_DEBUG checks are
- * not performed here.  Asynchronous, like fd_decode.
+ * The device address of the array is looked up (cudaGetSymbolAddress, with that
+ * device current) by the first call in each CUDA context of a device, and again
+ * after the context changes (e.g. after cudaDeviceReset); make that first call
+ * before any stream capture.  Each call clears the array's status word,
+ * counters and flags on `stream` before its launch; the array keeps the last
+ * call's partials.  Every call in the process shares the one array per device,
+ * so fd_decode_noalloc calls that overlap on the GPU (other streams, other
+ * threads) race and must be serialised by the caller.  A bounded in-kernel wait
+ * that gives up is reported by fd_noalloc_status (read it before the next call,
+ * which clears it); with FD_PLAN_DEBUG this call synchronises and returns that
+ * status itself.  Asynchronous otherwise, like fd_decode.
  */
 int fd_decode_noalloc(fd_plan_t plan, const void* q, const void* k, const void* v, void* out,
                       float* lse, cudaStream_t stream);
+
+/*
+ * fd_noalloc_status -- the device status of the last fd_decode_noalloc call on the
+ * current device (the paper has no counterpart; it serves fd_decode_noalloc).
+ * Synchronises `stream`, reads the static array's status word and the plan's
+ * counters and ready flags, then clears the status word.  *status is FD_OK,
+ * FD_ERR_TIMEOUT (a bounded wait gave up) or FD_ERR_STATE (a counter overflowed,
+ * or counters or flags are not back at zero).  Allocates nothing.
+ * FD_ERR_UNSUPPORTED for a plan whose scratch exceeds the array.
+ */
+int fd_noalloc_status(fd_plan_t plan, cudaStream_t stream, int32_t* status);
 
 /* Synchronise `stream` and read the device status word (0 = no error; else a
  * negative fd_status) into *status.  Then clear the word. */
@@ -245,7 +275,7 @@ typedef struct fd_plan_info {
   uint64_t workspace_bytes;
   uint64_t kv_bytes;       /* bytes of K and V one decode reads */
   int32_t path;            /* 0: CUDA-core (FFMA) consumers, 1: tensor-core (mma.sync),
-                              2: tensor-core over an E4M3 cache */
+                              2: tensor-core over an E4M3 cache, 3: tcgen05 tensor cores */
   int32_t records_per_segment; /* partial records per segment: 1 (chunks merged in a
                                   cluster) or chunks */
 } fd_plan_info;

@@ -30,12 +30,15 @@ from ._binding import (  # noqa: F401
     FD_PLAN_NO_CLUSTER,
     FD_PLAN_NO_PDL,
     FD_PLAN_TEST_DROP_FLAG,
+    FD_PLAN_TEST_SKIP_TILE,
+    FD_PLAN_TCGEN05,
     FD_PLAN_WAITS,
     FD_PLAN_TWO_LAUNCH,
     FdError,
     Plan,
     fd_decode,
     fd_decode_noalloc,
+    fd_noalloc_status,
     fd_decode_paged,
     fd_plan,
     fd_plan_paged,

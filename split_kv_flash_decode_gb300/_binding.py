@@ -34,6 +34,8 @@ FD_PLAN_WAITS = 0x20
 FD_PLAN_TEST_DROP_FLAG = 0x40
 FD_PLAN_NO_CLUSTER = 0x80
 FD_PLAN_CLUSTER = 0x100
+FD_PLAN_TEST_SKIP_TILE = 0x200
+FD_PLAN_TCGEN05 = 0x400
 FD_MAX_BATCH = 256
 FD_MAX_PARTIALS = 1024
 
@@ -43,7 +45,7 @@ DTYPES = {"f16": FD_F16, "bf16": FD_BF16, "f16_e4m3kv": FD_F16_E4M3KV}
 EXPORTED = (
     "fd_plan", "fd_plan_destroy", "fd_workspace_bytes", "fd_workspace_init", "fd_decode",
     "fd_workspace_status", "fd_strerror", "fd_plan_get_info", "fd_plan_get_range", "fd_version",
-    "fd_decode_noalloc", "fd_plan_paged", "fd_decode_paged",
+    "fd_decode_noalloc", "fd_noalloc_status", "fd_plan_paged", "fd_decode_paged",
 )
 FD_NOALLOC_SCRATCH_BYTES = 32 << 20
 
@@ -114,6 +116,8 @@ def lib() -> ctypes.CDLL:
             L.fd_decode_paged.restype = ctypes.c_int
             L.fd_decode_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp]
             L.fd_decode_noalloc.restype = ctypes.c_int
+            L.fd_noalloc_status.argtypes = [vp, vp, ctypes.POINTER(i32)]
+            L.fd_noalloc_status.restype = ctypes.c_int
             L.fd_version.argtypes = []
             L.fd_version.restype = ctypes.c_int
             _lib = L
@@ -245,6 +249,14 @@ def fd_decode_noalloc(plan: Plan, q, k, v, out, lse, stream=None) -> None:
     (for callers that cannot allocate device memory; see include/fd.h)."""
     _check(lib().fd_decode_noalloc(plan.handle, _ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse),
                                    _stream(stream)), "fd_decode_noalloc")
+
+
+def fd_noalloc_status(plan: Plan, stream=None) -> int:
+    """fd_noalloc_status: status of the last fd_decode_noalloc call (synchronises)."""
+    st = ctypes.c_int32(0)
+    _check(lib().fd_noalloc_status(plan.handle, _stream(stream), ctypes.byref(st)),
+           "fd_noalloc_status")
+    return st.value
 
 
 def fd_workspace_status(plan: Plan, workspace, stream=None) -> int:

@@ -22,7 +22,6 @@ constexpr size_t kAlign = 256;
 // 256-token chunks: the CUDA-core consumers of a CTA walk its tokens serially.
 constexpr int kMinChunkTokens = 128;
 constexpr int kMaxCluster = 8;        // portable thread-block cluster size
-constexpr int kCtasPerSm = 2;         // resident CTAs per SM (launch bounds + shared memory)
 
 size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 
@@ -75,9 +74,7 @@ int fd::encode_kv_map(CUtensorMap* map, const void* base, int64_t rows, int box_
 namespace {
 
 cudaError_t launch(const fd_plan_s* pl, const fd::Params& p, int mode, int grid, cudaStream_t s) {
-  const bool pdl = !(pl->flags & FD_PLAN_NO_PDL);
-  return pl->dtype == FD_BF16 ? fd::launch_bf16(p, pl->d, pl->G, pl->path, mode, pdl, grid, s)
-                              : fd::launch_f16(p, pl->d, pl->G, pl->path, mode, pdl, grid, s);
+  return fd::launch_plan(pl, p, mode, grid, s);
 }
 
 }  // namespace
@@ -116,12 +113,13 @@ int plan_impl(int B, int Hq, int Hkv, int d, const int32_t* seqlens, const int32
   if (dtype != FD_F16 && dtype != FD_BF16 && dtype != FD_F16_E4M3KV) return FD_ERR_INVALID;
   if (flags & ~(FD_PLAN_LITERAL_W | FD_PLAN_DEBUG | FD_PLAN_TWO_LAUNCH | FD_PLAN_FFMA |
                 FD_PLAN_NO_PDL | FD_PLAN_WAITS | FD_PLAN_TEST_DROP_FLAG |
-                FD_PLAN_NO_CLUSTER | FD_PLAN_CLUSTER))
+                FD_PLAN_NO_CLUSTER | FD_PLAN_CLUSTER | FD_PLAN_TEST_SKIP_TILE | FD_PLAN_TCGEN05))
     return FD_ERR_INVALID;
   if ((flags & FD_PLAN_CLUSTER) && (flags & (FD_PLAN_NO_CLUSTER | FD_PLAN_WAITS)))
     return FD_ERR_INVALID;
   if ((flags & FD_PLAN_WAITS) && (flags & FD_PLAN_TWO_LAUNCH)) return FD_ERR_INVALID;
   if ((flags & FD_PLAN_TEST_DROP_FLAG) && !(flags & FD_PLAN_WAITS)) return FD_ERR_INVALID;
+  if ((flags & FD_PLAN_TEST_DROP_FLAG) && (flags & FD_PLAN_TEST_SKIP_TILE)) return FD_ERR_INVALID;
   const int G = Hq / Hkv;
   if (page_size != 0 && (page_size < 16 || page_size > 256 || (page_size & (page_size - 1))))
     return FD_ERR_UNSUPPORTED;
@@ -131,8 +129,12 @@ int plan_impl(int B, int Hq, int Hkv, int d, const int32_t* seqlens, const int32
   if (G == 16 && (flags & FD_PLAN_FFMA)) return FD_ERR_UNSUPPORTED;  // tensor cores only
   if (dtype == FD_F16_E4M3KV && (d != 128 || G < 4 || (flags & FD_PLAN_FFMA)))
     return FD_ERR_UNSUPPORTED;
+  if ((flags & FD_PLAN_TCGEN05) &&
+      (dtype == FD_F16_E4M3KV || d != 128 || G < 4 || (flags & FD_PLAN_FFMA)))
+    return FD_ERR_UNSUPPORTED;
   // Tensor cores whenever the GQA group covers at least half of the mma N = 8 tile.
   const int path = dtype == FD_F16_E4M3KV                 ? fd::kPathMmaKv8
+                   : (flags & FD_PLAN_TCGEN05)            ? fd::kPathUmma
                    : (G >= 4 && !(flags & FD_PLAN_FFMA)) ? fd::kPathMma
                                                          : fd::kPathFfma;
 
@@ -164,7 +166,7 @@ int plan_impl(int B, int Hq, int Hkv, int d, const int32_t* seqlens, const int32
   } else {
     // Fill the resident CTA slots in one wave without cutting segments too short.
     const int64_t units = (int64_t)Hkv * sum_w;
-    const int64_t slots = (int64_t)num_sms * kCtasPerSm;
+    const int64_t slots = (int64_t)num_sms * fd::ctas_per_sm_for(path);
     int64_t c = std::max<int64_t>(1, slots / units);
     const int64_t avg_seg = sum_w > 0 ? n_tokens / sum_w : 0;
     c = std::min<int64_t>(c, std::max<int64_t>(1, avg_seg / kMinChunkTokens));
@@ -174,9 +176,9 @@ int plan_impl(int B, int Hq, int Hkv, int d, const int32_t* seqlens, const int32
   {
     // The combine's shared-memory scratch must fit in the ring it reuses.
     const int64_t wt = (int64_t)max_w * C;
-    int64_t need = (G * wt + 2 * G) * 4 + 16;                       // coefficients
+    int64_t need = (G * wt + 3 * G) * 4 + 16;                       // coefficients
     if (flags & FD_PLAN_WAITS)                                      // running state + lists
-      need = std::max<int64_t>(need, (int64_t)(G * d + 3 * G + G * wt) * 4 + (2 * wt + 2) * 4);
+      need = std::max<int64_t>(need, (int64_t)(G * d + 4 * G + G * wt) * 4 + (2 * wt + 2) * 4);
     if (need > (int64_t)fd::ring_bytes_for(path, d)) return FD_ERR_UNSUPPORTED;
   }
   const int64_t ctas = (int64_t)Hkv * sum_w * C;
@@ -200,10 +202,13 @@ int plan_impl(int B, int Hq, int Hkv, int d, const int32_t* seqlens, const int32
   fd::Params& p = pl->params;
   std::memset(&p, 0, sizeof(p));
   p.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)d));
+  p.test_hook = (flags & FD_PLAN_TEST_DROP_FLAG)   ? fd::kHookDropFlag
+                : (flags & FD_PLAN_TEST_SKIP_TILE) ? fd::kHookSkipTile
+                                                   : fd::kHookNone;
   p.B = B; p.Hq = Hq; p.Hkv = Hkv; p.C = C;
   // Only the first wave can start before the previous kernel ends; later CTAs
   // would only queue prefetches ahead of their own loads.
-  p.prefetch_ctas = (int32_t)std::min<int64_t>(ctas, (int64_t)num_sms * kCtasPerSm);
+  p.prefetch_ctas = (int32_t)std::min<int64_t>(ctas, (int64_t)num_sms * fd::ctas_per_sm_for(path));
   // When the chunk records of one (sequence, KV head) would need several passes
   // through the combine's shared memory (at least 2; 3 over an FP8 cache, whose
   // shorter CTAs gain less than the cluster barriers cost), segments cut into 2..8
@@ -348,7 +353,6 @@ int decode_impl(fd_plan_t pl, const void* q, const void* k, const void* v, int64
   p.counters = reinterpret_cast<uint32_t*>(ws + pl->off_counters);
   p.part = reinterpret_cast<float*>(ws + pl->off_part);
   p.flags = reinterpret_cast<uint32_t*>(ws + pl->off_flags);
-  p.drop_flag = (pl->flags & FD_PLAN_TEST_DROP_FLAG) ? 1 : 0;
 
   const bool debug = (pl->flags & FD_PLAN_DEBUG) != 0;
   if (debug) {

@@ -27,46 +27,80 @@ constexpr int kThreads = (kConsumerWarps + 1) * 32;
 // KV8: the MMA path over an FP8 (E4M3) cache, d = 128 only.  K/V land in the ring
 // as 128-byte swizzled rows of bytes; every thread loads its mma fragments from
 // there directly and widens them to f16 with integer ops.
+// UMMA: fifth-generation tensor cores (tcgen05.mma, accumulators in tensor memory),
+// d = 128 and G in {4, 8, 16}: S^T = K Q^T with 128 tokens on M and the heads
+// (padded to 16) on N, read straight from the TMA-swizzled K tile; P^T goes through
+// shared memory; O^T = V^T P^T accumulates in tensor memory with the 128 head
+// dimensions on M.  K and V tiles of 128 tokens occupy separate ring slots.
 constexpr int kPathFfma = 0;
 constexpr int kPathMma = 1;
 constexpr int kPathMmaKv8 = 2;
+constexpr int kPathUmma = 3;
 
 FD_HD constexpr bool is_mma(int path) { return path != kPathFfma; }
 // Bytes per stored K/V element.
 FD_HD constexpr int kv_elem_bytes(int path) { return path == kPathMmaKv8 ? 1 : 2; }
 // Tokens per pipeline stage.
-FD_HD constexpr int tile_for(int path) { return is_mma(path) ? 64 : 32; }
+FD_HD constexpr int tile_for(int path) { return path == kPathUmma ? 128 : is_mma(path) ? 64 : 32; }
 // Columns (elements) of one TMA box row: 128-byte swizzled rows on the MMA paths.
 FD_HD constexpr int box_cols_for(int path, int d) {
-  return path == kPathMma ? 64 : path == kPathMmaKv8 ? 128 : d;
+  return (path == kPathMma || path == kPathUmma) ? 64 : path == kPathMmaKv8 ? 128 : d;
 }
-// K/V tiles per CTA that the split kernel prefetches into L2 before it waits for
-// the previous kernel in the stream (4 measured best for fp16 and fp8 caches at
-// 32K and 128K tokens; 2 and 8 were slower).
-constexpr int kL2PrefetchTiles = 4;
+// Ring slots per tile: the tcgen05 path keeps K and V of a tile in separate slots
+// (the K slot is released when S^T is computed, the V slot after P.V).
+FD_HD constexpr int loads_per_tile(int path) { return path == kPathUmma ? 2 : 1; }
+// K/V tokens per CTA that the split kernel prefetches into L2 before it waits for
+// the previous kernel in the stream (256 = 4 tiles of 64 measured best for fp16 and
+// fp8 caches at 32K and 128K tokens; 2 and 8 tiles were slower).
+constexpr int kL2PrefetchTokens = 256;
 // The K/V ring, 96 KB on every path: slots of one tile of K rows followed by the
 // tile of V rows of one KV head.  (At d = 64 the ring used to be 64 KB; 96 KB is
 // 14% faster at 32K tokens.  A 112 KB ring, the most two CTAs per SM can hold,
 // was slower on every path, and so were separate K and V slots with their own
 // barriers on the multi-wave and FP8 cases.)
 constexpr int kRingBytes = 96 * 1024;
-FD_HD constexpr int slot_bytes_for(int path, int d) { return 2 * tile_for(path) * d * kv_elem_bytes(path); }
-FD_HD constexpr int ring_slots_for(int path, int d) { return kRingBytes / slot_bytes_for(path, d); }
+// A kernel that uses tcgen05 instructions is resident one CTA per SM (the occupancy
+// calculator reports 1 for any such kernel, whatever its shared memory), so that
+// path gets the bytes in flight of two CTAs of the other paths: a 192 KB ring.
+FD_HD constexpr int ctas_per_sm_for(int path) { return path == kPathUmma ? 1 : 2; }
+FD_HD constexpr int ring_target_bytes(int path) { return path == kPathUmma ? 2 * kRingBytes : kRingBytes; }
+FD_HD constexpr int slot_bytes_for(int path, int d) {
+  return (2 / loads_per_tile(path)) * tile_for(path) * d * kv_elem_bytes(path);
+}
+FD_HD constexpr int ring_slots_for(int path, int d) { return ring_target_bytes(path) / slot_bytes_for(path, d); }
 // Bytes of the K/V ring (also the scratch the combine reuses).
 FD_HD constexpr size_t ring_bytes_for(int path, int d) {
   return (size_t)ring_slots_for(path, d) * slot_bytes_for(path, d);
 }
 // Bytes after the ring: 2 mbarriers per slot, the combine's mbarrier, two flags,
-// and up to 1 KB of slack for aligning the ring to 1024 bytes.
+// the tcgen05 path's two mbarriers and tensor-memory address, and up to 1 KB of
+// slack for aligning the ring to 1024 bytes.
 constexpr int kRingMetaBytes = 2048;
-// Dynamic shared memory of one CTA: the ring and its metadata.
-FD_HD constexpr size_t smem_bytes_for(int path, int d) { return ring_bytes_for(path, d) + kRingMetaBytes; }
-// Floats per partial record: O[0..d), m, l and two pad words (16-byte records).
+// The tcgen05 path's operands outside the ring: Q (16 x 128, 4 KB), P^T (128 x 16,
+// 4 KB) and 1 KB of reduction scratch.
+FD_HD constexpr int extra_bytes_for(int path) { return path == kPathUmma ? 9216 : 0; }
+// Dynamic shared memory of one CTA: the ring, the extra operands and the metadata.
+FD_HD constexpr size_t smem_bytes_for(int path, int d) {
+  return ring_bytes_for(path, d) + extra_bytes_for(path) + kRingMetaBytes;
+}
+// Floats per partial record: O[0..d), m, l, l~ and a pad word (16-byte records).
+// l sums the fp32 softmax weights (it gives lse); l~ sums the weights as rounded
+// for the P.V product (it normalises out, so out is an exact convex combination
+// of V rows under those weights).  Without rounding (CUDA-core path) l~ = l.
 FD_HD constexpr int record_floats(int d) { return d + 4; }
 
 // Status word values written by the kernels (the host maps them to fd_status).
 constexpr uint32_t kStatusTimeout = 1u;
 constexpr uint32_t kStatusCounter = 2u;
+
+// Test hooks (chosen by plan flags) that make one bounded wait run out on purpose.
+// kHookDropFlag: partial slot 1 of (sequence 0, KV head 0) never sets its ready flag
+// (fine-grained-waits variant).  kHookSkipTile: the producer of partial slot 0 of
+// (sequence 0, KV head 0) never issues the loads of its second tile, so that CTA's
+// consumers give up waiting for it.
+constexpr int32_t kHookNone = 0;
+constexpr int32_t kHookDropFlag = 1;
+constexpr int32_t kHookSkipTile = 2;
 
 // Kernel parameters (passed by value as a __grid_constant__ struct; < 4 KB).
 struct Params {
@@ -75,11 +109,11 @@ struct Params {
   const void* q;     // [B, Hq, d]
   void* out;         // [B, Hq, d]
   float* lse;        // [B, Hq] or nullptr
-  float* part;       // [P, d + 4] records: O[0..d), m, l, 0, 0 (m in the log2 domain)
+  float* part;       // [P, d + 4] records: O[0..d), m, l, l~, 0 (m in the log2 domain)
   uint32_t* counters;  // [B * Hkv]
   uint32_t* flags;     // [CTAs] per-partial ready flags (fine-grained-waits variant)
   uint32_t* status;    // 1 word
-  int32_t drop_flag;   // test hook: partial slot 1 of (b=0, kvh=0) never sets its flag
+  int32_t test_hook;   // kHookNone, or one of the test hooks below
   // Paged KV cache: K/V rows of sequence b, token t live at pool row
   // block_table[b * bt_stride + (t >> page_shift)] * page_size + (t & (page_size - 1)).
   const int32_t* block_table;  // nullptr: contiguous [N, Hkv, d] layout
@@ -129,5 +163,9 @@ cudaError_t launch_f16(const Params& p, int d, int G, int path, int mode, bool p
                        cudaStream_t s);
 cudaError_t launch_bf16(const Params& p, int d, int G, int path, int mode, bool pdl, int grid,
                         cudaStream_t s);
+cudaError_t launch_umma_f16(const Params& p, int d, int G, int mode, bool pdl, int grid,
+                            cudaStream_t s);
+cudaError_t launch_umma_bf16(const Params& p, int d, int G, int mode, bool pdl, int grid,
+                             cudaStream_t s);
 
 }  // namespace fd

@@ -45,6 +45,7 @@
 #include <type_traits>
 
 #include "fd_common.h"
+#include "fd_tcgen05.cuh"
 
 namespace fd {
 namespace dev {
@@ -52,6 +53,9 @@ namespace dev {
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale when the max grows by > 2^8
 constexpr float kLn2 = 0.693147180559945309417f;
 constexpr uint64_t kWaitLimitNs = 1000000000ull;  // bounded waits give up after ~1 s
+constexpr uint32_t kTmemCols = 64;   // tensor-memory columns per CTA (tcgen05 path)
+constexpr uint32_t kColS = 0;        // S^T [128 tokens][16 heads]
+constexpr uint32_t kColO = 32;       // O^T [128 dims][16 heads]
 
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -329,12 +333,22 @@ __device__ __forceinline__ Work decode_work(const Params& p, int cta, bool seg) 
   return w;
 }
 
-// Merge two (max, sum) pairs of the log2-domain softmax (-inf max = empty).
-__device__ __forceinline__ void ml_merge(float& M, float& lam, float m2, float l2) {
+// Merge two (max, sum, rounded-weight sum) triples of the log2-domain softmax
+// (-inf max = empty).
+__device__ __forceinline__ void ml_merge(float& M, float& lam, float& lamr, float m2, float l2,
+                                         float lr2) {
   if (m2 == -INFINITY) return;
-  if (M == -INFINITY) { M = m2; lam = l2; return; }
-  if (m2 > M) { lam = fmaf(lam, ex2(M - m2), l2); M = m2; }
-  else lam = fmaf(l2, ex2(m2 - M), lam);
+  if (M == -INFINITY) { M = m2; lam = l2; lamr = lr2; return; }
+  if (m2 > M) {
+    const float c = ex2(M - m2);
+    lam = fmaf(lam, c, l2);
+    lamr = fmaf(lamr, c, lr2);
+    M = m2;
+  } else {
+    const float c = ex2(m2 - M);
+    lam = fmaf(l2, c, lam);
+    lamr = fmaf(lr2, c, lamr);
+  }
 }
 
 // 1-D bulk copy global -> shared memory, completing on mbarrier `bar`.
@@ -405,9 +419,11 @@ __device__ __forceinline__ float warp_sum(float x) {
 // [ng][wtot][D + 4].  One warp per head: M is the max of the partial maxima,
 // Lambda = sum_w exp2(m_w - M) l_w, O = sum_w exp2(m_w - M) O_w; lane l owns the
 // D/32 output dimensions starting at (D/32) l, and receives each coefficient by
-// shuffle from the lane that computed it.  The order of every sum is fixed
-// (partial index order for O, a fixed shuffle tree for Lambda), so the result
-// does not depend on the order in which the partials arrived.
+// shuffle from the lane that computed it.  out = O / Lambda~, where Lambda~ sums
+// the records' rounded-weight sums the same way (the weights P.V multiplied);
+// lse = M + log Lambda.  The order of every sum is fixed (partial index order for
+// O, a fixed shuffle tree for the Lambdas), so the result does not depend on the
+// order in which the partials arrived.
 template <typename T, int D, int G>
 __device__ __forceinline__ void combine_from_smem(const Params& p, int b, int kvh, int wtot,
                                                   int g0, int ng, const float* rec) {
@@ -423,7 +439,7 @@ __device__ __forceinline__ void combine_from_smem(const Params& p, int b, int kv
     float M = -INFINITY;
     for (int w = lane; w < wtot; w += 32) M = fmaxf(M, rg[(size_t)w * RS + D]);
     M = warp_max(M);
-    float lam = 0.f;
+    float lam = 0.f, lamr = 0.f;
     float acc[V];
 #pragma unroll
     for (int j = 0; j < V; ++j) acc[j] = 0.f;
@@ -431,9 +447,10 @@ __device__ __forceinline__ void combine_from_smem(const Params& p, int b, int kv
       const int n = min(32, wtot - w0);
       float cl = 0.f;
       if (lane < n && M != -INFINITY) {
-        const float2 ml = *reinterpret_cast<const float2*>(rg + (size_t)(w0 + lane) * RS + D);
+        const float4 ml = *reinterpret_cast<const float4*>(rg + (size_t)(w0 + lane) * RS + D);
         cl = ex2(ml.x - M);  // exp2(-inf) = 0 for an empty partial
         lam = fmaf(cl, ml.y, lam);
+        lamr = fmaf(cl, ml.z, lamr);
       }
       const float* base = rg + (size_t)w0 * RS + V * lane;
       int i = 0;
@@ -462,16 +479,17 @@ __device__ __forceinline__ void combine_from_smem(const Params& p, int b, int kv
       }
     }
     lam = warp_sum(lam);
+    lamr = warp_sum(lamr);
     T* dst = out + ((int64_t)b * p.Hq + kvh * G + g0 + g) * D + V * lane;
 #pragma unroll
-    for (int j = 0; j < V; ++j) dst[j] = Elem<T>::from_f(lam > 0.f ? acc[j] / lam : 0.f);
+    for (int j = 0; j < V; ++j) dst[j] = Elem<T>::from_f(lamr > 0.f ? acc[j] / lamr : 0.f);
     if (lane == 0 && p.lse != nullptr)
       p.lse[(int64_t)b * p.Hq + kvh * G + g0 + g] = lam > 0.f ? (M + log2f(lam)) * kLn2 : -INFINITY;
   }
 }
 
 // Same combine reading the records straight from L2 (for partial counts whose
-// records do not fit in shared memory); `coef` holds G * wtot + 2 * G floats.
+// records do not fit in shared memory); `coef` holds G * wtot + 3 * G floats.
 template <typename T, int D, int G>
 __device__ __forceinline__ void combine_from_global(const Params& p, int b, int kvh, int wtot,
                                                     int64_t pbase, float* coef) {
@@ -481,23 +499,25 @@ __device__ __forceinline__ void combine_from_global(const Params& p, int b, int 
   constexpr int kWarps = kThreads / 32;
   for (int g = warp; g < G; g += kWarps) {
     const float* row = p.part + (pbase + (int64_t)(kvh * G + g) * wtot) * RS + D;
-    float M = -INFINITY, lam = 0.f;
+    float M = -INFINITY, lam = 0.f, lamr = 0.f;
     for (int w = lane; w < wtot; w += 32) {
-      const float2 ml = __ldcg(reinterpret_cast<const float2*>(row + (size_t)w * RS));
+      const float4 ml = __ldcg(reinterpret_cast<const float4*>(row + (size_t)w * RS));
       coef[g * wtot + w] = ml.x;
-      ml_merge(M, lam, ml.x, ml.y);
+      ml_merge(M, lam, lamr, ml.x, ml.y, ml.z);
     }
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) {
       const float m2 = __shfl_xor_sync(0xffffffffu, M, off);
       const float l2 = __shfl_xor_sync(0xffffffffu, lam, off);
-      ml_merge(M, lam, m2, l2);
+      const float lr2 = __shfl_xor_sync(0xffffffffu, lamr, off);
+      ml_merge(M, lam, lamr, m2, l2, lr2);
     }
     for (int w = lane; w < wtot; w += 32)
       coef[g * wtot + w] = (M == -INFINITY) ? 0.f : ex2(coef[g * wtot + w] - M);
     if (lane == 0) {
-      ML[2 * g] = M;
-      ML[2 * g + 1] = lam;
+      ML[3 * g] = M;
+      ML[3 * g + 1] = lam;
+      ML[3 * g + 2] = lamr;
     }
   }
   __syncthreads();
@@ -530,10 +550,10 @@ __device__ __forceinline__ void combine_from_global(const Params& p, int b, int 
       a.z = fmaf(c, x.z, a.z);
       a.w = fmaf(c, x.w, a.w);
     }
-    store_out4<T>(out + ((int64_t)b * p.Hq + kvh * G + g) * D + 4 * c4, a, ML[2 * g + 1]);
+    store_out4<T>(out + ((int64_t)b * p.Hq + kvh * G + g) * D + 4 * c4, a, ML[3 * g + 2]);
   }
   if (tid < G && p.lse != nullptr) {
-    const float M = ML[2 * tid], lam = ML[2 * tid + 1];
+    const float M = ML[3 * tid], lam = ML[3 * tid + 1];
     p.lse[(int64_t)b * p.Hq + kvh * G + tid] = lam > 0.f ? (M + log2f(lam)) * kLn2 : -INFINITY;
   }
 }
@@ -577,7 +597,7 @@ __device__ __forceinline__ void combine_partials(const Params& p, int b, int kvh
 // batch that has arrived into a running (M, Lambda, O), in arrival order.  The
 // whole grid is co-resident (cooperative launch), so every producer can finish;
 // the poll is still bounded and reports a timeout through the status word.
-// `sm` provides G * (D + 2) + 2 * wtot + G * wtot + 4 floats of scratch.
+// `sm` provides G * (D + 4) + 2 * wtot + G * wtot + 2 floats of scratch.
 template <typename T, int D, int G>
 __device__ __forceinline__ void combine_as_arrived(const Params& p, const Work& wk, float* sm) {
   constexpr int RS = record_floats(D);
@@ -585,7 +605,8 @@ __device__ __forceinline__ void combine_as_arrived(const Params& p, const Work& 
   float* run_O = sm;                       // [G][D]
   float* run_M = run_O + G * D;            // [G]
   float* run_L = run_M + G;                // [G]
-  float* coef = run_L + G;                 // [G][wtot] (this batch)
+  float* run_Lr = run_L + G;               // [G] rounded-weight sums
+  float* coef = run_Lr + G;                // [G][wtot] (this batch)
   float* scl = coef + G * wtot;            // [G]
   int* ready = reinterpret_cast<int*>(scl + G);  // [wtot] slots of this batch
   int* done = ready + wtot;                // [wtot]
@@ -594,7 +615,7 @@ __device__ __forceinline__ void combine_as_arrived(const Params& p, const Work& 
   constexpr int kWarps = kThreads / 32;
   const int fbase = flag_index(p, wk.b, wk.kvh, 0);  // flag of slot w: fbase + w
   for (int i = tid; i < G * D; i += kThreads) run_O[i] = 0.f;
-  for (int g = tid; g < G; g += kThreads) { run_M[g] = -INFINITY; run_L[g] = 0.f; }
+  for (int g = tid; g < G; g += kThreads) { run_M[g] = -INFINITY; run_L[g] = 0.f; run_Lr[g] = 0.f; }
   for (int w = tid; w < wtot; w += kThreads) done[w] = 0;
   if (tid == 0) ctl[1] = 0;
   __syncthreads();
@@ -629,19 +650,21 @@ __device__ __forceinline__ void combine_as_arrived(const Params& p, const Work& 
       for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
       const float Mold = run_M[g];
       const float Mnew = fmaxf(Mold, mx);
-      float lam = 0.f;
+      float lam = 0.f, lamr = 0.f;
       for (int i = lane; i < n; i += 32) {
-        const float2 ml = __ldcg(reinterpret_cast<const float2*>(p.part + (row + ready[i]) * RS + D));
+        const float4 ml = __ldcg(reinterpret_cast<const float4*>(p.part + (row + ready[i]) * RS + D));
         const float c = (ml.x == -INFINITY) ? 0.f : ex2(ml.x - Mnew);
         coef[g * wtot + i] = c;
         lam = fmaf(c, ml.y, lam);
+        lamr = fmaf(c, ml.z, lamr);
       }
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) lam += __shfl_xor_sync(0xffffffffu, lam, off);
+      lam = warp_sum(lam);
+      lamr = warp_sum(lamr);
       if (lane == 0) {
         const float sc = (Mold == -INFINITY) ? 0.f : ex2(Mold - Mnew);
         scl[g] = sc;
         run_L[g] = fmaf(run_L[g], sc, lam);
+        run_Lr[g] = fmaf(run_Lr[g], sc, lamr);
         run_M[g] = Mnew;
       }
     }
@@ -673,7 +696,7 @@ __device__ __forceinline__ void combine_as_arrived(const Params& p, const Work& 
   for (int v = tid; v < G * (D / 4); v += kThreads) {
     const int g = v / (D / 4), c4 = v - (v / (D / 4)) * (D / 4);
     store_out4<T>(out + ((int64_t)wk.b * p.Hq + wk.kvh * G + g) * D + 4 * c4,
-                  reinterpret_cast<float4*>(run_O + g * D)[c4], run_L[g]);
+                  reinterpret_cast<float4*>(run_O + g * D)[c4], run_Lr[g]);
   }
   if (tid < G && p.lse != nullptr) {
     const float M = run_M[tid], lam = run_L[tid];
@@ -685,10 +708,10 @@ __device__ __forceinline__ void combine_as_arrived(const Params& p, const Work& 
 // every CTA holds its chunk record in shared memory (`crec`, [G][D + 4]); after a
 // cluster barrier each CTA reads all C records through distributed shared memory
 // and writes its share of the columns of the segment's record (fixed chunk
-// order; CTA 0 also writes M and Lambda).  Ends with this CTA's arrival at the
-// closing cluster barrier; the caller waits on it before the CTA exits, so no
-// CTA leaves while another still reads its shared memory.  `cf` is scratch for
-// G * (C + 2) floats.
+// order; CTA 0 also writes M and the two Lambdas).  Ends with this CTA's arrival
+// at the closing cluster barrier; the caller waits on it before the CTA exits, so
+// no CTA leaves while another still reads its shared memory.  `cf` is scratch for
+// G * (C + 3) floats.
 template <int D, int G>
 __device__ __forceinline__ void merge_segment(const Params& p, const Work& wk, const float* crec,
                                               float* cf) {
@@ -701,15 +724,17 @@ __device__ __forceinline__ void merge_segment(const Params& p, const Work& wk, c
     const uint32_t ml_a = crec_a + (uint32_t)(tid * RS + D) * 4u;
     float M = -INFINITY;
     for (int j = 0; j < C; ++j) M = fmaxf(M, ld_cluster_f2(cluster_map(ml_a, j)).x);
-    float lam = 0.f;
+    float lam = 0.f, lamr = 0.f;
     for (int j = 0; j < C; ++j) {
-      const float2 ml = ld_cluster_f2(cluster_map(ml_a, j));
+      const float4 ml = ld_cluster_f4(cluster_map(ml_a, j));
       const float f = (M == -INFINITY) ? 0.f : ex2(ml.x - M);  // an empty chunk has m = -inf
       cf[tid * C + j] = f;
       lam = fmaf(f, ml.y, lam);
+      lamr = fmaf(f, ml.z, lamr);
     }
     cf[G * C + tid] = M;
     cf[G * C + G + tid] = lam;
+    cf[G * C + 2 * G + tid] = lamr;
   }
   __syncthreads();
   constexpr int Q = D / 4;
@@ -731,12 +756,13 @@ __device__ __forceinline__ void merge_segment(const Params& p, const Work& wk, c
   }
   if (wk.c == 0 && tid < G)
     __stcg(reinterpret_cast<float4*>(p.part + (rec0 + (int64_t)tid * wk.nrec) * RS + D),
-           make_float4(cf[G * C + tid], cf[G * C + G + tid], 0.f, 0.f));
+           make_float4(cf[G * C + tid], cf[G * C + G + tid], cf[G * C + 2 * G + tid], 0.f));
   cluster_arrive();  // done reading the other CTAs' shared memory
 }
 
-// Merge NGRP running states (sm_acc [NGRP][G][D], sm_m / sm_l [NGRP][G], all in
-// shared memory) into this CTA's partial; then either finish directly (a single
+// Merge NGRP running states (sm_acc [NGRP][G][D], sm_m / sm_l / sm_lr [NGRP][G],
+// all in shared memory; sm_lr sums the rounded weights P.V used) into this CTA's
+// partial; then either finish directly (a single
 // partial), or publish the partial (merged per segment inside the cluster when
 // rps == 1), arrive, and combine if this CTA arrived last.  An `aborted` CTA (its
 // pipeline timed out; the status word says so) contributes an empty partial so
@@ -747,21 +773,24 @@ __device__ __forceinline__ void finish_cta(const Params& p, const Work& wk, floa
                                            uint32_t combine_bytes, uint32_t combine_bar) {
   float* sm_m = sm_acc + NGRP * G * D;  // [NGRP][G]
   float* sm_l = sm_m + NGRP * G;        // [NGRP][G]
-  float* sm_fac = sm_l + NGRP * G;      // [NGRP][G]
-  float* sm_ML = sm_fac + NGRP * G;     // [G][2]
+  float* sm_lr = sm_l + NGRP * G;       // [NGRP][G]
+  float* sm_fac = sm_lr + NGRP * G;     // [NGRP][G]
+  float* sm_ML = sm_fac + NGRP * G;     // [G][3]: M, Lambda, Lambda~
   const int tid = threadIdx.x;
   if (tid < G) {
     const int g = tid;
     float M = -INFINITY;
     for (int q = 0; q < NGRP; ++q) M = fmaxf(M, sm_m[q * G + g]);
-    float lam = 0.f;
+    float lam = 0.f, lamr = 0.f;
     for (int q = 0; q < NGRP; ++q) {
       const float f = (M == -INFINITY) ? 0.f : ex2(sm_m[q * G + g] - M);
       sm_fac[q * G + g] = f;
       lam = fmaf(sm_l[q * G + g], f, lam);
+      lamr = fmaf(sm_lr[q * G + g], f, lamr);
     }
-    sm_ML[2 * g] = aborted ? -INFINITY : M;
-    sm_ML[2 * g + 1] = aborted ? 0.f : lam;
+    sm_ML[3 * g] = aborted ? -INFINITY : M;
+    sm_ML[3 * g + 1] = aborted ? 0.f : lam;
+    sm_ML[3 * g + 2] = aborted ? 0.f : lamr;
   }
   __syncthreads();
 
@@ -774,11 +803,11 @@ __device__ __forceinline__ void finish_cta(const Params& p, const Work& wk, floa
       float a = 0.f;
 #pragma unroll 4
       for (int q = 0; q < NGRP; ++q) a = fmaf(sm_acc[(q * G + g) * D + dim], sm_fac[q * G + g], a);
-      const float lam = sm_ML[2 * g + 1];
-      out[((int64_t)wk.b * p.Hq + h0 + g) * D + dim] = Elem<T>::from_f(lam > 0.f ? a / lam : 0.f);
+      const float lamr = sm_ML[3 * g + 2];
+      out[((int64_t)wk.b * p.Hq + h0 + g) * D + dim] = Elem<T>::from_f(lamr > 0.f ? a / lamr : 0.f);
     }
     if (tid < G && p.lse != nullptr) {
-      const float M = sm_ML[2 * tid], lam = sm_ML[2 * tid + 1];
+      const float M = sm_ML[3 * tid], lam = sm_ML[3 * tid + 1];
       p.lse[(int64_t)wk.b * p.Hq + h0 + tid] = lam > 0.f ? (M + log2f(lam)) * kLn2 : -INFINITY;
     }
     return;
@@ -812,7 +841,7 @@ __device__ __forceinline__ void finish_cta(const Params& p, const Work& wk, floa
     }
   }
   if (tid < G) {
-    const float4 ml = make_float4(sm_ML[2 * tid], sm_ML[2 * tid + 1], 0.f, 0.f);
+    const float4 ml = make_float4(sm_ML[3 * tid], sm_ML[3 * tid + 1], sm_ML[3 * tid + 2], 0.f);
     if (merge_seg) {
       *reinterpret_cast<float4*>(crec + tid * RS + D) = ml;
     } else {
@@ -828,7 +857,7 @@ __device__ __forceinline__ void finish_cta(const Params& p, const Work& wk, floa
   if (MODE == 3) {
     __syncthreads();
     if (wk.slot != 0) {
-      const bool dropped = p.drop_flag && wk.b == 0 && wk.kvh == 0 && wk.slot == 1;
+      const bool dropped = p.test_hook == kHookDropFlag && wk.b == 0 && wk.kvh == 0 && wk.slot == 1;
       if (tid == 0 && !dropped) st_release_gpu(p.flags + flag_index(p, wk.b, wk.kvh, wk.slot), 1u);
       return;
     }
@@ -865,29 +894,36 @@ __global__ void __launch_bounds__(kThreads, 2) fd_split_kernel(const __grid_cons
   constexpr bool kSeg = MODE >= 4;
   constexpr int kMode = kSeg ? MODE - 4 : MODE;
   constexpr int TILE = tile_for(PATH);
-  constexpr int NSLOT = ring_slots_for(PATH, D);  // ring slots (one K + V tile each)
+  constexpr int LPT = loads_per_tile(PATH);       // ring slots per tile (2: K and V apart)
+  constexpr int NSLOT = ring_slots_for(PATH, D);  // ring slots
   constexpr int BOXC = box_cols_for(PATH, D);   // columns per TMA box
   constexpr int NBOX = D / BOXC;                // boxes per tensor per stage
   constexpr int KVES = kv_elem_bytes(PATH);     // bytes per stored K/V element
   constexpr uint32_t kRowsBytes = TILE * D * KVES;  // one tile of K (or V) rows
-  constexpr uint32_t kSlotBytes = 2 * kRowsBytes;   // K rows, then V rows
+  constexpr uint32_t kSlotBytes = (2 / LPT) * kRowsBytes;  // K rows then V rows, or one of them
   constexpr uint32_t kRing = NSLOT * kSlotBytes;
+  constexpr uint32_t kExtra = extra_bytes_for(PATH);
   static_assert(NSLOT >= 2 && kRowsBytes % 1024 == 0, "slots hold whole swizzle atoms");
-  static_assert((2 * NSLOT + 1) * 8 + 8 + 1024 <= kRingMetaBytes, "ring metadata must fit");
+  static_assert((2 * NSLOT + 5) * 8 + 1024 <= kRingMetaBytes, "ring metadata must fit");
+  static_assert(kRing == ring_bytes_for(PATH, D), "ring layout");
   constexpr int NGRP_FFMA = kConsumerWarps * (32 / ((G * D > 512) ? 16 : 8));
-  constexpr int NGRP = is_mma(PATH) ? kConsumerWarps : NGRP_FFMA;
+  constexpr int NGRP = PATH == kPathUmma ? 1 : is_mma(PATH) ? kConsumerWarps : NGRP_FFMA;
   static_assert(PATH == kPathFfma || G >= 4, "the MMA path needs G >= 4 heads on N");
-  static_assert(NGRP * G * D * 4 + 4 * NGRP * G * 4 + G * record_floats(D) * 4 <= kRing,
+  static_assert(NGRP * G * D * 4 + 4 * NGRP * G * 4 + 3 * G * 4 + G * record_floats(D) * 4 <= kRing,
                 "group merge and the segment-merge record must fit in the ring");
 
   // 1024-byte aligned ring: the 128-byte swizzle pattern repeats every 1024 bytes.
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kRing);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kRing + kExtra);
   int& sm_abort = *reinterpret_cast<int*>(bars + 2 * NSLOT + 1);
   int& sm_last = *(reinterpret_cast<int*>(bars + 2 * NSLOT + 1) + 1);
   auto full_bar = [&](int s) { return smem_addr(bars + s); };
   auto empty_bar = [&](int s) { return smem_addr(bars + NSLOT + s); };
+  // tcgen05 path: S^T ready, every MMA done, and the tensor-memory base address.
+  const uint32_t bar_s = smem_addr(bars + 2 * NSLOT + 2);
+  const uint32_t bar_o = smem_addr(bars + 2 * NSLOT + 3);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * NSLOT + 4);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   pdl_launch_dependents();
@@ -897,11 +933,24 @@ __global__ void __launch_bounds__(kThreads, 2) fd_split_kernel(const __grid_cons
   if (tid == 0) {
     for (int s = 0; s < NSLOT; ++s) {
       mbar_init(full_bar(s), 1);
-      mbar_init(empty_bar(s), kConsumerWarps);
+      // Released by every consumer warp, or by one tcgen05 commit.
+      mbar_init(empty_bar(s), PATH == kPathUmma ? 1 : kConsumerWarps);
     }
     mbar_init(smem_addr(bars + 2 * NSLOT), 1);  // combine copies
+    if (PATH == kPathUmma) {
+      mbar_init(bar_s, 1);
+      mbar_init(bar_o, 1);
+    }
     fence_mbar_init();
     sm_abort = 0;
+  }
+  if constexpr (PATH == kPathUmma) {
+    // 64 tensor-memory columns: S^T at 0..15, O^T at 32..47 (two CTAs per SM use 128
+    // of the 512, so the allocation never waits).
+    if (warp == 0) {
+      tc::tmem_alloc(smem_addr(tmem_slot), kTmemCols);
+      tc::tmem_relinquish();
+    }
   }
   if (warp == kConsumerWarps && lane == 0 && ntiles > 0) {
     prefetch_tensormap(&p.tm_k);
@@ -914,7 +963,7 @@ __global__ void __launch_bounds__(kThreads, 2) fd_split_kernel(const __grid_cons
     // So do CTAs past the first wave, which start after the previous kernel.
     if (p.block_table == nullptr && (int)blockIdx.x < p.prefetch_ctas) {
       const int row0 = p.cu[wk.b] + wk.t0;
-      const int npf = min(ntiles, kL2PrefetchTiles);
+      const int npf = min(ntiles, kL2PrefetchTokens / TILE);
       for (int kt = 0; kt < npf; ++kt) {
 #pragma unroll
         for (int bx = 0; bx < NBOX; ++bx) {
@@ -925,36 +974,44 @@ __global__ void __launch_bounds__(kThreads, 2) fd_split_kernel(const __grid_cons
     }
   }
   pdl_wait();  // q, K, V, the workspace and out may come from earlier kernels
+  if constexpr (PATH == kPathUmma) tc::fence_before_sync();
   __syncthreads();
 
   float* sm_acc = reinterpret_cast<float*>(smem);  // [NGRP][G][D] after the ring drains
   float* sm_m = sm_acc + NGRP * G * D;
   float* sm_l = sm_m + NGRP * G;
+  float* sm_lr = sm_l + NGRP * G;  // sums of the rounded weights P.V used
 
   if (warp == kConsumerWarps) {
     // ---------------- TMA producer ----------------
     if (lane == 0 && ntiles > 0) {
       const uint64_t policy = l2_evict_first_policy();
       const int row0 = p.cu[wk.b] + wk.t0;
-      // Tile kt goes to slot kt mod NSLOT: its K rows, then its V rows.
-      int kt = 0;
-      for (; kt < ntiles; ++kt) {
-        const int s = kt % NSLOT;
-        if (kt >= NSLOT && !mbar_wait(empty_bar(s), ((kt / NSLOT) - 1) & 1)) {
+      // Load j goes to slot j mod NSLOT.  One load per tile: its K rows, then its V
+      // rows; two loads per tile (tcgen05 path): K rows (j even), then V rows.
+      const int nload = ntiles * LPT;
+      int j = 0;
+      for (; j < nload; ++j) {
+        const int s = j % NSLOT, kt = j / LPT;
+        if (j >= NSLOT && !mbar_wait(empty_bar(s), ((j / NSLOT) - 1) & 1)) {
           atomicOr(p.status, kStatusTimeout);
           *(volatile int*)&sm_abort = 1;
           break;
         }
         if (*(volatile int*)&sm_abort) break;
+        if (p.test_hook == kHookSkipTile && kt == 1 && wk.b == 0 && wk.kvh == 0 && wk.slot == 0)
+          continue;  // test hook: this tile is never loaded
         const uint32_t dst = smem_addr(smem + (size_t)s * kSlotBytes);
+        const int h0 = LPT == 2 ? (j & 1) : 0, h1 = LPT == 2 ? (j & 1) + 1 : 2;
         mbar_arrive_expect_tx(full_bar(s), kSlotBytes);
         if (p.block_table == nullptr) {
 #pragma unroll
-          for (int h = 0; h < 2; ++h) {  // K rows, then V rows
+          for (int h = h0; h < h1; ++h) {  // K rows, then V rows
 #pragma unroll
             for (int bx = 0; bx < NBOX; ++bx)
-              tma_load_3d(dst + h * kRowsBytes + bx * (TILE * BOXC * KVES), h ? &p.tm_v : &p.tm_k,
-                          bx * BOXC, wk.kvh, row0 + kt * TILE, full_bar(s), policy);
+              tma_load_3d(dst + (h - h0) * kRowsBytes + bx * (TILE * BOXC * KVES),
+                          h ? &p.tm_v : &p.tm_k, bx * BOXC, wk.kvh, row0 + kt * TILE, full_bar(s),
+                          policy);
           }
         } else {
           // Paged: one box per page piece of the tile.  Tiles start on multiples of
@@ -963,25 +1020,232 @@ __global__ void __launch_bounds__(kThreads, 2) fd_split_kernel(const __grid_cons
           const int32_t* bt = p.block_table + (int64_t)wk.b * p.bt_stride;
           const int last_pg = (p.cu[wk.b + 1] - p.cu[wk.b] - 1) >> p.page_shift;
           const int a = wk.t0 + kt * TILE;
-          for (int j = 0; j < TILE; j += p.box_rows) {
-            const int pg = min((a + j) >> p.page_shift, last_pg);
-            const int row = __ldg(bt + pg) * (1 << p.page_shift) + ((a + j) & ((1 << p.page_shift) - 1));
+          for (int r = 0; r < TILE; r += p.box_rows) {
+            const int pg = min((a + r) >> p.page_shift, last_pg);
+            const int row = __ldg(bt + pg) * (1 << p.page_shift) + ((a + r) & ((1 << p.page_shift) - 1));
 #pragma unroll
-            for (int h = 0; h < 2; ++h) {  // K rows, then V rows
+            for (int h = h0; h < h1; ++h) {  // K rows, then V rows
 #pragma unroll
               for (int bx = 0; bx < NBOX; ++bx)
-                tma_load_3d(dst + h * kRowsBytes + bx * (TILE * BOXC * KVES) + j * BOXC * KVES,
+                tma_load_3d(dst + (h - h0) * kRowsBytes + bx * (TILE * BOXC * KVES) + r * BOXC * KVES,
                             h ? &p.tm_v : &p.tm_k, bx * BOXC, wk.kvh, row, full_bar(s), policy);
             }
           }
         }
       }
       // Every load issued must land before shared memory is reused or released.
-      for (int t = (kt > NSLOT ? kt - NSLOT : 0); t < kt; ++t) {
+      for (int t = (j > NSLOT ? j - NSLOT : 0); t < j; ++t) {
         if (!mbar_wait(full_bar(t % NSLOT), (t / NSLOT) & 1)) atomicOr(p.status, kStatusTimeout);
       }
     }
     __syncthreads();
+  } else if constexpr (PATH == kPathUmma) {
+    // ---------------- tcgen05 consumers ----------------
+    // Thread tid (0..127) owns row tid of S^T (token tid of the tile) and of O^T
+    // (head dimension tid), i.e. TMEM lane tid, which its warp's quarter reaches.
+    // Thread 0 also issues every MMA.  The running max m is per head and uniform
+    // across the CTA; l and l~ are per-thread partial sums over its tokens.
+    static_assert(D == 128 && (G == 4 || G == 8 || G == 16), "tcgen05 path: d = 128, G in {4, 8, 16}");
+    constexpr int NP = 16;  // MMA N: the G heads, padded with zero rows of Q
+    constexpr bool kBf16 = std::is_same<T, __nv_bfloat16>::value;
+    constexpr uint32_t kIdS = tc::idesc_f16(kBf16, false, false, 128, NP);  // K, Q: K-major
+    constexpr uint32_t kIdO = tc::idesc_f16(kBf16, true, true, 128, NP);    // V^T, P^T: MN-major
+    tc::fence_after_sync();
+    const uint32_t tmem = *tmem_slot;
+    const uint32_t trow = (uint32_t)(warp * 32) << 16;  // this warp's TMEM lane quarter
+    uint8_t* qs = smem + kRing;        // Q: 16 rows x 128, two 64-column 128-byte-swizzled halves
+    uint8_t* ps = qs + 4096;           // P^T: 128 token rows x 16 heads, 32-byte swizzle
+    float* wmax = reinterpret_cast<float*>(qs + 8192);  // [4 warps][16] per-warp tile maxima
+    const uint32_t qs_a = smem_addr(qs), ps_a = smem_addr(ps);
+
+    // Q into shared memory (zero rows for the padding heads).
+    for (int c = tid; c < NP * (D / 8); c += 4 * 32) {
+      const int r = c / (D / 8), ch = c - r * (D / 8);
+      uint4 v = make_uint4(0u, 0u, 0u, 0u);
+      if (r < G)
+        v = *reinterpret_cast<const uint4*>(reinterpret_cast<const T*>(p.q) +
+                                             ((int64_t)wk.b * p.Hq + wk.kvh * G + r) * D + ch * 8);
+      *reinterpret_cast<uint4*>(qs + (ch >> 3) * 2048 + r * 128 + (((ch & 7) ^ (r & 7)) << 4)) = v;
+    }
+    tc::fence_proxy_async_smem();
+    tc::named_sync(1, 4 * 32);
+
+    // S^T(kt) = K(kt) Q^T into columns kColS; releases K's slot when done.
+    auto issue_s = [&](int kt) -> bool {
+      const int jl = kt * 2, s = jl % NSLOT;
+      if (!mbar_wait(full_bar(s), (jl / NSLOT) & 1)) return false;
+      tc::fence_after_sync();
+      const uint32_t ka = smem_addr(smem + (size_t)s * kSlotBytes);
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk)
+        tc::mma_f16_ss(tmem + kColS,
+                       tc::smem_desc(ka + (kk >> 2) * (TILE * 128) + (kk & 3) * 32, 16, 1024,
+                                     tc::kSwizzle128B),
+                       tc::smem_desc(qs_a + (kk >> 2) * (NP * 128) + (kk & 3) * 32, 16, 1024,
+                                     tc::kSwizzle128B),
+                       kIdS, kk > 0);
+      tc::commit(empty_bar(s));
+      tc::commit(bar_s);
+      return true;
+    };
+    // O^T += V(kt)^T P^T into columns kColO; releases V's slot when done.
+    auto issue_pv = [&](int kt) -> bool {
+      const int jl = kt * 2 + 1, s = jl % NSLOT;
+      if (!mbar_wait(full_bar(s), (jl / NSLOT) & 1)) return false;
+      tc::fence_after_sync();
+      const uint32_t va = smem_addr(smem + (size_t)s * kSlotBytes);
+#pragma unroll
+      for (int kk = 0; kk < TILE / 16; ++kk)
+        tc::mma_f16_ss(tmem + kColO,
+                       tc::smem_desc(va + kk * 2048, TILE * 128, 1024, tc::kSwizzle128B),
+                       tc::smem_desc(ps_a + kk * 512, 16, 256, tc::kSwizzle32B),
+                       kIdO, (kt > 0 || kk > 0) ? 1u : 0u);
+      tc::commit(empty_bar(s));
+      return true;
+    };
+    auto give_up = [&]() {  // thread 0: a load never arrived
+      atomicOr(p.status, kStatusTimeout);
+      *(volatile int*)&sm_abort = 1;
+    };
+
+    float m_run[G], l_ex[G], l_rd[G];
+#pragma unroll
+    for (int g = 0; g < G; ++g) { m_run[g] = -INFINITY; l_ex[g] = 0.f; l_rd[g] = 0.f; }
+    const float scale = p.scale_log2;
+    if (tid == 0 && ntiles > 0 && !issue_s(0)) {
+      give_up();
+      mbar_arrive(bar_s);
+    }
+    __syncwarp();
+    for (int kt = 0; kt < ntiles; ++kt) {
+      const bool ok = mbar_wait(bar_s, kt & 1);
+      tc::fence_after_sync();
+      float x[16];
+      tc::ld16(tmem + trow + kColS, x);
+      tc::wait_ld();
+      const int ntok = min(TILE, wk.t1 - (wk.t0 + kt * TILE));
+      const bool valid = tid < ntok;
+      bool need = false;
+#pragma unroll
+      for (int g = 0; g < G; ++g) {
+        x[g] = valid ? x[g] * scale : -INFINITY;
+        need |= x[g] > m_run[g] + kRescaleThreshold;
+      }
+      // The producer may set sm_abort at any time, so whether to stop is decided
+      // only by barrier reductions, whose result every consumer thread shares.
+      const bool stop = !ok || *(volatile int*)&sm_abort != 0;
+      if (tc::named_sync_or(1, 4 * 32, need || stop)) {
+        // Rare: a wait gave up, or some head's maximum grew by more than 2^8.
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+          const float mx = warp_max(x[g]);
+          if (lane == 0) wmax[warp * NP + g] = mx;
+        }
+        if (tc::named_sync_or(1, 4 * 32, stop)) {
+          if (!ok) atomicOr(p.status, kStatusTimeout);
+          *(volatile int*)&sm_abort = 1;
+          break;
+        }
+        float corr[G];
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+          const float mt = fmaxf(fmaxf(wmax[g], wmax[NP + g]), fmaxf(wmax[2 * NP + g], wmax[3 * NP + g]));
+          const float mn = fmaxf(m_run[g], mt);
+          corr[g] = m_run[g] == -INFINITY ? 0.f : ex2(m_run[g] - mn);
+          m_run[g] = mn;
+          l_ex[g] *= corr[g];
+          l_rd[g] *= corr[g];
+        }
+        if (kt > 0) {
+          // O^T holds the earlier tiles (their P.V completed before S^T(kt) did).
+          float o[16];
+          tc::ld16(tmem + trow + kColO, o);
+          tc::wait_ld();
+#pragma unroll
+          for (int g = 0; g < G; ++g) o[g] *= corr[g];
+          tc::st16(tmem + trow + kColO, o);
+          tc::wait_st();
+        }
+      }
+      // P^T row of token tid (zero for padding heads and masked tokens).
+      uint32_t pk[NP / 2];
+#pragma unroll
+      for (int i = 0; i < NP / 2; ++i) {
+        if (2 * i < G) {
+          const float pa = ex2(x[2 * i] - m_run[2 * i]), pb = ex2(x[2 * i + 1] - m_run[2 * i + 1]);
+          l_ex[2 * i] += pa;
+          l_ex[2 * i + 1] += pb;
+          pk[i] = pack2<T>(pa, pb);
+          const float2 w = Elem<T>::to_f2(pk[i]);
+          l_rd[2 * i] += w.x;
+          l_rd[2 * i + 1] += w.y;
+        } else {
+          pk[i] = 0u;
+        }
+      }
+      {
+        uint8_t* prow = ps + (tid >> 3) * 256 + (tid & 7) * 32;
+        const int sw = (tid >> 2) & 1;  // 32-byte swizzle: 16-byte halves swap in rows 4..7
+        *reinterpret_cast<uint4*>(prow + (sw << 4)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+        *reinterpret_cast<uint4*>(prow + ((sw ^ 1) << 4)) = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+      }
+      tc::fence_proxy_async_smem();
+      tc::fence_before_sync();
+      tc::named_sync(1, 4 * 32);
+      if (tid == 0) {
+        if (!issue_pv(kt)) {
+          give_up();
+          if (kt + 1 < ntiles) mbar_arrive(bar_s);
+        } else if (kt + 1 < ntiles && !issue_s(kt + 1)) {
+          give_up();
+          mbar_arrive(bar_s);
+        }
+      }
+      __syncwarp();
+    }
+    // Every MMA issued has completed once bar_o fires (commit with nothing pending
+    // arrives at once).
+    if (tid == 0) tc::commit(bar_o);
+    __syncwarp();
+    if (!mbar_wait(bar_o, 0)) {
+      atomicOr(p.status, kStatusTimeout);
+      *(volatile int*)&sm_abort = 1;
+    }
+    tc::fence_after_sync();
+    float o[16];
+    tc::ld16(tmem + trow + kColO, o);
+    tc::wait_ld();
+    // l and l~ over the 128 token rows: warp trees, then the four warps in order.
+    float* red = wmax;  // [4 warps][2][16]
+    tc::named_sync(1, 4 * 32);
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+      const float a = warp_sum(l_ex[g]), b = warp_sum(l_rd[g]);
+      if (lane == 0) {
+        red[warp * 2 * NP + g] = a;
+        red[warp * 2 * NP + NP + g] = b;
+      }
+    }
+    tc::fence_before_sync();
+    __syncthreads();  // ring drained (the producer waited for its loads): reuse it
+    if (*(volatile int*)&sm_abort == 0) {
+#pragma unroll
+      for (int g = 0; g < G; ++g) sm_acc[g * D + tid] = ntiles > 0 ? o[g] : 0.f;
+      if (tid < G) {
+        float a = 0.f, b = 0.f;
+#pragma unroll
+        for (int w = 0; w < 4; ++w) {
+          a += red[w * 2 * NP + tid];
+          b += red[w * 2 * NP + NP + tid];
+        }
+        float mrun = -INFINITY;
+#pragma unroll
+        for (int g = 0; g < G; ++g) mrun = g == tid ? m_run[g] : mrun;
+        sm_m[tid] = mrun;
+        sm_l[tid] = a;
+        sm_lr[tid] = b;
+      }
+    }
   } else if constexpr (PATH == kPathMmaKv8) {
     // ---------------- MMA consumers over an FP8 (E4M3) cache ----------------
     // Fragments are loaded straight from the 128-byte swizzled byte rows.  Two index
@@ -1009,13 +1273,14 @@ __global__ void __launch_bounds__(kThreads, 2) fd_split_kernel(const __grid_cons
       }
     }
     float o[NT][KT][4];
-    float mA[NT], mB[NT], lA[NT], lB[NT];
+    // l: sums of the fp32 weights (for lse); lr: of the 16-bit weights P.V uses (for out).
+    float mA[NT], mB[NT], lA[NT], lB[NT], lrA[NT], lrB[NT];
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
 #pragma unroll
       for (int mi = 0; mi < KT; ++mi) o[nt][mi][0] = o[nt][mi][1] = o[nt][mi][2] = o[nt][mi][3] = 0.f;
       mA[nt] = mB[nt] = -INFINITY;
-      lA[nt] = lB[nt] = 0.f;
+      lA[nt] = lB[nt] = lrA[nt] = lrB[nt] = 0.f;
     }
     const float scale = p.scale_log2 * 256.f;
     const int tok0 = warp * 16;
@@ -1077,6 +1342,7 @@ __global__ void __launch_bounds__(kThreads, 2) fd_split_kernel(const __grid_cons
           if (xA > mA[nt] + kRescaleThreshold) {
             const float corr = ex2(mA[nt] - xA);
             lA[nt] *= corr;
+            lrA[nt] *= corr;
 #pragma unroll
             for (int mi = 0; mi < KT; ++mi) { o[nt][mi][0] *= corr; o[nt][mi][2] *= corr; }
             mA[nt] = xA;
@@ -1084,6 +1350,7 @@ __global__ void __launch_bounds__(kThreads, 2) fd_split_kernel(const __grid_cons
           if (xB > mB[nt] + kRescaleThreshold) {
             const float corr = ex2(mB[nt] - xB);
             lB[nt] *= corr;
+            lrB[nt] *= corr;
 #pragma unroll
             for (int mi = 0; mi < KT; ++mi) { o[nt][mi][1] *= corr; o[nt][mi][3] *= corr; }
             mB[nt] = xB;
@@ -1092,8 +1359,14 @@ __global__ void __launch_bounds__(kThreads, 2) fd_split_kernel(const __grid_cons
           const float pA1 = ex2(sA1 - mA[nt]), pB1 = ex2(sB1 - mB[nt]);
           lA[nt] += pA0 + pA1;
           lB[nt] += pB0 + pB1;
-          pb0[nt] = movmatrix_trans(pack2<T>(pA0, pB0));
-          pb1[nt] = movmatrix_trans(pack2<T>(pA1, pB1));
+          const uint32_t r0 = pack2<T>(pA0, pB0), r1 = pack2<T>(pA1, pB1);
+          // lr sums the same 16-bit weights that P.V multiplies, so the output is an
+          // exact convex combination of V rows under the rounded weights.
+          const float2 w0 = Elem<T>::to_f2(r0), w1 = Elem<T>::to_f2(r1);
+          lrA[nt] += w0.x + w1.x;
+          lrB[nt] += w0.y + w1.y;
+          pb0[nt] = movmatrix_trans(r0);
+          pb1[nt] = movmatrix_trans(r1);
         }
         // V^T: token rows tok0 + 2t, +1, +8, +9; the 16-byte chunk g (dims 16g ..).
         uint4 vw[4];
@@ -1133,6 +1406,8 @@ __global__ void __launch_bounds__(kThreads, 2) fd_split_kernel(const __grid_cons
       for (int off = 4; off < 32; off <<= 1) {
         lA[nt] += __shfl_xor_sync(0xffffffffu, lA[nt], off);
         lB[nt] += __shfl_xor_sync(0xffffffffu, lB[nt], off);
+        lrA[nt] += __shfl_xor_sync(0xffffffffu, lrA[nt], off);
+        lrB[nt] += __shfl_xor_sync(0xffffffffu, lrB[nt], off);
       }
     }
     __syncthreads();  // ring drained: reuse it for the per-warp states
@@ -1155,6 +1430,8 @@ __global__ void __launch_bounds__(kThreads, 2) fd_split_kernel(const __grid_cons
             sm_m[warp * G + hA + 1] = mB[nt];
             sm_l[warp * G + hA] = lA[nt];
             sm_l[warp * G + hA + 1] = lB[nt];
+            sm_lr[warp * G + hA] = lrA[nt];
+            sm_lr[warp * G + hA + 1] = lrB[nt];
           }
         }
       }
@@ -1180,13 +1457,14 @@ __global__ void __launch_bounds__(kThreads, 2) fd_split_kernel(const __grid_cons
       }
     }
     float o[NT][KT][4];
-    float mA[NT], mB[NT], lA[NT], lB[NT];
+    // l: sums of the fp32 weights (for lse); lr: of the 16-bit weights P.V uses (for out).
+    float mA[NT], mB[NT], lA[NT], lB[NT], lrA[NT], lrB[NT];
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
 #pragma unroll
       for (int mi = 0; mi < KT; ++mi) o[nt][mi][0] = o[nt][mi][1] = o[nt][mi][2] = o[nt][mi][3] = 0.f;
       mA[nt] = mB[nt] = -INFINITY;
-      lA[nt] = lB[nt] = 0.f;
+      lA[nt] = lB[nt] = lrA[nt] = lrB[nt] = 0.f;
     }
     const float scale = p.scale_log2;
     const int tok0 = warp * 16;
@@ -1234,6 +1512,7 @@ __global__ void __launch_bounds__(kThreads, 2) fd_split_kernel(const __grid_cons
           if (xA > mA[nt] + kRescaleThreshold) {
             const float corr = ex2(mA[nt] - xA);
             lA[nt] *= corr;
+            lrA[nt] *= corr;
 #pragma unroll
             for (int mi = 0; mi < KT; ++mi) { o[nt][mi][0] *= corr; o[nt][mi][2] *= corr; }
             mA[nt] = xA;
@@ -1241,6 +1520,7 @@ __global__ void __launch_bounds__(kThreads, 2) fd_split_kernel(const __grid_cons
           if (xB > mB[nt] + kRescaleThreshold) {
             const float corr = ex2(mB[nt] - xB);
             lB[nt] *= corr;
+            lrB[nt] *= corr;
 #pragma unroll
             for (int mi = 0; mi < KT; ++mi) { o[nt][mi][1] *= corr; o[nt][mi][3] *= corr; }
             mB[nt] = xB;
@@ -1250,9 +1530,15 @@ __global__ void __launch_bounds__(kThreads, 2) fd_split_kernel(const __grid_cons
           const float pA1 = ex2(sA1 - mA[nt]), pB1 = ex2(sB1 - mB[nt]);
           lA[nt] += pA0 + pA1;
           lB[nt] += pB0 + pB1;
+          const uint32_t r0 = pack2<T>(pA0, pB0), r1 = pack2<T>(pA1, pB1);
+          // lr sums the same 16-bit weights that P.V multiplies (numerator and
+          // normaliser of out see one set of weights).
+          const float2 w0 = Elem<T>::to_f2(r0), w1 = Elem<T>::to_f2(r1);
+          lrA[nt] += w0.x + w1.x;
+          lrB[nt] += w0.y + w1.y;
           // P (tokens x heads, accumulator layout) -> P^T as the B operand (k = token).
-          pb0[nt] = movmatrix_trans(pack2<T>(pA0, pB0));
-          pb1[nt] = movmatrix_trans(pack2<T>(pA1, pB1));
+          pb0[nt] = movmatrix_trans(r0);
+          pb1[nt] = movmatrix_trans(r1);
         }
 #pragma unroll
         for (int mi = 0; mi < KT; ++mi) {
@@ -1272,6 +1558,8 @@ __global__ void __launch_bounds__(kThreads, 2) fd_split_kernel(const __grid_cons
       for (int off = 4; off < 32; off <<= 1) {
         lA[nt] += __shfl_xor_sync(0xffffffffu, lA[nt], off);
         lB[nt] += __shfl_xor_sync(0xffffffffu, lB[nt], off);
+        lrA[nt] += __shfl_xor_sync(0xffffffffu, lrA[nt], off);
+        lrB[nt] += __shfl_xor_sync(0xffffffffu, lrB[nt], off);
       }
     }
     __syncthreads();  // ring drained: reuse it for the per-warp states
@@ -1294,6 +1582,8 @@ __global__ void __launch_bounds__(kThreads, 2) fd_split_kernel(const __grid_cons
             sm_m[warp * G + hA + 1] = mB[nt];
             sm_l[warp * G + hA] = lA[nt];
             sm_l[warp * G + hA + 1] = lB[nt];
+            sm_lr[warp * G + hA] = lrA[nt];
+            sm_lr[warp * G + hA + 1] = lrB[nt];
           }
         }
       }
@@ -1426,14 +1716,21 @@ __global__ void __launch_bounds__(kThreads, 2) fd_split_kernel(const __grid_cons
         for (int g = 0; g < G; ++g) {
           sm_m[gi * G + g] = m_run[g];
           sm_l[gi * G + g] = l_run[g];
+          sm_lr[gi * G + g] = l_run[g];  // fp32 weights: P.V used the same ones
         }
       }
     }
   }
   __syncthreads();
-  // A CTA of a cluster must still reach the cluster barriers: it finishes with an
-  // empty partial instead.
-  if (sm_abort && !kSeg) return;
+  if constexpr (PATH == kPathUmma) {
+    if (warp == 0) {  // the allocating warp; every tensor-memory read has completed
+      tc::fence_after_sync();
+      tc::tmem_dealloc(*tmem_slot, kTmemCols);
+    }
+  }
+  // A CTA whose pipeline gave up (the status word says so) still finishes, with an
+  // empty partial: its (sequence, KV head) counter must complete and return to zero,
+  // and a CTA of a cluster must still reach the cluster barriers.
   finish_cta<T, D, G, NGRP, kMode, kSeg>(p, wk, sm_acc, sm_last, sm_abort != 0, smem, kRing,
                                          smem_addr(bars + 2 * NSLOT));
 }
@@ -1536,6 +1833,16 @@ cudaError_t launch_typed(const Params& p, int d, int G, int path, int mode, bool
     FD_CASE(128, 4, kPathMmaKv8) FD_CASE(128, 8, kPathMmaKv8) FD_CASE(128, 16, kPathMmaKv8)
   }
 #undef FD_CASE
+  return cudaErrorInvalidValue;
+}
+
+// The tcgen05 consumers (d = 128, G in {4, 8, 16}); their own translation units.
+template <typename T>
+cudaError_t launch_typed_umma(const Params& p, int d, int G, int mode, bool pdl, int grid,
+                              cudaStream_t s) {
+  if (d == 128 && G == 4) return launch_dgp<T, 128, 4, kPathUmma>(p, mode, pdl, grid, s);
+  if (d == 128 && G == 8) return launch_dgp<T, 128, 8, kPathUmma>(p, mode, pdl, grid, s);
+  if (d == 128 && G == 16) return launch_dgp<T, 128, 16, kPathUmma>(p, mode, pdl, grid, s);
   return cudaErrorInvalidValue;
 }
 

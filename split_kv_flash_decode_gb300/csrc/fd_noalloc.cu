@@ -9,7 +9,10 @@
 // array of FD_NOALLOC_SCRATCH_BYTES, which every GPU that loads the library
 // holds until the process exits.  It calls no cudaMalloc, cudaFree or other
 // allocating routine.
+#include <algorithm>
 #include <mutex>
+
+#include <cudaTypedefs.h>  // PFN_cuCtxGetCurrent, PFN_cuCtxGetId
 
 #include "fd_plan_internal.h"
 
@@ -21,10 +24,49 @@ static __device__ __align__(256) uint8_t g_noalloc_scratch[FD_NOALLOC_SCRATCH_BY
 
 constexpr int kMaxDevices = 64;
 std::mutex g_mu;
-void* g_scratch_addr[kMaxDevices] = {};
+struct ScratchSlot {
+  unsigned long long ctx_id;  // driver id of the context the address belongs to
+  void* addr;
+};
+ScratchSlot g_scratch[kMaxDevices] = {};
 
-// Device address of the scratch array on the current device, looked up once per
-// device (with that device current) on the first call made on it.
+// Driver calls that name the current context: its unique id changes when the
+// context is destroyed and created again (cudaDeviceReset), even if the handle
+// value is reused, and the module holding the array is then loaded again.
+struct CtxFns {
+  PFN_cuCtxGetCurrent_v4000 get_current = nullptr;
+  PFN_cuCtxGetId_v12000 get_id = nullptr;
+};
+const CtxFns& ctx_fns() {
+  static CtxFns fns;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &ptr, 4000, cudaEnableDefault, &q) ==
+            cudaSuccess && q == cudaDriverEntryPointSuccess)
+      fns.get_current = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(ptr);
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess && q == cudaDriverEntryPointSuccess)
+      fns.get_id = reinterpret_cast<PFN_cuCtxGetId_v12000>(ptr);
+  });
+  return fns;
+}
+
+// Id of the calling thread's current context; 0 if there is none yet.
+unsigned long long current_ctx_id() {
+  const CtxFns& f = ctx_fns();
+  CUcontext ctx = nullptr;
+  unsigned long long id = 0;
+  if (!f.get_current || !f.get_id || f.get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr ||
+      f.get_id(ctx, &id) != CUDA_SUCCESS)
+    return 0;
+  return id;
+}
+
+// Device address of the scratch array in the current device's context.  It is
+// looked up (cudaGetSymbolAddress, with that device current) on the first call in
+// each context, and kept for later calls in the same context.
 int scratch_address(void** out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) {
@@ -33,15 +75,17 @@ int scratch_address(void** out) {
   }
   if (dev < 0 || dev >= kMaxDevices) return FD_ERR_UNSUPPORTED;
   std::lock_guard<std::mutex> lock(g_mu);
-  if (g_scratch_addr[dev] == nullptr) {
+  const unsigned long long id = current_ctx_id();
+  if (id == 0 || g_scratch[dev].addr == nullptr || g_scratch[dev].ctx_id != id) {
     void* addr = nullptr;
     if (cudaGetSymbolAddress(&addr, g_noalloc_scratch) != cudaSuccess || addr == nullptr) {
       cudaGetLastError();
       return FD_ERR_CUDA;
     }
-    g_scratch_addr[dev] = addr;
+    g_scratch[dev].addr = addr;
+    g_scratch[dev].ctx_id = current_ctx_id();  // the lookup made the context current
   }
-  *out = g_scratch_addr[dev];
+  *out = g_scratch[dev].addr;
   return FD_OK;
 }
 
@@ -77,26 +121,65 @@ extern "C" int fd_decode_noalloc(fd_plan_t pl, const void* q, const void* k, con
   p.counters = reinterpret_cast<uint32_t*>(ws + pl->off_counters);
   p.part = reinterpret_cast<float*>(ws + pl->off_part);
   p.flags = reinterpret_cast<uint32_t*>(ws + pl->off_flags);
-  p.drop_flag = (pl->flags & FD_PLAN_TEST_DROP_FLAG) ? 1 : 0;
 
   // The array keeps whatever the previous call left: the status word and the
   // arrival counters must start at zero, so clear them on the stream first.
   cudaError_t err = cudaMemsetAsync(ws, 0, pl->off_part, stream);
   if (err == cudaSuccess) {
-    auto launch = pl->dtype == FD_BF16 ? fd::launch_bf16 : fd::launch_f16;
-    const bool pdl = !(pl->flags & FD_PLAN_NO_PDL);
     if (pl->flags & FD_PLAN_TWO_LAUNCH) {
-      err = launch(p, pl->d, pl->G, pl->path, 1, pdl, pl->ctas, stream);
-      if (err == cudaSuccess)
-        err = launch(p, pl->d, pl->G, pl->path, 2, pdl, pl->B * pl->Hkv, stream);
+      err = fd::launch_plan(pl, p, 1, pl->ctas, stream);
+      if (err == cudaSuccess) err = fd::launch_plan(pl, p, 2, pl->B * pl->Hkv, stream);
     } else {
-      err = launch(p, pl->d, pl->G, pl->path, (pl->flags & FD_PLAN_WAITS) ? 3 : 0, pdl, pl->ctas,
-                   stream);
+      err = fd::launch_plan(pl, p, (pl->flags & FD_PLAN_WAITS) ? 3 : 0, pl->ctas, stream);
     }
   }
   if (err != cudaSuccess) {
     cudaGetLastError();
     return err == cudaErrorCooperativeLaunchTooLarge ? FD_ERR_UNSUPPORTED : FD_ERR_CUDA;
   }
+  if (pl->flags & FD_PLAN_DEBUG) {
+    int32_t st = FD_OK;
+    rc = fd_noalloc_status(pl, stream, &st);
+    if (rc != FD_OK) return rc;
+    if (st != FD_OK) return st;
+  }
+  return FD_OK;
+}
+
+// Status of the last fd_decode_noalloc call of this plan's shape on the current
+// device: the status word, then the counters and ready flags, which a completed
+// decode leaves at zero.  Reads through the runtime (device-to-host copies into
+// stack buffers); allocates nothing.
+extern "C" int fd_noalloc_status(fd_plan_t pl, cudaStream_t stream, int32_t* status) {
+  if (!pl || !status) return FD_ERR_INVALID;
+  if (pl->ws_bytes > (size_t)FD_NOALLOC_SCRATCH_BYTES) return FD_ERR_UNSUPPORTED;
+  void* scratch = nullptr;
+  int rc = scratch_address(&scratch);
+  if (rc != FD_OK) return rc;
+  const uint8_t* ws = static_cast<const uint8_t*>(scratch);
+  uint32_t word = 0;
+  if (cudaStreamSynchronize(stream) != cudaSuccess ||
+      cudaMemcpy(&word, ws, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess) {
+    cudaGetLastError();
+    return FD_ERR_CUDA;
+  }
+  // Counters and flags: [off_counters, off_part) holds both (flags follow the counters).
+  bool at_rest = true;
+  uint32_t buf[1024];
+  for (size_t off = pl->off_counters; off < pl->off_part && at_rest; off += sizeof(buf)) {
+    const size_t n = std::min(sizeof(buf), pl->off_part - off);
+    if (cudaMemcpy(buf, ws + off, n, cudaMemcpyDeviceToHost) != cudaSuccess) {
+      cudaGetLastError();
+      return FD_ERR_CUDA;
+    }
+    for (size_t i = 0; i < n / sizeof(uint32_t); ++i) at_rest = at_rest && buf[i] == 0u;
+  }
+  if (cudaMemset(const_cast<uint8_t*>(ws), 0, sizeof(word)) != cudaSuccess) {
+    cudaGetLastError();
+    return FD_ERR_CUDA;
+  }
+  *status = (word & fd::kStatusTimeout) ? FD_ERR_TIMEOUT
+          : (word != 0 || !at_rest)     ? FD_ERR_STATE
+                                        : FD_OK;
   return FD_OK;
 }

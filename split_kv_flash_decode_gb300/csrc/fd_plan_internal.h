@@ -7,7 +7,7 @@ struct fd_plan_s {
   int B, Hq, Hkv, d, G, dtype;
   uint32_t flags;
   int C;
-  int path;       // fd::kPathFfma or fd::kPathMma
+  int path;       // fd::kPathFfma, kPathMma, kPathMmaKv8 or kPathUmma
   int page_size;  // 0: contiguous K/V; else tokens per page of a paged cache
   int max_pages;  // max_b ceil(L_b / page_size) (paged plans)
   int num_sms;
@@ -24,4 +24,17 @@ namespace fd {
 // pool) at `base`; one box is `box_rows` token rows of one head.
 int encode_kv_map(CUtensorMap* map, const void* base, int64_t rows, int box_rows,
                   const fd_plan_s* pl);
+}  // namespace fd
+
+namespace fd {
+// One kernel launch of the plan's consumer path and dtype (mode as for launch_f16).
+inline cudaError_t launch_plan(const fd_plan_s* pl, const Params& p, int mode, int grid,
+                               cudaStream_t s) {
+  const bool pdl = !(pl->flags & FD_PLAN_NO_PDL);
+  if (pl->path == kPathUmma)
+    return pl->dtype == FD_BF16 ? launch_umma_bf16(p, pl->d, pl->G, mode, pdl, grid, s)
+                                : launch_umma_f16(p, pl->d, pl->G, mode, pdl, grid, s);
+  return pl->dtype == FD_BF16 ? launch_bf16(p, pl->d, pl->G, pl->path, mode, pdl, grid, s)
+                              : launch_f16(p, pl->d, pl->G, pl->path, mode, pdl, grid, s);
+}
 }  // namespace fd

@@ -85,7 +85,7 @@ def test_plan_validation(args, code):
 def test_plan_bad_dtype_flags_chunks():
     assert _raw_plan(1, 8, 8, 128, [10], [1], dtype=3) == fd.FD_ERR_INVALID
     assert _raw_plan(1, 8, 8, 128, [10], [1], dtype=2) == fd.FD_ERR_UNSUPPORTED  # FP8 K/V: G >= 4
-    assert _raw_plan(1, 8, 8, 128, [10], [1], flags=0x200) == fd.FD_ERR_INVALID
+    assert _raw_plan(1, 8, 8, 128, [10], [1], flags=0x10000) == fd.FD_ERR_INVALID
     assert _raw_plan(1, 8, 8, 128, [10], [1], flags=fd.FD_PLAN_CLUSTER | fd.FD_PLAN_NO_CLUSTER) == fd.FD_ERR_INVALID
     assert _raw_plan(1, 8, 8, 128, [10], [1], flags=fd.FD_PLAN_CLUSTER | fd.FD_PLAN_WAITS) == fd.FD_ERR_INVALID
     assert _raw_plan(1, 8, 8, 128, [10], [1], chunks=-1) == fd.FD_ERR_INVALID
@@ -94,6 +94,9 @@ def test_plan_bad_dtype_flags_chunks():
     assert _raw_plan(1, 8, 8, 128, [10], [1], flags=fd.FD_PLAN_WAITS | fd.FD_PLAN_TWO_LAUNCH) == fd.FD_ERR_INVALID
     assert _raw_plan(1, 8, 8, 128, [10], [1], flags=fd.FD_PLAN_TEST_DROP_FLAG) == fd.FD_ERR_INVALID
     assert _raw_plan(1, 8, 8, 128, [10], [1], flags=fd.FD_PLAN_WAITS | fd.FD_PLAN_TEST_DROP_FLAG) == fd.FD_OK
+    assert _raw_plan(1, 8, 8, 128, [10], [1], flags=fd.FD_PLAN_TEST_SKIP_TILE) == fd.FD_OK
+    assert _raw_plan(1, 8, 8, 128, [10], [1], flags=fd.FD_PLAN_WAITS | fd.FD_PLAN_TEST_DROP_FLAG
+                     | fd.FD_PLAN_TEST_SKIP_TILE) == fd.FD_ERR_INVALID
     L = fd.lib()
     assert L.fd_plan(1, 8, 8, 128, None, None, 0, 0, 0, 152, None) == fd.FD_ERR_INVALID
     assert L.fd_plan_destroy(None) == fd.FD_OK
@@ -210,6 +213,27 @@ def test_consumer_path_choice():
     assert ei.value.status == fd.FD_ERR_UNSUPPORTED
 
 
+def test_tcgen05_plan_rules():
+    """tcgen05 consumers: d = 128, G in {4, 8, 16}, 16-bit K/V; paged caches align
+    segments and chunks to its 128-token tiles."""
+    for G in (4, 8, 16):
+        for dtype in ("f16", "bf16"):
+            p = fd.fd_plan(1, 8 * G, 8, 128, [1000], 2, dtype, flags=fd.FD_PLAN_TCGEN05,
+                           num_sms=152)
+            assert p.info["path"] == 3
+    for Hq, d, dtype, flags in ((16, 128, "f16", 0), (8, 128, "bf16", 0), (32, 64, "f16", 0),
+                                (32, 128, "f16_e4m3kv", 0), (32, 128, "f16", fd.FD_PLAN_FFMA)):
+        with pytest.raises(fd.FdError) as ei:
+            fd.fd_plan(1, Hq, 8, d, [4096], 4, dtype, flags=flags | fd.FD_PLAN_TCGEN05, num_sms=152)
+        assert ei.value.status == fd.FD_ERR_UNSUPPORTED
+    p = fd.fd_plan_paged(2, 32, 8, 128, [5000, 777], [3, 2], 16, "f16",
+                         flags=fd.FD_PLAN_TCGEN05, num_sms=152)
+    for b, L in ((0, 5000), (1, 777)):
+        for slot in range(p.info["max_partials"] if b == 0 else 2 * p.info["chunks"]):
+            lo, hi = p.range(b, slot)
+            assert (lo % 128 == 0 or lo == L) and (hi % 128 == 0 or hi == L)
+
+
 def test_fp8_kv_plan_rules():
     p = fd.fd_plan(1, 32, 8, 128, [4096], 4, "f16_e4m3kv", num_sms=152)
     assert p.info["path"] == 2 and p.info["kv_bytes"] == 4096 * 8 * 128 * 2
@@ -220,7 +244,7 @@ def test_fp8_kv_plan_rules():
 
 
 def test_combine_scratch_limit():
-    # The combine's coefficient scratch, (G * partials + 2 G) * 4 bytes, must fit the ring
+    # The combine's coefficient scratch, (G * partials + 3 G) * 4 bytes, must fit the ring
     # it reuses; with a 96 KB ring even G = 16 with 1024 partials fits (66 KB), for the
     # fine-grained-waits variant too.
     fd.fd_plan(1, 128, 8, 64, [100000], 1024, "f16", flags=fd.FD_PLAN_LITERAL_W, num_sms=152)

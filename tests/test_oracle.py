@@ -307,9 +307,28 @@ def check_bf16_bit_patterns():
             and abs(l[0, 0] - math.log(L)) <= TOL and abs(l2[0, 0] - math.log(L)) <= TOL)
 
 
+def check_f16_bit_patterns():
+    """fp16 inputs given as bit patterns of known values (IEEE binary16): 0x3C00 = 1,
+    0xC000 = -2, 0x0001 = 2^-24 (smallest subnormal), 0x7BFF = 65504 (largest finite)."""
+    vals = {0x3C00: 1.0, 0xC000: -2.0, 0x0001: 2.0 ** -24, 0x7BFF: 65504.0}
+    bits = np.array(list(vals), dtype=np.uint16)
+    if not np.array_equal(oracle.widen(bits.view(np.float16), "f16"), np.array(list(vals.values()))):
+        return False
+    L, d = 4, 4
+    q = np.zeros((1, 1, d), dtype=np.float16)
+    k = np.zeros((L, 1, d), dtype=np.float16)
+    v = np.stack([np.roll(bits, j) for j in range(L)])[:, None, :].view(np.float16)
+    o, l = oracle.decode_reference(q, k, v, [L], dtype="f16")
+    o2, l2, _ = oracle.split_kv_decode(q, k, v, [L], 3, dtype="f16")
+    mean = (1.0 - 2.0 + 2.0 ** -24 + 65504.0) / L                  # exact in float64
+    return (np.array_equal(o, np.full((1, 1, d), mean)) and _close(o2, np.full((1, 1, d), mean))
+            and abs(l[0, 0] - math.log(L)) <= TOL and abs(l2[0, 0] - math.log(L)) <= TOL)
+
+
 PINS = {
     "golden": check_golden,
     "bf16_bit_patterns": check_bf16_bit_patterns,
+    "f16_bit_patterns": check_f16_bit_patterns,
     "brute_force": check_brute_force,
     "split_matches_definition": check_split_matches_definition,
     "permutation_invariance": check_permutation_invariance,

@@ -249,17 +249,19 @@ def gqa4_d128_L32k_W8(seed: int = 1001) -> DecodeProblem:
     return make_problem("gqa4_d128_L32k_W8", 1, 32, 8, 128, [32768], 8, F16, seed)
 
 
-def gqa8_d128_L128k_W8_spiky(seed: int = 1002) -> DecodeProblem:
+def gqa8_d128_L128k_W8_spiky(seed: int = 1002, dtype: str = F16) -> DecodeProblem:
     """B=1, Hq=64 / Hkv=8, d=128, L=131072, W=8; fp16 N(0,1) with 0.1% of key rows x20.
 
     round(0.001 * L) = 131 token positions are drawn without replacement from
     their own stream; every KV head of K at those positions is multiplied by 20
-    in float32 before rounding once to fp16.  V is untouched.
+    in float32 before rounding once to fp16.  V is untouched.  ``dtype="bf16"``
+    gives the same draw rounded to bf16 instead (not one of the five cases).
     """
     L = 131072
     n_spike = int(round(0.001 * L))
     rows = rng(seed, _STREAM_SPIKE).choice(L, size=n_spike, replace=False)
-    return make_problem("gqa8_d128_L128k_W8_spiky", 1, 64, 8, 128, [L], 8, F16, seed,
+    name = "gqa8_d128_L128k_W8_spiky" + ("" if dtype == F16 else "_" + dtype)
+    return make_problem(name, 1, 64, 8, 128, [L], 8, dtype, seed,
                         k_spike_rows=rows, k_spike_factor=20.0,
                         notes={"k_spike_rows": n_spike, "k_spike_factor": 20.0})
 
