@@ -59,6 +59,8 @@ def parse_args(argv=None):
     ap.add_argument("--two-launch", action="store_true", help="split + combine as two kernels")
     ap.add_argument("--ffma", action="store_true", help="CUDA-core consumers even when G >= 4")
     ap.add_argument("--tcgen05", action="store_true", help="tcgen05 tensor cores (d = 128, G >= 4)")
+    ap.add_argument("--cluster-combine", action="store_true",
+                    help="combine each (sequence, KV head) pair inside one thread-block cluster")
     ap.add_argument("--no-pdl", action="store_true", help="launch without programmatic dependent launch")
     ap.add_argument("--no-cluster", action="store_true",
                     help="one partial record per chunk (no in-cluster segment merge)")
@@ -412,7 +414,8 @@ def plan_flags(fd, args, prob):
         fd.FD_PLAN_TWO_LAUNCH if args.two_launch else 0) | (fd.FD_PLAN_FFMA if args.ffma else 0) | (
         fd.FD_PLAN_NO_PDL if args.no_pdl else 0) | (fd.FD_PLAN_WAITS if args.waits else 0) | (
         fd.FD_PLAN_NO_CLUSTER if args.no_cluster else 0) | (fd.FD_PLAN_CLUSTER if args.cluster else 0) | (
-        fd.FD_PLAN_TCGEN05 if args.tcgen05 else 0)
+        fd.FD_PLAN_TCGEN05 if args.tcgen05 else 0) | (
+        fd.FD_PLAN_CLUSTER_COMBINE if args.cluster_combine else 0)
 
 
 class CaseRun:
@@ -671,7 +674,10 @@ def run_fd(args):
                              else "contiguous [N, Hkv, d]",
                 "combine": "fine-grained waits (slot 0 combines as flags arrive)" if args.waits
                            else ("separate combine kernel" if args.two_launch
-                                 else "last arriver (atomic counter)"),
+                                 else (f"in a cluster of {info['combine_cluster']} CTAs per (sequence,"
+                                       " KV head), distributed shared memory"
+                                       if info["combine_cluster"] else
+                                       "last arriver (atomic counter)")),
                 "consumer": {0: "FFMA (CUDA cores)", 1: "mma.sync m16n8k16 (tensor cores)",
                              2: "mma.sync m16n8k16 over E4M3 K/V widened in registers",
                              3: "tcgen05.mma (accumulators in tensor memory)"}[info["path"]],

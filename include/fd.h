@@ -99,10 +99,25 @@ enum fd_status {
 #define FD_PLAN_TEST_SKIP_TILE 0x200u
 /* Fifth-generation tensor cores (tcgen05.mma with accumulators in tensor memory)
  * for the scores and P.V: 128-token tiles, d = 128, G in {4, 8, 16}, fp16 or bf16
- * (FD_ERR_UNSUPPORTED otherwise).  S^T = K Q^T runs with the tokens on M and the
+ * (FD_ERR_UNSUPPORTED otherwise).  The default for G = 16 at d = 128; this flag
+ * selects it for G = 4 and 8 too.  A kernel with tcgen05 instructions is resident
+ * one CTA per SM, so these plans size their grid for one CTA per SM and give it a
+ * 192 KB K/V ring.  S^T = K Q^T runs with the tokens on M and the
  * heads, padded to 16, on N, straight from the TMA-swizzled K tile; P^T is staged
  * in shared memory; O^T = V^T P^T accumulates in tensor memory. */
 #define FD_PLAN_TCGEN05 0x400u
+/* Combine in a thread-block cluster: the W * C partial CTAs of each (sequence, KV
+ * head) pair run as one cluster (at most 16 CTAs), keep their partials in shared
+ * memory and, after a cluster barrier, each combines its share of the pair's output
+ * columns from all partials through distributed shared memory.  No partial record,
+ * counter or flag touches global memory.  Needs the same W for every sequence and
+ * W <= 16 (FD_ERR_UNSUPPORTED otherwise); the planner caps C at 16 / W.  Not with
+ * FD_PLAN_WAITS, FD_PLAN_TWO_LAUNCH, FD_PLAN_CLUSTER or FD_PLAN_NO_CLUSTER.  A
+ * device that cannot place the clusters makes fd_decode return FD_ERR_UNSUPPORTED. */
+#define FD_PLAN_CLUSTER_COMBINE 0x800u
+/* The mma.sync tensor-core consumers even where tcgen05 is the default (G = 16 at
+ * d = 128).  Not with FD_PLAN_TCGEN05 or FD_PLAN_FFMA. */
+#define FD_PLAN_MMA_SYNC 0x1000u
 
 /* Compiled limits. */
 #define FD_MAX_BATCH 256       /* sequences per plan */
@@ -278,6 +293,8 @@ typedef struct fd_plan_info {
                               2: tensor-core over an E4M3 cache, 3: tcgen05 tensor cores */
   int32_t records_per_segment; /* partial records per segment: 1 (chunks merged in a
                                   cluster) or chunks */
+  int32_t combine_cluster; /* CTAs per cluster that combine a pair's partials in shared
+                              memory (FD_PLAN_CLUSTER_COMBINE: W * chunks), else 0 */
 } fd_plan_info;
 
 int fd_plan_get_info(fd_plan_t plan, fd_plan_info* info);

@@ -32,6 +32,8 @@ from ._binding import (  # noqa: F401
     FD_PLAN_TEST_DROP_FLAG,
     FD_PLAN_TEST_SKIP_TILE,
     FD_PLAN_TCGEN05,
+    FD_PLAN_CLUSTER_COMBINE,
+    FD_PLAN_MMA_SYNC,
     FD_PLAN_WAITS,
     FD_PLAN_TWO_LAUNCH,
     FdError,

@@ -36,6 +36,8 @@ FD_PLAN_NO_CLUSTER = 0x80
 FD_PLAN_CLUSTER = 0x100
 FD_PLAN_TEST_SKIP_TILE = 0x200
 FD_PLAN_TCGEN05 = 0x400
+FD_PLAN_CLUSTER_COMBINE = 0x800
+FD_PLAN_MMA_SYNC = 0x1000
 FD_MAX_BATCH = 256
 FD_MAX_PARTIALS = 1024
 
@@ -65,6 +67,7 @@ class PlanInfo(ctypes.Structure):
         ("total_tokens", ctypes.c_int64), ("total_partials", ctypes.c_int64),
         ("workspace_bytes", ctypes.c_uint64), ("kv_bytes", ctypes.c_uint64),
         ("path", ctypes.c_int32), ("records_per_segment", ctypes.c_int32),
+        ("combine_cluster", ctypes.c_int32),
     ]
 
 

@@ -113,11 +113,15 @@ int plan_impl(int B, int Hq, int Hkv, int d, const int32_t* seqlens, const int32
   if (dtype != FD_F16 && dtype != FD_BF16 && dtype != FD_F16_E4M3KV) return FD_ERR_INVALID;
   if (flags & ~(FD_PLAN_LITERAL_W | FD_PLAN_DEBUG | FD_PLAN_TWO_LAUNCH | FD_PLAN_FFMA |
                 FD_PLAN_NO_PDL | FD_PLAN_WAITS | FD_PLAN_TEST_DROP_FLAG |
-                FD_PLAN_NO_CLUSTER | FD_PLAN_CLUSTER | FD_PLAN_TEST_SKIP_TILE | FD_PLAN_TCGEN05))
+                FD_PLAN_NO_CLUSTER | FD_PLAN_CLUSTER | FD_PLAN_TEST_SKIP_TILE | FD_PLAN_TCGEN05 |
+                FD_PLAN_CLUSTER_COMBINE | FD_PLAN_MMA_SYNC))
     return FD_ERR_INVALID;
   if ((flags & FD_PLAN_CLUSTER) && (flags & (FD_PLAN_NO_CLUSTER | FD_PLAN_WAITS)))
     return FD_ERR_INVALID;
   if ((flags & FD_PLAN_WAITS) && (flags & FD_PLAN_TWO_LAUNCH)) return FD_ERR_INVALID;
+  if ((flags & FD_PLAN_CLUSTER_COMBINE) &&
+      (flags & (FD_PLAN_WAITS | FD_PLAN_TWO_LAUNCH | FD_PLAN_CLUSTER | FD_PLAN_NO_CLUSTER)))
+    return FD_ERR_INVALID;
   if ((flags & FD_PLAN_TEST_DROP_FLAG) && !(flags & FD_PLAN_WAITS)) return FD_ERR_INVALID;
   if ((flags & FD_PLAN_TEST_DROP_FLAG) && (flags & FD_PLAN_TEST_SKIP_TILE)) return FD_ERR_INVALID;
   const int G = Hq / Hkv;
@@ -130,11 +134,17 @@ int plan_impl(int B, int Hq, int Hkv, int d, const int32_t* seqlens, const int32
   if (dtype == FD_F16_E4M3KV && (d != 128 || G < 4 || (flags & FD_PLAN_FFMA)))
     return FD_ERR_UNSUPPORTED;
   if ((flags & FD_PLAN_TCGEN05) &&
-      (dtype == FD_F16_E4M3KV || d != 128 || G < 4 || (flags & FD_PLAN_FFMA)))
+      (dtype == FD_F16_E4M3KV || d != 128 || G < 4 || (flags & (FD_PLAN_FFMA | FD_PLAN_MMA_SYNC))))
     return FD_ERR_UNSUPPORTED;
+  if ((flags & FD_PLAN_MMA_SYNC) && (flags & FD_PLAN_FFMA)) return FD_ERR_INVALID;
   // Tensor cores whenever the GQA group covers at least half of the mma N = 8 tile.
+  // tcgen05 by default where it was measured faster: G = 16 at d = 128 (a 32K decode
+  // in 26.5 us against 27.5 us for two mma.sync N tiles).
+  const bool umma = (flags & FD_PLAN_TCGEN05) ||
+                    (G == 16 && d == 128 && dtype != FD_F16_E4M3KV &&
+                     !(flags & (FD_PLAN_MMA_SYNC | FD_PLAN_FFMA)));
   const int path = dtype == FD_F16_E4M3KV                 ? fd::kPathMmaKv8
-                   : (flags & FD_PLAN_TCGEN05)            ? fd::kPathUmma
+                   : umma                                 ? fd::kPathUmma
                    : (G >= 4 && !(flags & FD_PLAN_FFMA)) ? fd::kPathMma
                                                          : fd::kPathFfma;
 
@@ -148,6 +158,13 @@ int plan_impl(int B, int Hq, int Hkv, int d, const int32_t* seqlens, const int32
     max_w = std::max(max_w, (int)W[b]);
   }
   if (n_tokens >= (int64_t)1 << 31) return FD_ERR_UNSUPPORTED;
+  const bool pair = (flags & FD_PLAN_CLUSTER_COMBINE) != 0;
+  if (pair) {
+    // One cluster per (sequence, KV head): every sequence has the same W.
+    for (int b = 1; b < B; ++b)
+      if (W[b] != W[0]) return FD_ERR_UNSUPPORTED;
+    if (W[0] > fd::kMaxPairCluster) return FD_ERR_UNSUPPORTED;
+  }
 
   if (num_sms == 0) {
     int dev = 0;
@@ -170,8 +187,10 @@ int plan_impl(int B, int Hq, int Hkv, int d, const int32_t* seqlens, const int32
     int64_t c = std::max<int64_t>(1, slots / units);
     const int64_t avg_seg = sum_w > 0 ? n_tokens / sum_w : 0;
     c = std::min<int64_t>(c, std::max<int64_t>(1, avg_seg / kMinChunkTokens));
+    if (pair) c = std::min<int64_t>(c, fd::kMaxPairCluster / W[0]);
     C = (int)c;
   }
+  if (pair && (int64_t)W[0] * C > fd::kMaxPairCluster) return FD_ERR_UNSUPPORTED;
   if ((int64_t)max_w * C > FD_MAX_PARTIALS) return FD_ERR_UNSUPPORTED;
   {
     // The combine's shared-memory scratch must fit in the ring it reuses.
@@ -218,7 +237,8 @@ int plan_impl(int B, int Hq, int Hkv, int d, const int32_t* seqlens, const int32
   const int64_t ring = (int64_t)fd::ring_bytes_for(pl->path, d);
   const bool multi_pass = rec_bytes > (pl->path == fd::kPathMmaKv8 ? 2 : 1) * ring;
   p.rps = ((multi_pass || (flags & FD_PLAN_CLUSTER)) && C > 1 && C <= kMaxCluster &&
-           !(flags & (FD_PLAN_WAITS | FD_PLAN_NO_CLUSTER))) ? 1 : C;
+           !(flags & (FD_PLAN_WAITS | FD_PLAN_NO_CLUSTER | FD_PLAN_CLUSTER_COMBINE))) ? 1 : C;
+  p.pair_cluster = pair ? W[0] * C : 0;
   // Paged caches: boundaries on whole tiles, so that every TMA box stays in one page.
   p.align = page_size ? fd::tile_for(pl->path) : 1;
   p.box_rows = page_size ? std::min(fd::tile_for(pl->path), page_size) : fd::tile_for(pl->path);
@@ -283,6 +303,7 @@ int fd_plan_get_info(fd_plan_t pl, fd_plan_info* info) {
   info->kv_bytes = (uint64_t)pl->n_tokens * pl->Hkv * pl->d * 2 * fd::kv_elem_bytes(pl->path);
   info->path = pl->path;
   info->records_per_segment = pl->params.rps;
+  info->combine_cluster = pl->params.pair_cluster;
   return FD_OK;
 }
 
@@ -372,11 +393,11 @@ int decode_impl(fd_plan_t pl, const void* q, const void* k, const void* v, int64
     err = launch(pl, p, 1, pl->ctas, stream);
     if (err == cudaSuccess) err = launch(pl, p, 2, pl->B * pl->Hkv, stream);
   } else {
-    err = launch(pl, p, (pl->flags & FD_PLAN_WAITS) ? 3 : 0, pl->ctas, stream);
+    err = launch(pl, p, fd::fused_mode(pl), pl->ctas, stream);
   }
   if (err != cudaSuccess) {
     cudaGetLastError();
-    return err == cudaErrorCooperativeLaunchTooLarge ? FD_ERR_UNSUPPORTED : FD_ERR_CUDA;
+    return fd::launch_status(err);
   }
   if (debug) {
     int32_t st = FD_OK;

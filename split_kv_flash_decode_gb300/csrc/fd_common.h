@@ -89,6 +89,10 @@ FD_HD constexpr size_t smem_bytes_for(int path, int d) {
 // of V rows under those weights).  Without rounding (CUDA-core path) l~ = l.
 FD_HD constexpr int record_floats(int d) { return d + 4; }
 
+// Largest cluster of the pair-cluster combine (FD_PLAN_CLUSTER_COMBINE): the
+// non-portable cluster size limit.
+constexpr int kMaxPairCluster = 16;
+
 // Status word values written by the kernels (the host maps them to fd_status).
 constexpr uint32_t kStatusTimeout = 1u;
 constexpr uint32_t kStatusCounter = 2u;
@@ -125,6 +129,9 @@ struct Params {
   // Partial records per segment: C, or 1 when the C chunk CTAs of a segment form a
   // thread-block cluster and merge their partials through distributed shared memory.
   int32_t rps;
+  // CTAs per cluster when every partial of a (sequence, KV head) pair forms one
+  // cluster and combines there (kernel mode 6): W * C, equal for every sequence.
+  int32_t pair_cluster;
   float scale_log2;    // log2(e) / sqrt(d)
   int32_t B, Hq, Hkv, C;
   int32_t cu[FD_MAX_BATCH + 1];         // token prefix sums
@@ -156,7 +163,8 @@ FD_HD void chunk_range(int L, int W, int C, int slot, int align, int* t0, int* t
 // Launchers defined in the per-dtype kernel translation units.
 // mode 0: fused split + last-arriver combine; 1: split only (partials); 2: combine only;
 // 3: fused split + fine-grained waits (slot 0 combines partials as their flags arrive;
-//    cooperative launch).
+//    cooperative launch); 6: fused, every partial of a (sequence, KV head) pair in one
+//    thread-block cluster, combined through distributed shared memory.
 // pdl: launch with programmatic stream serialization (the kernel waits on its
 // predecessors with griddepcontrol.wait before touching global memory).
 cudaError_t launch_f16(const Params& p, int d, int G, int path, int mode, bool pdl, int grid,

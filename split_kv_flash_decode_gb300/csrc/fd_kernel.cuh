@@ -144,6 +144,13 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map
       : "memory");
 }
 
+// Load through L2 only (no L1 line is allocated).
+__device__ __forceinline__ int32_t ld_cg_s32(const int32_t* addr) {
+  int32_t v;
+  asm volatile("ld.global.cg.s32 %0, [%1];" : "=r"(v) : "l"(addr));
+  return v;
+}
+
 __device__ __forceinline__ uint32_t atom_add_acq_rel_gpu(uint32_t* addr, uint32_t v) {
   uint32_t old;
   asm volatile("atom.add.acq_rel.gpu.global.u32 %0, [%1], %2;"
@@ -300,22 +307,34 @@ __device__ __forceinline__ int flag_index(const Params& p, int b, int kvh, int s
   return p.unit_base[b] + kvh * p.wseg[b] * p.C + slot;
 }
 
-// `seg`: the plan merges each segment's chunks in a cluster (rps == 1 < C).
-__device__ __forceinline__ Work decode_work(const Params& p, int cta, bool seg) {
+// CTA orders within a sequence.  kOrderHeads: KV head fastest, then partial slot.
+// kOrderSegment (chunks of a segment merge in a cluster): chunk fastest, then KV
+// head, then segment, so that the C chunks of one segment are consecutive (one
+// cluster).  kOrderPair (every partial of a (sequence, KV head) in one cluster):
+// partial slot fastest, then KV head.
+constexpr int kOrderHeads = 0;
+constexpr int kOrderSegment = 1;
+constexpr int kOrderPair = 2;
+
+__device__ __forceinline__ Work decode_work(const Params& p, int cta, int order) {
+  const bool seg = order == kOrderSegment;
   int lo = 0, hi = p.B;
   while (hi - lo > 1) {
     const int mid = (lo + hi) >> 1;
     if (p.unit_base[mid] <= cta) lo = mid; else hi = mid;
   }
-  // CTA order within a sequence: KV head fastest, then partial slot; with the
-  // segment merge, chunk fastest, then KV head, then segment, so that the C chunks
-  // of one segment are consecutive (one cluster).
   Work w;
   w.b = lo;
   const int r = cta - p.unit_base[lo];
-  if (!seg) {
+  if (order == kOrderHeads) {
     w.kvh = r % p.Hkv;
     w.slot = r / p.Hkv;
+    w.w = w.slot / p.C;
+    w.c = w.slot - w.w * p.C;
+  } else if (order == kOrderPair) {
+    const int wc = p.wseg[lo] * p.C;
+    w.kvh = r / wc;
+    w.slot = r - w.kvh * wc;
     w.w = w.slot / p.C;
     w.c = w.slot - w.w * p.C;
   } else {
@@ -416,75 +435,76 @@ __device__ __forceinline__ float warp_sum(float x) {
 
 // OnlineSoftmaxCombine of the Wtot partials of (b, kvh) for query heads
 // [g0, g0 + ng), from their records in shared memory, head-major
-// [ng][wtot][D + 4].  One warp per head: M is the max of the partial maxima,
-// Lambda = sum_w exp2(m_w - M) l_w, O = sum_w exp2(m_w - M) O_w; lane l owns the
-// D/32 output dimensions starting at (D/32) l, and receives each coefficient by
-// shuffle from the lane that computed it.  out = O / Lambda~, where Lambda~ sums
-// the records' rounded-weight sums the same way (the weights P.V multiplied);
-// lse = M + log Lambda.  The order of every sum is fixed (partial index order for
-// O, a fixed shuffle tree for the Lambdas), so the result does not depend on the
-// order in which the partials arrived.
+// [ng][wtot][D + 4].  Two phases over all threads.  (1) One warp per head: M is the
+// max of the partial maxima, each lane computes the coefficients exp2(m_w - M) of
+// its partials into `coef` ([ng][wtot] after the records), and Lambda =
+// sum_w coef_w l_w and Lambda~ = sum_w coef_w l~_w go through a fixed shuffle tree.
+// (2) Every thread owns one (head, 4 output dimensions) slice and sums
+// coef_w O_w over the partials in index order, its loads independent of each
+// other.  out = O / Lambda~ (the weights P.V multiplied), lse = M + log Lambda.  The
+// order of every sum is fixed, so the result does not depend on the order in which
+// the partials arrived.
 template <typename T, int D, int G>
 __device__ __forceinline__ void combine_from_smem(const Params& p, int b, int kvh, int wtot,
-                                                  int g0, int ng, const float* rec) {
+                                                  int g0, int ng, const float* rec, float* coef) {
   constexpr int RS = record_floats(D);
-  constexpr int V = D / 32;  // 4 (d = 128) or 2 (d = 64)
-  static_assert(V == 2 || V == 4, "head dim must be 64 or 128");
-  constexpr int U = 8;       // records in flight per lane
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  constexpr int Q = D / 4;   // float4 columns per head
+  constexpr int U = 8;       // partials in flight per thread
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   constexpr int kWarps = kThreads / 32;
-  T* out = reinterpret_cast<T*>(p.out);
+  float* lams = coef + (size_t)ng * wtot;  // [ng][2]: Lambda, Lambda~
   for (int g = warp; g < ng; g += kWarps) {
-    const float* rg = rec + (size_t)g * wtot * RS;
+    const float* rg = rec + (size_t)g * wtot * RS + D;
     float M = -INFINITY;
-    for (int w = lane; w < wtot; w += 32) M = fmaxf(M, rg[(size_t)w * RS + D]);
+    for (int w = lane; w < wtot; w += 32) M = fmaxf(M, rg[(size_t)w * RS]);
     M = warp_max(M);
     float lam = 0.f, lamr = 0.f;
-    float acc[V];
-#pragma unroll
-    for (int j = 0; j < V; ++j) acc[j] = 0.f;
-    for (int w0 = 0; w0 < wtot; w0 += 32) {
-      const int n = min(32, wtot - w0);
-      float cl = 0.f;
-      if (lane < n && M != -INFINITY) {
-        const float4 ml = *reinterpret_cast<const float4*>(rg + (size_t)(w0 + lane) * RS + D);
-        cl = ex2(ml.x - M);  // exp2(-inf) = 0 for an empty partial
-        lam = fmaf(cl, ml.y, lam);
-        lamr = fmaf(cl, ml.z, lamr);
-      }
-      const float* base = rg + (size_t)w0 * RS + V * lane;
-      int i = 0;
-      for (; i + U <= n; i += U) {
-        float x[U][V], c[U];
-#pragma unroll
-        for (int u = 0; u < U; ++u) {
-          if constexpr (V == 4) {
-            const float4 t = *reinterpret_cast<const float4*>(base + (size_t)(i + u) * RS);
-            x[u][0] = t.x; x[u][1] = t.y; x[u][2] = t.z; x[u][3] = t.w;
-          } else {
-            const float2 t = *reinterpret_cast<const float2*>(base + (size_t)(i + u) * RS);
-            x[u][0] = t.x; x[u][1] = t.y;
-          }
-          c[u] = __shfl_sync(0xffffffffu, cl, i + u);
-        }
-#pragma unroll
-        for (int u = 0; u < U; ++u)
-#pragma unroll
-          for (int j = 0; j < V; ++j) acc[j] = fmaf(c[u], x[u][j], acc[j]);
-      }
-      for (; i < n; ++i) {
-        const float c = __shfl_sync(0xffffffffu, cl, i);
-#pragma unroll
-        for (int j = 0; j < V; ++j) acc[j] = fmaf(c, base[(size_t)i * RS + j], acc[j]);
-      }
+    for (int w = lane; w < wtot; w += 32) {
+      const float4 ml = *reinterpret_cast<const float4*>(rg + (size_t)w * RS);
+      const float c = M == -INFINITY ? 0.f : ex2(ml.x - M);  // exp2(-inf) = 0: empty partial
+      coef[(size_t)g * wtot + w] = c;
+      lam = fmaf(c, ml.y, lam);
+      lamr = fmaf(c, ml.z, lamr);
     }
     lam = warp_sum(lam);
     lamr = warp_sum(lamr);
-    T* dst = out + ((int64_t)b * p.Hq + kvh * G + g0 + g) * D + V * lane;
+    if (lane == 0) {
+      lams[2 * g] = lam;
+      lams[2 * g + 1] = lamr;
+      if (p.lse != nullptr)
+        p.lse[(int64_t)b * p.Hq + kvh * G + g0 + g] = lam > 0.f ? (M + log2f(lam)) * kLn2 : -INFINITY;
+    }
+  }
+  __syncthreads();
+  T* out = reinterpret_cast<T*>(p.out);
+  for (int i = tid; i < ng * Q; i += kThreads) {
+    const int g = i / Q, c4 = i - (i / Q) * Q;
+    const float* base = rec + (size_t)g * wtot * RS + 4 * c4;
+    const float* cg = coef + (size_t)g * wtot;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    int w = 0;
+    for (; w + U <= wtot; w += U) {
+      float4 x[U];
 #pragma unroll
-    for (int j = 0; j < V; ++j) dst[j] = Elem<T>::from_f(lamr > 0.f ? acc[j] / lamr : 0.f);
-    if (lane == 0 && p.lse != nullptr)
-      p.lse[(int64_t)b * p.Hq + kvh * G + g0 + g] = lam > 0.f ? (M + log2f(lam)) * kLn2 : -INFINITY;
+      for (int u = 0; u < U; ++u) x[u] = *reinterpret_cast<const float4*>(base + (size_t)(w + u) * RS);
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const float c = cg[w + u];
+        acc.x = fmaf(c, x[u].x, acc.x);
+        acc.y = fmaf(c, x[u].y, acc.y);
+        acc.z = fmaf(c, x[u].z, acc.z);
+        acc.w = fmaf(c, x[u].w, acc.w);
+      }
+    }
+    for (; w < wtot; ++w) {
+      const float4 x = *reinterpret_cast<const float4*>(base + (size_t)w * RS);
+      const float c = cg[w];
+      acc.x = fmaf(c, x.x, acc.x);
+      acc.y = fmaf(c, x.y, acc.y);
+      acc.z = fmaf(c, x.z, acc.z);
+      acc.w = fmaf(c, x.w, acc.w);
+    }
+    store_out4<T>(out + ((int64_t)b * p.Hq + kvh * G + g0 + g) * D + 4 * c4, acc, lams[2 * g + 1]);
   }
 }
 
@@ -566,8 +586,10 @@ __device__ __forceinline__ void combine_partials(const Params& p, int b, int kvh
                                                  int64_t pbase, uint8_t* smem, uint32_t smem_bytes,
                                                  uint32_t bar, uint32_t& phase) {
   constexpr int RS = record_floats(D);
+  // Per head: its records, plus its coefficients and two Lambdas (phase 1 scratch).
   const uint32_t head_bytes = (uint32_t)wtot * RS * 4;
-  const int hpp = head_bytes > 0 ? (int)min((uint32_t)G, smem_bytes / head_bytes) : 0;
+  const uint32_t head_need = head_bytes + (uint32_t)(wtot + 2) * 4;
+  const int hpp = head_bytes > 0 ? (int)min((uint32_t)G, smem_bytes / head_need) : 0;
   if (hpp == 0) {
     combine_from_global<T, D, G>(p, b, kvh, wtot, pbase, reinterpret_cast<float*>(smem));
     return;
@@ -587,7 +609,8 @@ __device__ __forceinline__ void combine_partials(const Params& p, int b, int kvh
     }
     if (!mbar_wait(bar, phase)) atomicOr(p.status, kStatusTimeout);
     phase ^= 1u;
-    combine_from_smem<T, D, G>(p, b, kvh, wtot, g0, ng, rec);
+    combine_from_smem<T, D, G>(p, b, kvh, wtot, g0, ng, rec,
+                               rec + (size_t)ng * wtot * RS);
     __syncthreads();  // the next pass overwrites the records
   }
 }
@@ -760,6 +783,80 @@ __device__ __forceinline__ void merge_segment(const Params& p, const Work& wk, c
   cluster_arrive();  // done reading the other CTAs' shared memory
 }
 
+// OnlineSoftmaxCombine of all Wtot partials of (b, kvh) inside one thread-block
+// cluster (the Wtot CTAs of the pair, cluster rank = partial slot): every CTA holds
+// its record in shared memory (`crec`, [G][D + 4]); after a cluster barrier each CTA
+// reads the (m, l, l~) of all records through distributed shared memory, then
+// combines its share of the G x D output columns from all Wtot records, in slot
+// order, and writes out (CTA 0 also writes lse).  No global records, no counter.
+// A closing cluster barrier keeps every CTA alive until no peer reads its shared
+// memory.  `cf` is scratch for G * (Wtot + 3) floats.
+template <typename T, int D, int G>
+__device__ __forceinline__ void combine_in_cluster(const Params& p, const Work& wk, const float* crec,
+                                                   float* cf) {
+  constexpr int RS = record_floats(D);
+  constexpr int kMaxCluster = 16;
+  const int tid = threadIdx.x, CS = wk.wtot;
+  cluster_arrive();
+  cluster_wait();  // every record of the pair is in place
+  const uint32_t crec_a = smem_addr(crec);
+  if (tid < G) {
+    const uint32_t ml_a = crec_a + (uint32_t)(tid * RS + D) * 4u;
+    float4 ml[kMaxCluster];
+#pragma unroll
+    for (int j = 0; j < kMaxCluster; ++j)
+      if (j < CS) ml[j] = ld_cluster_f4(cluster_map(ml_a, j));
+    float M = -INFINITY;
+#pragma unroll
+    for (int j = 0; j < kMaxCluster; ++j)
+      if (j < CS) M = fmaxf(M, ml[j].x);
+    float lam = 0.f, lamr = 0.f;
+#pragma unroll
+    for (int j = 0; j < kMaxCluster; ++j) {
+      if (j < CS) {
+        const float f = (M == -INFINITY) ? 0.f : ex2(ml[j].x - M);  // an empty partial has m = -inf
+        cf[tid * CS + j] = f;
+        lam = fmaf(f, ml[j].y, lam);
+        lamr = fmaf(f, ml[j].z, lamr);
+      }
+    }
+    cf[G * CS + tid] = M;
+    cf[G * CS + G + tid] = lam;
+    cf[G * CS + 2 * G + tid] = lamr;
+  }
+  __syncthreads();
+  constexpr int Q = D / 4;
+  const int n = G * Q, lo = wk.slot * n / CS, hi = (wk.slot + 1) * n / CS;
+  T* out = reinterpret_cast<T*>(p.out);
+  for (int i = lo + tid; i < hi; i += kThreads) {
+    const int g = i / Q, c4 = i - (i / Q) * Q;
+    const uint32_t src = crec_a + (uint32_t)(g * RS + 4 * c4) * 4u;
+    float4 x[kMaxCluster];
+#pragma unroll
+    for (int j = 0; j < kMaxCluster; ++j)
+      if (j < CS) x[j] = ld_cluster_f4(cluster_map(src, j));
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int j = 0; j < kMaxCluster; ++j) {
+      if (j < CS) {
+        const float f = cf[g * CS + j];
+        acc.x = fmaf(f, x[j].x, acc.x);
+        acc.y = fmaf(f, x[j].y, acc.y);
+        acc.z = fmaf(f, x[j].z, acc.z);
+        acc.w = fmaf(f, x[j].w, acc.w);
+      }
+    }
+    store_out4<T>(out + ((int64_t)wk.b * p.Hq + wk.kvh * G + g) * D + 4 * c4, acc,
+                  cf[G * CS + 2 * G + g]);
+  }
+  if (wk.slot == 0 && tid < G && p.lse != nullptr) {
+    const float M = cf[G * CS + tid], lam = cf[G * CS + G + tid];
+    p.lse[(int64_t)wk.b * p.Hq + wk.kvh * G + tid] = lam > 0.f ? (M + log2f(lam)) * kLn2 : -INFINITY;
+  }
+  cluster_arrive();  // done reading the other CTAs' shared memory
+  cluster_wait();
+}
+
 // Merge NGRP running states (sm_acc [NGRP][G][D], sm_m / sm_l / sm_lr [NGRP][G],
 // all in shared memory; sm_lr sums the rounded weights P.V used) into this CTA's
 // partial; then either finish directly (a single
@@ -767,7 +864,7 @@ __device__ __forceinline__ void merge_segment(const Params& p, const Work& wk, c
 // rps == 1), arrive, and combine if this CTA arrived last.  An `aborted` CTA (its
 // pipeline timed out; the status word says so) contributes an empty partial so
 // that its cluster and its (b, kvh) counter still complete.
-template <typename T, int D, int G, int NGRP, int MODE, bool SEG>
+template <typename T, int D, int G, int NGRP, int MODE, bool SEG, bool PAIR>
 __device__ __forceinline__ void finish_cta(const Params& p, const Work& wk, float* sm_acc,
                                            int& sm_last, bool aborted, uint8_t* combine_smem,
                                            uint32_t combine_bytes, uint32_t combine_bar) {
@@ -816,8 +913,9 @@ __device__ __forceinline__ void finish_cta(const Params& p, const Work& wk, floa
   // Publish this CTA's partial record (O unnormalised w.r.t. M, then M, Lambda):
   // to global memory, or to `crec` at the end of the ring for the segment merge.
   constexpr int RS = record_floats(D);
-  constexpr bool merge_seg = SEG;
+  constexpr bool merge_seg = SEG || PAIR;  // the record goes to shared memory
   static_assert(!SEG || MODE == 0 || MODE == 1, "segment merge: fused or split-only kernels");
+  static_assert(!PAIR || MODE == 0, "pair clusters: fused kernel");
   const uint32_t crec_bytes = merge_seg ? (uint32_t)(G * RS * 4) : 0u;
   float* crec = reinterpret_cast<float*>(combine_smem + combine_bytes - G * RS * 4);
   for (int idx = tid; idx < G * D / 4; idx += kThreads) {
@@ -848,6 +946,10 @@ __device__ __forceinline__ void finish_cta(const Params& p, const Work& wk, floa
       const int64_t pidx = wk.pbase + (int64_t)(h0 + tid) * wk.nrec + wk.rslot;
       __stcg(reinterpret_cast<float4*>(p.part + pidx * RS + D), ml);
     }
+  }
+  if constexpr (PAIR) {
+    combine_in_cluster<T, D, G>(p, wk, crec, sm_acc);
+    return;
   }
   if (merge_seg) merge_segment<D, G>(p, wk, crec, sm_acc);
   if (MODE == 1) {
@@ -889,10 +991,13 @@ __device__ __forceinline__ void finish_cta(const Params& p, const Work& wk, floa
 // MODE 0: fused split + last-arriver combine.  MODE 1: split only (partials).
 // MODE 3: fused split + fine-grained waits.  MODE 4 / 5: MODE 0 / 1 with each
 // segment's chunk partials merged inside a thread-block cluster (rps == 1).
+// MODE 6: fused, every partial of a (sequence, KV head) in one thread-block cluster
+// that combines them through distributed shared memory.
 template <typename T, int D, int G, int PATH, int MODE>
 __global__ void __launch_bounds__(kThreads, 2) fd_split_kernel(const __grid_constant__ Params p) {
-  constexpr bool kSeg = MODE >= 4;
-  constexpr int kMode = kSeg ? MODE - 4 : MODE;
+  constexpr bool kSeg = MODE == 4 || MODE == 5;
+  constexpr bool kPair = MODE == 6;
+  constexpr int kMode = kSeg ? MODE - 4 : kPair ? 0 : MODE;
   constexpr int TILE = tile_for(PATH);
   constexpr int LPT = loads_per_tile(PATH);       // ring slots per tile (2: K and V apart)
   constexpr int NSLOT = ring_slots_for(PATH, D);  // ring slots
@@ -928,7 +1033,7 @@ __global__ void __launch_bounds__(kThreads, 2) fd_split_kernel(const __grid_cons
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   pdl_launch_dependents();
   // Prologue that touches no global memory: it may overlap the previous kernel.
-  const Work wk = decode_work(p, blockIdx.x, kSeg);
+  const Work wk = decode_work(p, blockIdx.x, kSeg ? kOrderSegment : kPair ? kOrderPair : kOrderHeads);
   const int ntiles = (wk.t1 - wk.t0 + TILE - 1) / TILE;
   if (tid == 0) {
     for (int s = 0; s < NSLOT; ++s) {
@@ -958,17 +1063,41 @@ __global__ void __launch_bounds__(kThreads, 2) fd_split_kernel(const __grid_cons
     // Warm L2 with the first tiles of the chunk while the previous kernel drains
     // (its combine tail leaves HBM idle).  An L2 prefetch hands no data to this
     // SM, and L2 is where every global write becomes visible, so it cannot expose
-    // K/V that the previous kernel is still writing.  The paged layout would have
-    // to read the block table first, which may be such a write: it skips this.
-    // So do CTAs past the first wave, which start after the previous kernel.
-    if (p.block_table == nullptr && (int)blockIdx.x < p.prefetch_ctas) {
-      const int row0 = p.cu[wk.b] + wk.t0;
+    // K/V that the previous kernel is still writing.  CTAs past the first wave,
+    // which start after the previous kernel, skip it.
+    if ((int)blockIdx.x < p.prefetch_ctas) {
       const int npf = min(ntiles, kL2PrefetchTokens / TILE);
-      for (int kt = 0; kt < npf; ++kt) {
+      if (p.block_table == nullptr) {
+        const int row0 = p.cu[wk.b] + wk.t0;
+        for (int kt = 0; kt < npf; ++kt) {
 #pragma unroll
-        for (int bx = 0; bx < NBOX; ++bx) {
-          tma_prefetch_l2_3d(&p.tm_k, bx * BOXC, wk.kvh, row0 + kt * TILE);
-          tma_prefetch_l2_3d(&p.tm_v, bx * BOXC, wk.kvh, row0 + kt * TILE);
+          for (int bx = 0; bx < NBOX; ++bx) {
+            tma_prefetch_l2_3d(&p.tm_k, bx * BOXC, wk.kvh, row0 + kt * TILE);
+            tma_prefetch_l2_3d(&p.tm_v, bx * BOXC, wk.kvh, row0 + kt * TILE);
+          }
+        }
+      } else if (p.box_rows == TILE) {
+        // Paged (pages of at least one tile; smaller pages would need many small
+        // prefetches, which measured slower): the block table may itself be written
+        // by the previous kernel, so these entries are only a guess (read through
+        // L2, leaving no L1 line that the loads after the wait could hit).  A wrong
+        // page costs bandwidth, never
+        // correctness: the loads re-read the table after the wait, and a prefetch
+        // outside the pool fetches nothing.
+        const int32_t* bt = p.block_table + (int64_t)wk.b * p.bt_stride;
+        const int last_pg = (p.cu[wk.b + 1] - p.cu[wk.b] - 1) >> p.page_shift;
+        for (int kt = 0; kt < npf; ++kt) {
+          const int a = wk.t0 + kt * TILE;
+          for (int r = 0; r < TILE; r += p.box_rows) {
+            const int pg = ld_cg_s32(bt + min((a + r) >> p.page_shift, last_pg));
+            if (pg < 0 || pg > (0x3fffffff >> p.page_shift)) continue;
+            const int row = pg * (1 << p.page_shift) + ((a + r) & ((1 << p.page_shift) - 1));
+#pragma unroll
+            for (int bx = 0; bx < NBOX; ++bx) {
+              tma_prefetch_l2_3d(&p.tm_k, bx * BOXC, wk.kvh, row);
+              tma_prefetch_l2_3d(&p.tm_v, bx * BOXC, wk.kvh, row);
+            }
+          }
         }
       }
     }
@@ -1307,9 +1436,12 @@ __global__ void __launch_bounds__(kThreads, 2) fd_split_kernel(const __grid_cons
             kw[rh][grp] = *reinterpret_cast<const uint4*>(
                 smem + (size_t)s * kSlotBytes + r * 128 + ((c ^ (r & 7)) << 4));
           }
-        float sc[NT][4];
+        // Two accumulators (even and odd k-steps) halve the chain of dependent mma.
+        float sc[NT][4], sd[NT][4];
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt) sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+          for (int i = 0; i < 4; ++i) sc[nt][i] = sd[nt][i] = 0.f;
 #pragma unroll
         for (int kk = 0; kk < KT; ++kk) {
           const uint4& w0 = kw[0][kk >> 2];
@@ -1323,8 +1455,13 @@ __global__ void __launch_bounds__(kThreads, 2) fd_split_kernel(const __grid_cons
           a[2] = e4m3x2_to_f16x2_scaled(x0, 0u, 0xB3A2u);  // bytes 2, 3
           a[3] = e4m3x2_to_f16x2_scaled(x1, 0u, 0xB3A2u);
 #pragma unroll
-          for (int nt = 0; nt < NT; ++nt) mma16816<T>(sc[nt], a, qb[nt][kk][0], qb[nt][kk][1]);
+          for (int nt = 0; nt < NT; ++nt)
+            mma16816<T>((kk & 1) ? sd[nt] : sc[nt], a, qb[nt][kk][0], qb[nt][kk][1]);
         }
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+          for (int i = 0; i < 4; ++i) sc[nt][i] += sd[nt][i];
         const bool v0 = tok0 + g < ntok, v1 = tok0 + g + 8 < ntok;
         uint32_t pb0[NT], pb1[NT];
 #pragma unroll
@@ -1485,16 +1622,24 @@ __global__ void __launch_bounds__(kThreads, 2) fd_split_kernel(const __grid_cons
       if (tok0 < ntok) {
         const uint32_t kbase = smem_addr(smem + (size_t)s * kSlotBytes);
         const uint32_t vbase = kbase + kRowsBytes;
-        float sc[NT][4];
+        // Two accumulators (even and odd k-steps) halve the chain of dependent mma.
+        float sc[NT][4], sd[NT][4];
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt) sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+          for (int i = 0; i < 4; ++i) sc[nt][i] = sd[nt][i] = 0.f;
 #pragma unroll
         for (int kk = 0; kk < KT; ++kk) {
           uint32_t a[4];
           ldmatrix_x4(a, swz_addr(kbase, TILE, krow, 2 * kk + (mj >> 1)));
 #pragma unroll
-          for (int nt = 0; nt < NT; ++nt) mma16816<T>(sc[nt], a, qb[nt][kk][0], qb[nt][kk][1]);
+          for (int nt = 0; nt < NT; ++nt)
+            mma16816<T>((kk & 1) ? sd[nt] : sc[nt], a, qb[nt][kk][0], qb[nt][kk][1]);
         }
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+          for (int i = 0; i < 4; ++i) sc[nt][i] += sd[nt][i];
         const bool v0 = tok0 + qrow < ntok, v1 = tok0 + qrow + 8 < ntok;
         uint32_t pb0[NT], pb1[NT];
 #pragma unroll
@@ -1731,7 +1876,7 @@ __global__ void __launch_bounds__(kThreads, 2) fd_split_kernel(const __grid_cons
   // A CTA whose pipeline gave up (the status word says so) still finishes, with an
   // empty partial: its (sequence, KV head) counter must complete and return to zero,
   // and a CTA of a cluster must still reach the cluster barriers.
-  finish_cta<T, D, G, NGRP, kMode, kSeg>(p, wk, sm_acc, sm_last, sm_abort != 0, smem, kRing,
+  finish_cta<T, D, G, NGRP, kMode, kSeg, kPair>(p, wk, sm_acc, sm_last, sm_abort != 0, smem, kRing,
                                          smem_addr(bars + 2 * NSLOT));
 }
 
@@ -1763,6 +1908,8 @@ cudaError_t launch_dgp(const Params& p, int mode, bool pdl, int grid, cudaStream
   const size_t smem = smem_bytes_for(PATH, D);
   // The split kernels of plans that merge segments in clusters are separate
   // instantiations (kernel modes 4 and 5).
+  // Mode 6 (every partial of a pair in one cluster) comes from the host; the split
+  // kernels of plans that merge segments in clusters are kernel modes 4 and 5.
   const bool seg = mode <= 1 && p.rps != p.C;
   const int kmode = seg ? mode + 4 : mode;
   const void* fn;
@@ -1772,16 +1919,20 @@ cudaError_t launch_dgp(const Params& p, int mode, bool pdl, int grid, cudaStream
     case 2: fn = reinterpret_cast<const void*>(&dev::fd_combine_kernel<T, D, G, PATH>); break;
     case 3: fn = reinterpret_cast<const void*>(&dev::fd_split_kernel<T, D, G, PATH, 3>); break;
     case 4: fn = reinterpret_cast<const void*>(&dev::fd_split_kernel<T, D, G, PATH, 4>); break;
-    default: fn = reinterpret_cast<const void*>(&dev::fd_split_kernel<T, D, G, PATH, 5>); break;
+    case 5: fn = reinterpret_cast<const void*>(&dev::fd_split_kernel<T, D, G, PATH, 5>); break;
+    default: fn = reinterpret_cast<const void*>(&dev::fd_split_kernel<T, D, G, PATH, 6>); break;
   }
   int dev_id = 0;
   cudaError_t err = cudaGetDevice(&dev_id);
   if (err != cudaSuccess) return err;
-  // The opt-in shared-memory size is a per-device function attribute.
-  static uint64_t done_mask[6] = {0, 0, 0, 0, 0, 0};
+  // The opt-in shared-memory size (and, for clusters of more than 8 CTAs, the
+  // non-portable cluster size) are per-device function attributes.
+  static uint64_t done_mask[7] = {0, 0, 0, 0, 0, 0, 0};
   const uint64_t bit = 1ull << (dev_id & 63);
   if (!(__atomic_load_n(&done_mask[kmode], __ATOMIC_ACQUIRE) & bit)) {
     err = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (err == cudaSuccess && kmode == 6)
+      err = cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
     if (err != cudaSuccess) return err;
     __atomic_fetch_or(&done_mask[kmode], bit, __ATOMIC_RELEASE);
   }
@@ -1800,10 +1951,11 @@ cudaError_t launch_dgp(const Params& p, int mode, bool pdl, int grid, cudaStream
   } else {
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
-    if (seg) {
-      // The C chunk CTAs of a segment (consecutive block indices) form one cluster.
+    if (seg || kmode == 6) {
+      // The C chunk CTAs of a segment, or all W C partial CTAs of a (sequence, KV
+      // head) pair (consecutive block indices), form one cluster.
       attr[1].id = cudaLaunchAttributeClusterDimension;
-      attr[1].val.clusterDim.x = (unsigned)p.C;
+      attr[1].val.clusterDim.x = (unsigned)(kmode == 6 ? p.pair_cluster : p.C);
       attr[1].val.clusterDim.y = 1;
       attr[1].val.clusterDim.z = 1;
       nattr = 2;

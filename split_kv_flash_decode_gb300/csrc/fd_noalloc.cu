@@ -130,12 +130,12 @@ extern "C" int fd_decode_noalloc(fd_plan_t pl, const void* q, const void* k, con
       err = fd::launch_plan(pl, p, 1, pl->ctas, stream);
       if (err == cudaSuccess) err = fd::launch_plan(pl, p, 2, pl->B * pl->Hkv, stream);
     } else {
-      err = fd::launch_plan(pl, p, (pl->flags & FD_PLAN_WAITS) ? 3 : 0, pl->ctas, stream);
+      err = fd::launch_plan(pl, p, fd::fused_mode(pl), pl->ctas, stream);
     }
   }
   if (err != cudaSuccess) {
     cudaGetLastError();
-    return err == cudaErrorCooperativeLaunchTooLarge ? FD_ERR_UNSUPPORTED : FD_ERR_CUDA;
+    return fd::launch_status(err);
   }
   if (pl->flags & FD_PLAN_DEBUG) {
     int32_t st = FD_OK;

@@ -27,6 +27,19 @@ int encode_kv_map(CUtensorMap* map, const void* base, int64_t rows, int box_rows
 }  // namespace fd
 
 namespace fd {
+// Kernel mode of a one-launch decode: fine-grained waits (3), every partial of a pair
+// in one cluster (6), or the last-arriver combine (0).
+inline int fused_mode(const fd_plan_s* pl) {
+  return (pl->flags & FD_PLAN_WAITS) ? 3 : (pl->flags & FD_PLAN_CLUSTER_COMBINE) ? 6 : 0;
+}
+// fd_status of a failed launch: a grid that cannot be co-resident (cooperative
+// launch) or a cluster the device cannot place is unsupported; anything else is a
+// CUDA failure.
+inline int launch_status(cudaError_t err) {
+  return (err == cudaErrorCooperativeLaunchTooLarge || err == cudaErrorInvalidClusterSize)
+             ? FD_ERR_UNSUPPORTED
+             : FD_ERR_CUDA;
+}
 // One kernel launch of the plan's consumer path and dtype (mode as for launch_f16).
 inline cudaError_t launch_plan(const fd_plan_s* pl, const Params& p, int mode, int grid,
                                cudaStream_t s) {

@@ -207,10 +207,19 @@ def test_consumer_path_choice():
         assert p.info["path"] == path, G
     p = fd.fd_plan(1, 64, 8, 128, [1000], 2, "bf16", flags=fd.FD_PLAN_FFMA, num_sms=152)
     assert p.info["path"] == 0
-    assert fd.fd_plan(1, 128, 8, 128, [1000], 2, "f16", num_sms=152).info["path"] == 1
+    # G = 16: tcgen05 at d = 128 unless mma.sync is asked for; mma.sync at d = 64
+    assert fd.fd_plan(1, 128, 8, 128, [1000], 2, "f16", num_sms=152).info["path"] == 3
+    assert fd.fd_plan(1, 128, 8, 128, [1000], 2, "bf16", flags=fd.FD_PLAN_MMA_SYNC,
+                      num_sms=152).info["path"] == 1
+    assert fd.fd_plan(1, 128, 8, 64, [1000], 2, "f16", num_sms=152).info["path"] == 1
+    assert fd.fd_plan(1, 128, 8, 128, [1000], 2, "f16_e4m3kv", num_sms=152).info["path"] == 2
     with pytest.raises(fd.FdError) as ei:
         fd.fd_plan(1, 128, 8, 128, [1000], 2, "f16", flags=fd.FD_PLAN_FFMA, num_sms=152)
     assert ei.value.status == fd.FD_ERR_UNSUPPORTED
+    assert _raw_plan(1, 32, 8, 128, [10], [1], flags=fd.FD_PLAN_MMA_SYNC | fd.FD_PLAN_FFMA) \
+        == fd.FD_ERR_INVALID
+    assert _raw_plan(1, 32, 8, 128, [10], [1], flags=fd.FD_PLAN_MMA_SYNC | fd.FD_PLAN_TCGEN05) \
+        == fd.FD_ERR_UNSUPPORTED
 
 
 def test_tcgen05_plan_rules():
@@ -232,6 +241,26 @@ def test_tcgen05_plan_rules():
         for slot in range(p.info["max_partials"] if b == 0 else 2 * p.info["chunks"]):
             lo, hi = p.range(b, slot)
             assert (lo % 128 == 0 or lo == L) and (hi % 128 == 0 or hi == L)
+
+
+def test_cluster_combine_plan_rules():
+    """FD_PLAN_CLUSTER_COMBINE: one cluster of W * C <= 16 CTAs per (sequence, KV head)."""
+    p = fd.fd_plan(1, 32, 8, 128, [32768], 8, "f16", flags=fd.FD_PLAN_CLUSTER_COMBINE, num_sms=152)
+    assert p.info["chunks"] == 2 and p.info["combine_cluster"] == 16 and p.info["ctas"] == 128
+    p = fd.fd_plan(64, 32, 8, 128, [8192] * 64, 16, "bf16",
+                   flags=fd.FD_PLAN_CLUSTER_COMBINE | fd.FD_PLAN_LITERAL_W, num_sms=152)
+    assert p.info["combine_cluster"] == 16 and p.info["ctas"] == 8192
+    p = fd.fd_plan(2, 16, 4, 64, [300, 0], 3, "f16", flags=fd.FD_PLAN_CLUSTER_COMBINE, num_sms=152)
+    assert p.info["combine_cluster"] == 3 * p.info["chunks"] <= 16
+    assert fd.fd_plan(1, 32, 8, 128, [1000], 2, "f16", num_sms=152).info["combine_cluster"] == 0
+    for W, chunks in (([4, 5], 0), ([17, 17], 0), ([8, 8], 3)):
+        with pytest.raises(fd.FdError) as ei:      # ragged W, W > 16, W * C > 16
+            fd.fd_plan(2, 32, 8, 128, [4096, 4096], W, "f16", flags=fd.FD_PLAN_CLUSTER_COMBINE,
+                       chunks=chunks, num_sms=152)
+        assert ei.value.status == fd.FD_ERR_UNSUPPORTED
+    for other in (fd.FD_PLAN_WAITS, fd.FD_PLAN_TWO_LAUNCH, fd.FD_PLAN_CLUSTER, fd.FD_PLAN_NO_CLUSTER):
+        assert _raw_plan(1, 8, 8, 128, [10], [1], flags=fd.FD_PLAN_CLUSTER_COMBINE | other) \
+            == fd.FD_ERR_INVALID
 
 
 def test_fp8_kv_plan_rules():

@@ -174,16 +174,18 @@ def test_forced_ffma_path(fd, G):
     check(out, lse, ref_out, ref_lse, dtype=p.dtype)
 
 
-@pytest.mark.parametrize("dtype,d", [("f16", 128), ("bf16", 64)])
+@pytest.mark.parametrize("dtype,d", [("f16", 128), ("bf16", 64), ("bf16", 128)])
 def test_gqa16_tensor_core_path(fd, dtype, d):
-    """G = 16 query heads per KV head: two mma N tiles per KV tile."""
+    """G = 16 query heads per KV head: tcgen05 by default at d = 128, two mma.sync N
+    tiles per KV tile at d = 64 or with FD_PLAN_MMA_SYNC."""
     p = workloads.make_problem("gqa16", 3, 128, 8, d, [9000, 1, 2049], [4, 1, 3], dtype,
                                seed=60 + d)
     ref_out, ref_lse = oracle.decode_reference(p.q, p.k, p.v, p.seqlens, p.dtype)
-    for flags in (0, fd.FD_PLAN_TWO_LAUNCH, fd.FD_PLAN_WAITS):
-        (out, lse), dec = run_gpu(fd, p, flags=flags)
-        assert dec.info["path"] == 1 and dec.info["G"] == 16
-        check(out, lse, ref_out, ref_lse, dtype=p.dtype)
+    for sync in ((False, True) if d == 128 else (False,)):
+        for flags in (0, fd.FD_PLAN_TWO_LAUNCH, fd.FD_PLAN_WAITS):
+            (out, lse), dec = run_gpu(fd, p, flags=flags | (fd.FD_PLAN_MMA_SYNC if sync else 0))
+            assert dec.info["path"] == (3 if d == 128 and not sync else 1) and dec.info["G"] == 16
+            check(out, lse, ref_out, ref_lse, dtype=p.dtype)
 
 
 # ---------------------------------------------------------------------------
@@ -267,6 +269,71 @@ def test_tcgen05_closed_forms(fd):
     for h in range(Hkv * G):
         assert np.abs(out[0, h] - mean[h // G]).max() <= OUT_TOL
     assert np.abs(lse - np.log(L)).max() <= LSE_TOL
+
+
+# ---------------------------------------------------------------------------
+# Combine inside a thread-block cluster per (sequence, KV head) (FD_PLAN_CLUSTER_COMBINE).
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("dtype,G,d,extra", [("f16", 1, 64, 0), ("bf16", 2, 128, 0),
+                                             ("f16", 4, 128, 0), ("bf16", 8, 64, 0),
+                                             ("f16", 16, 128, 0), ("bf16", 4, 128, "tcgen05"),
+                                             ("f16", 16, 128, "tcgen05"), ("f16", 8, 128, "ffma")])
+def test_cluster_combine(fd, dtype, G, d, extra):
+    """Edge lengths, empty sequences, W beyond L and C in {auto, 1, 4}: against the oracle,
+    and bitwise across runs (the combine order inside the cluster is fixed)."""
+    flag = fd.FD_PLAN_CLUSTER_COMBINE | {0: 0, "tcgen05": fd.FD_PLAN_TCGEN05,
+                                         "ffma": fd.FD_PLAN_FFMA}[extra]
+    lens = [1, 2, 127, 128, 129, 0, 1000, 3001, 9000]
+    p = workloads.make_problem("cc", len(lens), 2 * G, 2, d, lens, 4, dtype, seed=130 + G + d)
+    ref_out, ref_lse = oracle.decode_reference(p.q, p.k, p.v, p.seqlens, p.dtype)
+    for chunks in (0, 1, 4):
+        runs, dec = run_gpu(fd, p, chunks=chunks, flags=flag, repeat=2)
+        assert dec.info["combine_cluster"] == 4 * dec.info["chunks"]
+        assert np.array_equal(runs[0][0], runs[1][0]) and np.array_equal(runs[0][1], runs[1][1])
+        check(*runs[0], ref_out, ref_lse, dtype=dtype)
+
+
+@pytest.mark.parametrize("name", ["gqa4_d128_L32k_W8", "gqa8_d128_L128k_W8_spiky",
+                                  "gqa16_d128_L32k_W8", "mha8_d64_L4k_W4"])
+@pytest.mark.parametrize("tcgen05", [False, True])
+def test_cluster_combine_full_cases(fd, name, tcgen05):
+    p = (workloads.CASES.get(name) or workloads.EXTRA[name])()
+    if tcgen05 and p.Hq // p.Hkv < 4:
+        pytest.skip("tcgen05 consumers need G >= 4")
+    flags = fd.FD_PLAN_CLUSTER_COMBINE | (fd.FD_PLAN_TCGEN05 if tcgen05 else 0)
+    (out, lse), dec = run_gpu(fd, p, flags=flags)
+    assert dec.info["combine_cluster"] >= 2
+    ref_out, ref_lse = oracle.decode_reference(p.q, p.k, p.v, p.seqlens, p.dtype)
+    check(out, lse, ref_out, ref_lse)
+
+
+def test_cluster_combine_batch64_w_sweep(fd):
+    """The W sweep of the bf16 batch with clusters of W CTAs: against the oracle, and
+    bitwise across repeats."""
+    p1 = workloads.batch64_gqa4_d128_L8k_bf16(W=1)
+    ref_out, ref_lse = oracle.decode_reference(p1.q, p1.k, p1.v, p1.seqlens, p1.dtype)
+    for W in (2, 16):
+        p = workloads.batch64_gqa4_d128_L8k_bf16(W=W)
+        runs, dec = run_gpu(fd, p, flags=fd.FD_PLAN_CLUSTER_COMBINE, repeat=3)
+        assert dec.info["combine_cluster"] == W
+        for o, l in runs[1:]:
+            assert np.array_equal(o, runs[0][0]) and np.array_equal(l, runs[0][1])
+        check(*runs[0], ref_out, ref_lse)
+
+
+def test_cluster_combine_fp8_and_paged(fd):
+    base = workloads.make_problem("cc8", 3, 64, 8, 128, [7000, 0, 2049], 4, "f16", seed=140)
+    p = workloads.with_e4m3_kv(base)
+    ref_out, ref_lse = reference(p)
+    (out, lse), dec = run_gpu(fd, p, flags=fd.FD_PLAN_CLUSTER_COMBINE)
+    assert dec.info["path"] == 2
+    check(out, lse, ref_out, ref_lse, dtype="f16")
+    q = workloads.make_problem("ccp", 3, 32, 8, 128, [7000, 33, 2049], 4, "bf16", seed=141)
+    ref_out, ref_lse = oracle.decode_reference(q.q, q.k, q.v, q.seqlens, q.dtype)
+    for flags in (fd.FD_PLAN_CLUSTER_COMBINE, fd.FD_PLAN_CLUSTER_COMBINE | fd.FD_PLAN_TCGEN05):
+        out, lse, dec, _ = run_paged(fd, q, 64, flags=flags)
+        check(out, lse, ref_out, ref_lse, dtype="bf16")
 
 
 def test_ragged_with_empty_sequences(fd):
@@ -396,7 +463,8 @@ def test_fine_grained_waits_timeout_is_reported(fd):
 
 
 @pytest.mark.parametrize("G,flags", [(4, 0), (4, "two_launch"), (8, "cluster"), (1, 0),
-                                     (8, "tcgen05"), (16, "tcgen05_cluster")])
+                                     (8, "tcgen05"), (16, "tcgen05_cluster"),
+                                     (4, "cluster_combine")])
 def test_pipeline_wait_timeout_leaves_workspace_clean(fd, G, flags):
     """A tile that is never loaded (test hook): the consumers' bounded wait gives up,
     the status word says so, the CTA still publishes an (empty) partial and arrives, so
@@ -405,8 +473,10 @@ def test_pipeline_wait_timeout_leaves_workspace_clean(fd, G, flags):
     import torch
     flag = {0: 0, "two_launch": fd.FD_PLAN_TWO_LAUNCH, "cluster": fd.FD_PLAN_CLUSTER,
             "tcgen05": fd.FD_PLAN_TCGEN05,
-            "tcgen05_cluster": fd.FD_PLAN_TCGEN05 | fd.FD_PLAN_CLUSTER}[flags]
-    p = workloads.make_problem("skip", 2, 4 * G, 4, 128, [5000, 700], [4, 2], "f16", seed=42 + G)
+            "tcgen05_cluster": fd.FD_PLAN_TCGEN05 | fd.FD_PLAN_CLUSTER,
+            "cluster_combine": fd.FD_PLAN_CLUSTER_COMBINE}[flags]
+    W = 4 if flags == "cluster_combine" else [4, 2]      # one W for every sequence there
+    p = workloads.make_problem("skip", 2, 4 * G, 4, 128, [5000, 700], W, "f16", seed=42 + G)
     ref_out, ref_lse = oracle.decode_reference(p.q, p.k, p.v, p.seqlens, p.dtype)
     dec = fd.Decoder(p.Hq, p.Hkv, p.d, p.seqlens, p.W, p.dtype,
                      flags=flag | fd.FD_PLAN_TEST_SKIP_TILE)

@@ -7,7 +7,8 @@ static device array instead, and fd_noalloc_status reads that array's status.
 
 The GPU tests call both through the C ABI.  Every variant of the kernel that
 the entry point can launch (f16, bf16, two launches, the in-cluster segment
-merge, an FP8 cache, fine-grained waits) is compared with fd_decode (the
+merge, an FP8 cache, fine-grained waits, the combine inside a cluster per
+(sequence, KV head), tcgen05 consumers) is compared with fd_decode (the
 workspace entry point) on the same plan and inputs, on two calls in a row that
 follow a call with a different plan (the array keeps the previous call's
 partials).  The deterministic variants must match bit for bit; the
@@ -91,11 +92,16 @@ def _variants(fd):
         "cluster": (lambda: _small("f16", 93, G=8), fd.FD_PLAN_CLUSTER),
         "e4m3_kv": (lambda: workloads.with_e4m3_kv(_small("f16", 94)), 0),
         "waits": (lambda: _small("f16", 95), fd.FD_PLAN_WAITS),
+        "cluster_combine": (lambda: workloads.make_problem("noalloc_cc", 3, 32, 8, 128,
+                                                           [9000, 17, 4096], 4, "bf16", seed=98),
+                            fd.FD_PLAN_CLUSTER_COMBINE),
+        "tcgen05": (lambda: _small("f16", 99, G=16), fd.FD_PLAN_TCGEN05),
     }
 
 
 @pytest.mark.gpu
-@pytest.mark.parametrize("variant", ["f16_32k", "bf16", "two_launch", "cluster", "e4m3_kv", "waits"])
+@pytest.mark.parametrize("variant", ["f16_32k", "bf16", "two_launch", "cluster", "e4m3_kv", "waits",
+                                     "cluster_combine", "tcgen05"])
 def test_noalloc_matches_fd_decode_on_two_calls_in_a_row(variant):
     import torch
     fd = _fd()
