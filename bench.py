@@ -59,6 +59,8 @@ def parse_args(argv=None):
     ap.add_argument("--two-launch", action="store_true", help="split + combine as two kernels")
     ap.add_argument("--ffma", action="store_true", help="CUDA-core consumers even when G >= 4")
     ap.add_argument("--tcgen05", action="store_true", help="tcgen05 tensor cores (d = 128, G >= 4)")
+    ap.add_argument("--mma-sync", action="store_true",
+                    help="mma.sync tensor cores where tcgen05 is the default (G = 16)")
     ap.add_argument("--cluster-combine", action="store_true",
                     help="combine each (sequence, KV head) pair inside one thread-block cluster")
     ap.add_argument("--no-pdl", action="store_true", help="launch without programmatic dependent launch")
@@ -415,7 +417,8 @@ def plan_flags(fd, args, prob):
         fd.FD_PLAN_NO_PDL if args.no_pdl else 0) | (fd.FD_PLAN_WAITS if args.waits else 0) | (
         fd.FD_PLAN_NO_CLUSTER if args.no_cluster else 0) | (fd.FD_PLAN_CLUSTER if args.cluster else 0) | (
         fd.FD_PLAN_TCGEN05 if args.tcgen05 else 0) | (
-        fd.FD_PLAN_CLUSTER_COMBINE if args.cluster_combine else 0)
+        fd.FD_PLAN_CLUSTER_COMBINE if args.cluster_combine else 0) | (
+        fd.FD_PLAN_MMA_SYNC if args.mma_sync else 0)
 
 
 class CaseRun:

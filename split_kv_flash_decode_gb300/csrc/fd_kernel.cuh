@@ -22,7 +22,8 @@
 //            operand layout by movmatrix.  K/V tiles are 64-column half-tiles
 //            with the 128-byte swizzle, so ldmatrix is conflict-free.
 //       MMA over an E4M3 cache (fp16 q/out): the same mma.sync, fragments
-//            loaded straight from the byte rows and widened in registers.
+//            loaded straight from the byte rows and widened in registers by the
+//            hardware E4M3 -> f16 conversion.
 //       FFMA (G <= 2, or forced): lanes form groups of LPT lanes, a group owns
 //            one token at a time, scores use FFMA plus an xor-shuffle reduction.
 //     Each warp (MMA) or token group (FFMA) keeps its own running (m, l, acc)
@@ -250,18 +251,19 @@ __device__ __forceinline__ void mma16816<__nv_bfloat16>(float (&d)[4], const uin
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
-// Two FP8 E4M3 values widened to an f16 pair equal to the E4M3 values times 2^-8,
-// exactly: the E4M3 exponent and mantissa bits become the low bits of the f16
-// exponent and the top of its mantissa (exponent bias 7 vs 15), subnormals
-// included.  `sel` is a prmt selector over the bytes of {a, b} that puts, in each
-// 16-bit half, an E4M3 byte in the low byte and that byte sign-extended (selector
-// nibble bit 3) in the high byte.  Shifting left by 7 then moves the byte's
-// exponent and mantissa to bits 7-13 and the sign copy to bit 15; the mask clears
-// bit 14 (the byte's own sign bit) and the bits below 7.
-__device__ __forceinline__ uint32_t e4m3x2_to_f16x2_scaled(uint32_t a, uint32_t b, uint32_t sel) {
-  uint32_t y;
-  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(y) : "r"(a), "r"(b), "r"(sel));
-  return (y * 128u) & 0xBF80BF80u;
+// Four FP8 E4M3 values (the bytes of x) widened to two f16 pairs with the
+// hardware conversion, two values per instruction: lo <- bytes 0 (low half) and 1,
+// hi <- bytes 2 and 3.  Every E4M3 value is exact in f16; the codes 0x7F / 0xFF
+// (NaN in the format) become NaN.  (An earlier integer widening, prmt + shift +
+// mask, kept the ALU pipe 38-50% busy and ran a 32K decode in 17.6 us against 14.6 us
+// with this instruction.)
+__device__ __forceinline__ void e4m3x4_to_f16x4(uint32_t x, uint32_t& lo, uint32_t& hi) {
+  asm("{\n\t.reg .b16 a, b;\n\t"
+      "mov.b32 {a, b}, %2;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %0, a;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %1, b;\n\t}"
+      : "=r"(lo), "=r"(hi)
+      : "r"(x));
 }
 
 // Two fp32 values rounded (RN) to one packed 16-bit pair: lo in bits 0-15.
@@ -413,13 +415,14 @@ __device__ __forceinline__ void fence_proxy_async_global() {
   asm volatile("fence.proxy.async.global;" ::: "memory");
 }
 
-// Write out[b, h, 4*c4 .. 4*c4+3] = a / lam (zero where lam == 0).
+// Write out[b, h, 4*c4 .. 4*c4+3] = a / lam (zero where lam == 0, i.e. no token; a
+// NaN sum, from a NaN in K or V, stays NaN).
 template <typename T>
 __device__ __forceinline__ void store_out4(T* dst, float4 a, float lam) {
-  dst[0] = Elem<T>::from_f(lam > 0.f ? a.x / lam : 0.f);
-  dst[1] = Elem<T>::from_f(lam > 0.f ? a.y / lam : 0.f);
-  dst[2] = Elem<T>::from_f(lam > 0.f ? a.z / lam : 0.f);
-  dst[3] = Elem<T>::from_f(lam > 0.f ? a.w / lam : 0.f);
+  dst[0] = Elem<T>::from_f(lam != 0.f ? a.x / lam : 0.f);
+  dst[1] = Elem<T>::from_f(lam != 0.f ? a.y / lam : 0.f);
+  dst[2] = Elem<T>::from_f(lam != 0.f ? a.z / lam : 0.f);
+  dst[3] = Elem<T>::from_f(lam != 0.f ? a.w / lam : 0.f);
 }
 
 __device__ __forceinline__ float warp_max(float x) {
@@ -433,17 +436,29 @@ __device__ __forceinline__ float warp_sum(float x) {
   return x;
 }
 
+// Maximum over the warp (floating-point redux; NaN inputs are ignored, like fmaxf).
+__device__ __forceinline__ float warp_max_redux(float x) {
+  float r;
+  asm volatile("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(x));
+  return r;
+}
+
 // OnlineSoftmaxCombine of the Wtot partials of (b, kvh) for query heads
 // [g0, g0 + ng), from their records in shared memory, head-major
-// [ng][wtot][D + 4].  Two phases over all threads.  (1) One warp per head: M is the
-// max of the partial maxima, each lane computes the coefficients exp2(m_w - M) of
-// its partials into `coef` ([ng][wtot] after the records), and Lambda =
-// sum_w coef_w l_w and Lambda~ = sum_w coef_w l~_w go through a fixed shuffle tree.
-// (2) Every thread owns one (head, 4 output dimensions) slice and sums
-// coef_w O_w over the partials in index order, its loads independent of each
-// other.  out = O / Lambda~ (the weights P.V multiplied), lse = M + log Lambda.  The
-// order of every sum is fixed, so the result does not depend on the order in which
-// the partials arrived.
+// [ng][wtot][D + 4].  Two phases over all threads.
+//   (1) Per head: M = max of the partial maxima, coef_w = exp2(m_w - M) into
+//       `coef` ([ng][wtot]), Lambda = sum_w coef_w l_w and Lambda~ = sum_w coef_w l~_w
+//       in a fixed shuffle tree, lse = M + log Lambda.  With at most 16 partials a
+//       warp takes several heads at once (lanes = head x partial, segmented
+//       reductions); otherwise one warp per head.
+//   (2) Every thread owns one (head, 4 output dimensions) slice and sums
+//       coef_w O_w over the partials in index order, its loads independent of each
+//       other; out = that sum times 1 / Lambda~ (the weights P.V multiplied).
+// The order of every sum is fixed, so the result does not depend on the order in
+// which the partials arrived.  (Measured: the chain of dependent shuffles of phase
+// 1 costs ~900 cycles per round of heads, so packing 16 heads of 8 partials into one
+// round instead of four, and one reciprocal instead of four divisions per slice,
+// shorten the last arriver's combine.)
 template <typename T, int D, int G>
 __device__ __forceinline__ void combine_from_smem(const Params& p, int b, int kvh, int wtot,
                                                   int g0, int ng, const float* rec, float* coef) {
@@ -452,27 +467,51 @@ __device__ __forceinline__ void combine_from_smem(const Params& p, int b, int kv
   constexpr int U = 8;       // partials in flight per thread
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   constexpr int kWarps = kThreads / 32;
-  float* lams = coef + (size_t)ng * wtot;  // [ng][2]: Lambda, Lambda~
-  for (int g = warp; g < ng; g += kWarps) {
-    const float* rg = rec + (size_t)g * wtot * RS + D;
-    float M = -INFINITY;
-    for (int w = lane; w < wtot; w += 32) M = fmaxf(M, rg[(size_t)w * RS]);
-    M = warp_max(M);
-    float lam = 0.f, lamr = 0.f;
-    for (int w = lane; w < wtot; w += 32) {
-      const float4 ml = *reinterpret_cast<const float4*>(rg + (size_t)w * RS);
-      const float c = M == -INFINITY ? 0.f : ex2(ml.x - M);  // exp2(-inf) = 0: empty partial
-      coef[(size_t)g * wtot + w] = c;
-      lam = fmaf(c, ml.y, lam);
-      lamr = fmaf(c, ml.z, lamr);
+  float* lams = coef + (size_t)ng * wtot;  // [ng][2]: Lambda, 1 / Lambda~
+  auto finish_head = [&](int g, float M, float lam, float lamr) {
+    lams[2 * g] = lam;
+    lams[2 * g + 1] = lamr != 0.f ? 1.f / lamr : 0.f;  // no token: out = 0 (NaN stays NaN)
+    if (p.lse != nullptr)
+      p.lse[(int64_t)b * p.Hq + kvh * G + g0 + g] = lam != 0.f ? (M + log2f(lam)) * kLn2 : -INFINITY;
+  };
+  if (wtot <= 16) {
+    // S lanes per head (a power of two >= wtot), 32 / S heads per warp.
+    const int S = wtot <= 2 ? 2 : wtot <= 4 ? 4 : wtot <= 8 ? 8 : 16;
+    const int hpw = 32 / S;
+    const int w = lane & (S - 1);
+    for (int gb = warp * hpw; gb < ng; gb += kWarps * hpw) {
+      const int g = gb + lane / S;
+      const bool valid = g < ng && w < wtot;
+      float4 ml = make_float4(-INFINITY, 0.f, 0.f, 0.f);
+      if (valid) ml = *reinterpret_cast<const float4*>(rec + ((size_t)g * wtot + w) * RS + D);
+      float M = ml.x;
+      for (int off = 1; off < S; off <<= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+      const float c = (valid && M != -INFINITY) ? ex2(ml.x - M) : 0.f;
+      if (valid) coef[(size_t)g * wtot + w] = c;
+      float lam = c * ml.y, lamr = c * ml.z;
+      for (int off = 1; off < S; off <<= 1) {
+        lam += __shfl_xor_sync(0xffffffffu, lam, off);
+        lamr += __shfl_xor_sync(0xffffffffu, lamr, off);
+      }
+      if (w == 0 && g < ng) finish_head(g, M, lam, lamr);
     }
-    lam = warp_sum(lam);
-    lamr = warp_sum(lamr);
-    if (lane == 0) {
-      lams[2 * g] = lam;
-      lams[2 * g + 1] = lamr;
-      if (p.lse != nullptr)
-        p.lse[(int64_t)b * p.Hq + kvh * G + g0 + g] = lam > 0.f ? (M + log2f(lam)) * kLn2 : -INFINITY;
+  } else {
+    for (int g = warp; g < ng; g += kWarps) {
+      const float* rg = rec + (size_t)g * wtot * RS + D;
+      float M = -INFINITY;
+      for (int w = lane; w < wtot; w += 32) M = fmaxf(M, rg[(size_t)w * RS]);
+      M = warp_max_redux(M);
+      float lam = 0.f, lamr = 0.f;
+      for (int w = lane; w < wtot; w += 32) {
+        const float4 ml = *reinterpret_cast<const float4*>(rg + (size_t)w * RS);
+        const float c = M == -INFINITY ? 0.f : ex2(ml.x - M);  // exp2(-inf) = 0: empty partial
+        coef[(size_t)g * wtot + w] = c;
+        lam = fmaf(c, ml.y, lam);
+        lamr = fmaf(c, ml.z, lamr);
+      }
+      lam = warp_sum(lam);
+      lamr = warp_sum(lamr);
+      if (lane == 0) finish_head(g, M, lam, lamr);
     }
   }
   __syncthreads();
@@ -504,7 +543,12 @@ __device__ __forceinline__ void combine_from_smem(const Params& p, int b, int kv
       acc.z = fmaf(c, x.z, acc.z);
       acc.w = fmaf(c, x.w, acc.w);
     }
-    store_out4<T>(out + ((int64_t)b * p.Hq + kvh * G + g0 + g) * D + 4 * c4, acc, lams[2 * g + 1]);
+    const float inv = lams[2 * g + 1];
+    T* dst = out + ((int64_t)b * p.Hq + kvh * G + g0 + g) * D + 4 * c4;
+    dst[0] = Elem<T>::from_f(acc.x * inv);
+    dst[1] = Elem<T>::from_f(acc.y * inv);
+    dst[2] = Elem<T>::from_f(acc.z * inv);
+    dst[3] = Elem<T>::from_f(acc.w * inv);
   }
 }
 
@@ -574,7 +618,7 @@ __device__ __forceinline__ void combine_from_global(const Params& p, int b, int 
   }
   if (tid < G && p.lse != nullptr) {
     const float M = ML[3 * tid], lam = ML[3 * tid + 1];
-    p.lse[(int64_t)b * p.Hq + kvh * G + tid] = lam > 0.f ? (M + log2f(lam)) * kLn2 : -INFINITY;
+    p.lse[(int64_t)b * p.Hq + kvh * G + tid] = lam != 0.f ? (M + log2f(lam)) * kLn2 : -INFINITY;
   }
 }
 
@@ -723,7 +767,7 @@ __device__ __forceinline__ void combine_as_arrived(const Params& p, const Work& 
   }
   if (tid < G && p.lse != nullptr) {
     const float M = run_M[tid], lam = run_L[tid];
-    p.lse[(int64_t)wk.b * p.Hq + wk.kvh * G + tid] = lam > 0.f ? (M + log2f(lam)) * kLn2 : -INFINITY;
+    p.lse[(int64_t)wk.b * p.Hq + wk.kvh * G + tid] = lam != 0.f ? (M + log2f(lam)) * kLn2 : -INFINITY;
   }
 }
 
@@ -851,7 +895,7 @@ __device__ __forceinline__ void combine_in_cluster(const Params& p, const Work& 
   }
   if (wk.slot == 0 && tid < G && p.lse != nullptr) {
     const float M = cf[G * CS + tid], lam = cf[G * CS + G + tid];
-    p.lse[(int64_t)wk.b * p.Hq + wk.kvh * G + tid] = lam > 0.f ? (M + log2f(lam)) * kLn2 : -INFINITY;
+    p.lse[(int64_t)wk.b * p.Hq + wk.kvh * G + tid] = lam != 0.f ? (M + log2f(lam)) * kLn2 : -INFINITY;
   }
   cluster_arrive();  // done reading the other CTAs' shared memory
   cluster_wait();
@@ -901,11 +945,11 @@ __device__ __forceinline__ void finish_cta(const Params& p, const Work& wk, floa
 #pragma unroll 4
       for (int q = 0; q < NGRP; ++q) a = fmaf(sm_acc[(q * G + g) * D + dim], sm_fac[q * G + g], a);
       const float lamr = sm_ML[3 * g + 2];
-      out[((int64_t)wk.b * p.Hq + h0 + g) * D + dim] = Elem<T>::from_f(lamr > 0.f ? a / lamr : 0.f);
+      out[((int64_t)wk.b * p.Hq + h0 + g) * D + dim] = Elem<T>::from_f(lamr != 0.f ? a / lamr : 0.f);
     }
     if (tid < G && p.lse != nullptr) {
       const float M = sm_ML[3 * tid], lam = sm_ML[3 * tid + 1];
-      p.lse[(int64_t)wk.b * p.Hq + h0 + tid] = lam > 0.f ? (M + log2f(lam)) * kLn2 : -INFINITY;
+      p.lse[(int64_t)wk.b * p.Hq + h0 + tid] = lam != 0.f ? (M + log2f(lam)) * kLn2 : -INFINITY;
     }
     return;
   }
@@ -1382,8 +1426,7 @@ __global__ void __launch_bounds__(kThreads, 2) fd_split_kernel(const __grid_cons
     // of S = K q^T (k-step kk, thread quad t covers d = 16(2t + kk/4) + 4(kk%4) +
     // {0,1} for a0/a1/b0 and + {2,3} for a2/a3/b1, applied to K and to q alike), and
     // the rows of O^T (row g / g+8 of m-tile mi is dim 16g + 2mi / 16g + 2mi + 1,
-    // undone when the state is written).  Widened values are E4M3 * 2^-8: the 2^8
-    // folds exactly into the score scale (K) and into O (V).
+    // undone when the state is written).  Widening is exact (cvt to f16).
     static_assert(D == 128, "FP8 K/V rows are single 128-byte swizzle rows");
     constexpr int KT = 8;                   // k-steps of S, m-tiles of O^T
     constexpr int NT = G >= 8 ? G / 8 : 1;  // N tiles of 8 query heads
@@ -1411,7 +1454,7 @@ __global__ void __launch_bounds__(kThreads, 2) fd_split_kernel(const __grid_cons
       mA[nt] = mB[nt] = -INFINITY;
       lA[nt] = lB[nt] = lrA[nt] = lrB[nt] = 0.f;
     }
-    const float scale = p.scale_log2 * 256.f;
+    const float scale = p.scale_log2;
     const int tok0 = warp * 16;
 
     for (int kt = 0; kt < ntiles; ++kt) {
@@ -1450,10 +1493,8 @@ __global__ void __launch_bounds__(kThreads, 2) fd_split_kernel(const __grid_cons
           const uint32_t x0 = wi == 0 ? w0.x : wi == 1 ? w0.y : wi == 2 ? w0.z : w0.w;
           const uint32_t x1 = wi == 0 ? w1.x : wi == 1 ? w1.y : wi == 2 ? w1.z : w1.w;
           uint32_t a[4];
-          a[0] = e4m3x2_to_f16x2_scaled(x0, 0u, 0x9180u);  // bytes 0, 1
-          a[1] = e4m3x2_to_f16x2_scaled(x1, 0u, 0x9180u);
-          a[2] = e4m3x2_to_f16x2_scaled(x0, 0u, 0xB3A2u);  // bytes 2, 3
-          a[3] = e4m3x2_to_f16x2_scaled(x1, 0u, 0xB3A2u);
+          e4m3x4_to_f16x4(x0, a[0], a[2]);  // bytes 0, 1 and 2, 3 of row g
+          e4m3x4_to_f16x4(x1, a[1], a[3]);  // the same of row g + 8
 #pragma unroll
           for (int nt = 0; nt < NT; ++nt)
             mma16816<T>((kk & 1) ? sd[nt] : sc[nt], a, qb[nt][kk][0], qb[nt][kk][1]);
@@ -1521,15 +1562,15 @@ __global__ void __launch_bounds__(kThreads, 2) fd_split_kernel(const __grid_cons
           const uint32_t y1 = wi == 0 ? vw[1].x : wi == 1 ? vw[1].y : wi == 2 ? vw[1].z : vw[1].w;
           const uint32_t y2 = wi == 0 ? vw[2].x : wi == 1 ? vw[2].y : wi == 2 ? vw[2].z : vw[2].w;
           const uint32_t y3 = wi == 0 ? vw[3].x : wi == 1 ? vw[3].y : wi == 2 ? vw[3].z : vw[3].w;
-          // byte k (dim 16g + 2mi) and k + 1 (dim 16g + 2mi + 1) of two token rows:
-          // low half <- row of the first word, high half <- row of the second
-          const uint32_t sel0 = ((12u + k) << 12) | ((4u + k) << 8) | ((8u + k) << 4) | k;
-          const uint32_t sel1 = ((13u + k) << 12) | ((5u + k) << 8) | ((9u + k) << 4) | (k + 1u);
-          uint32_t a[4];
-          a[0] = e4m3x2_to_f16x2_scaled(y0, y1, sel0);
-          a[1] = e4m3x2_to_f16x2_scaled(y0, y1, sel1);
-          a[2] = e4m3x2_to_f16x2_scaled(y2, y3, sel0);
-          a[3] = e4m3x2_to_f16x2_scaled(y2, y3, sel1);
+          // bytes k (dim 16g + 2mi) and k + 1 (dim 16g + 2mi + 1) of two token rows,
+          // gathered as [row0 k, row1 k, row0 k+1, row1 k+1]: each widened pair holds
+          // the row of the first word in its low half, the second in its high half
+          const uint32_t sel = ((5u + k) << 12) | ((1u + k) << 8) | ((4u + k) << 4) | k;
+          uint32_t a[4], z;
+          asm("prmt.b32 %0, %1, %2, %3;" : "=r"(z) : "r"(y0), "r"(y1), "r"(sel));
+          e4m3x4_to_f16x4(z, a[0], a[1]);
+          asm("prmt.b32 %0, %1, %2, %3;" : "=r"(z) : "r"(y2), "r"(y3), "r"(sel));
+          e4m3x4_to_f16x4(z, a[2], a[3]);
 #pragma unroll
           for (int nt = 0; nt < NT; ++nt) mma16816<T>(o[nt][mi], a, pb0[nt], pb1[nt]);
         }
@@ -1557,10 +1598,10 @@ __global__ void __launch_bounds__(kThreads, 2) fd_split_kernel(const __grid_cons
           float* accB = accA + D;
 #pragma unroll
           for (int mi = 0; mi < KT; ++mi) {
-            accA[16 * g + 2 * mi] = o[nt][mi][0] * 256.f;
-            accB[16 * g + 2 * mi] = o[nt][mi][1] * 256.f;
-            accA[16 * g + 2 * mi + 1] = o[nt][mi][2] * 256.f;
-            accB[16 * g + 2 * mi + 1] = o[nt][mi][3] * 256.f;
+            accA[16 * g + 2 * mi] = o[nt][mi][0];
+            accB[16 * g + 2 * mi] = o[nt][mi][1];
+            accA[16 * g + 2 * mi + 1] = o[nt][mi][2];
+            accB[16 * g + 2 * mi + 1] = o[nt][mi][3];
           }
           if (g == 0) {
             sm_m[warp * G + hA] = mA[nt];
