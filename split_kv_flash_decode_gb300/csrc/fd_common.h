@@ -41,7 +41,10 @@ FD_HD constexpr bool is_mma(int path) { return path != kPathFfma; }
 // Bytes per stored K/V element.
 FD_HD constexpr int kv_elem_bytes(int path) { return path == kPathMmaKv8 ? 1 : 2; }
 // Tokens per pipeline stage.
-FD_HD constexpr int tile_for(int path) { return path == kPathUmma ? 128 : is_mma(path) ? 64 : 32; }
+// (FP8: 128-token tiles, two 16-token groups per consumer warp per stage.)
+FD_HD constexpr int tile_for(int path) {
+  return (path == kPathUmma || path == kPathMmaKv8) ? 128 : is_mma(path) ? 64 : 32;
+}
 // Columns (elements) of one TMA box row: 128-byte swizzled rows on the MMA paths.
 FD_HD constexpr int box_cols_for(int path, int d) {
   return (path == kPathMma || path == kPathUmma) ? 64 : path == kPathMmaKv8 ? 128 : d;

@@ -1455,7 +1455,12 @@ __global__ void __launch_bounds__(kThreads, 2) fd_split_kernel(const __grid_cons
       lA[nt] = lB[nt] = lrA[nt] = lrB[nt] = 0.f;
     }
     const float scale = p.scale_log2;
-    const int tok0 = warp * 16;
+    // Each warp takes SUB groups of 16 tokens per tile: their K loads, widening and
+    // score mma are independent chains, one max update covers all of them, and P.V
+    // accumulates them into the same O^T fragments.
+    constexpr int SUB = TILE / (kConsumerWarps * 16);
+    static_assert(SUB * kConsumerWarps * 16 == TILE, "the FP8 tile splits into 16-token groups");
+    const int tok0 = warp * 16 * SUB;
 
     for (int kt = 0; kt < ntiles; ++kt) {
       const int s = kt % NSLOT;
@@ -1469,49 +1474,62 @@ __global__ void __launch_bounds__(kThreads, 2) fd_split_kernel(const __grid_cons
       }
       const int ntok = min(TILE, wk.t1 - (wk.t0 + kt * TILE));
       if (tok0 < ntok) {
-        // K: rows tok0 + g (+8), 16-byte chunks 2t and 2t + 1.
-        uint4 kw[2][2];
+        const uint8_t* kslot = smem + (size_t)s * kSlotBytes;
+        const uint8_t* vslot = kslot + kRowsBytes;
+        // Scores of every group: two accumulators each (even and odd k-steps) halve
+        // the chains of dependent mma.
+        float sc[SUB][NT][4];
 #pragma unroll
-        for (int rh = 0; rh < 2; ++rh)
+        for (int u = 0; u < SUB; ++u) {
+          const int tb = tok0 + 16 * u;
+          // K: rows tb + g (+8), 16-byte chunks 2t and 2t + 1.
+          uint4 kw[2][2];
 #pragma unroll
-          for (int grp = 0; grp < 2; ++grp) {
-            const int r = tok0 + g + 8 * rh, c = 2 * t + grp;
-            kw[rh][grp] = *reinterpret_cast<const uint4*>(
-                smem + (size_t)s * kSlotBytes + r * 128 + ((c ^ (r & 7)) << 4));
-          }
-        // Two accumulators (even and odd k-steps) halve the chain of dependent mma.
-        float sc[NT][4], sd[NT][4];
+          for (int rh = 0; rh < 2; ++rh)
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-          for (int i = 0; i < 4; ++i) sc[nt][i] = sd[nt][i] = 0.f;
-#pragma unroll
-        for (int kk = 0; kk < KT; ++kk) {
-          const uint4& w0 = kw[0][kk >> 2];
-          const uint4& w1 = kw[1][kk >> 2];
-          const int wi = kk & 3;
-          const uint32_t x0 = wi == 0 ? w0.x : wi == 1 ? w0.y : wi == 2 ? w0.z : w0.w;
-          const uint32_t x1 = wi == 0 ? w1.x : wi == 1 ? w1.y : wi == 2 ? w1.z : w1.w;
-          uint32_t a[4];
-          e4m3x4_to_f16x4(x0, a[0], a[2]);  // bytes 0, 1 and 2, 3 of row g
-          e4m3x4_to_f16x4(x1, a[1], a[3]);  // the same of row g + 8
+            for (int grp = 0; grp < 2; ++grp) {
+              const int r = tb + g + 8 * rh, c = 2 * t + grp;
+              kw[rh][grp] = *reinterpret_cast<const uint4*>(kslot + r * 128 + ((c ^ (r & 7)) << 4));
+            }
+          float sd[NT][4];
 #pragma unroll
           for (int nt = 0; nt < NT; ++nt)
-            mma16816<T>((kk & 1) ? sd[nt] : sc[nt], a, qb[nt][kk][0], qb[nt][kk][1]);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) sc[u][nt][i] = sd[nt][i] = 0.f;
+#pragma unroll
+          for (int kk = 0; kk < KT; ++kk) {
+            const uint4& w0 = kw[0][kk >> 2];
+            const uint4& w1 = kw[1][kk >> 2];
+            const int wi = kk & 3;
+            const uint32_t x0 = wi == 0 ? w0.x : wi == 1 ? w0.y : wi == 2 ? w0.z : w0.w;
+            const uint32_t x1 = wi == 0 ? w1.x : wi == 1 ? w1.y : wi == 2 ? w1.z : w1.w;
+            uint32_t a[4];
+            e4m3x4_to_f16x4(x0, a[0], a[2]);  // bytes 0, 1 and 2, 3 of row g
+            e4m3x4_to_f16x4(x1, a[1], a[3]);  // the same of row g + 8
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+              mma16816<T>((kk & 1) ? sd[nt] : sc[u][nt], a, qb[nt][kk][0], qb[nt][kk][1]);
+          }
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int i = 0; i < 4; ++i) sc[u][nt][i] += sd[nt][i];
         }
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-          for (int i = 0; i < 4; ++i) sc[nt][i] += sd[nt][i];
-        const bool v0 = tok0 + g < ntok, v1 = tok0 + g + 8 < ntok;
-        uint32_t pb0[NT], pb1[NT];
+        uint32_t pb0[SUB][NT], pb1[SUB][NT];
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
-          const float sA0 = v0 ? sc[nt][0] * scale : -INFINITY;
-          const float sB0 = v0 ? sc[nt][1] * scale : -INFINITY;
-          const float sA1 = v1 ? sc[nt][2] * scale : -INFINITY;
-          const float sB1 = v1 ? sc[nt][3] * scale : -INFINITY;
-          float xA = fmaxf(sA0, sA1), xB = fmaxf(sB0, sB1);
+          float sA0[SUB], sB0[SUB], sA1[SUB], sB1[SUB];
+          float xA = -INFINITY, xB = -INFINITY;
+#pragma unroll
+          for (int u = 0; u < SUB; ++u) {
+            const bool v0 = tok0 + 16 * u + g < ntok, v1 = tok0 + 16 * u + g + 8 < ntok;
+            sA0[u] = v0 ? sc[u][nt][0] * scale : -INFINITY;
+            sB0[u] = v0 ? sc[u][nt][1] * scale : -INFINITY;
+            sA1[u] = v1 ? sc[u][nt][2] * scale : -INFINITY;
+            sB1[u] = v1 ? sc[u][nt][3] * scale : -INFINITY;
+            xA = fmaxf(xA, fmaxf(sA0[u], sA1[u]));
+            xB = fmaxf(xB, fmaxf(sB0[u], sB1[u]));
+          }
 #pragma unroll
           for (int off = 4; off < 32; off <<= 1) {
             xA = fmaxf(xA, __shfl_xor_sync(0xffffffffu, xA, off));
@@ -1533,46 +1551,53 @@ __global__ void __launch_bounds__(kThreads, 2) fd_split_kernel(const __grid_cons
             for (int mi = 0; mi < KT; ++mi) { o[nt][mi][1] *= corr; o[nt][mi][3] *= corr; }
             mB[nt] = xB;
           }
-          const float pA0 = ex2(sA0 - mA[nt]), pB0 = ex2(sB0 - mB[nt]);
-          const float pA1 = ex2(sA1 - mA[nt]), pB1 = ex2(sB1 - mB[nt]);
-          lA[nt] += pA0 + pA1;
-          lB[nt] += pB0 + pB1;
-          const uint32_t r0 = pack2<T>(pA0, pB0), r1 = pack2<T>(pA1, pB1);
-          // lr sums the same 16-bit weights that P.V multiplies, so the output is an
-          // exact convex combination of V rows under the rounded weights.
-          const float2 w0 = Elem<T>::to_f2(r0), w1 = Elem<T>::to_f2(r1);
-          lrA[nt] += w0.x + w1.x;
-          lrB[nt] += w0.y + w1.y;
-          pb0[nt] = movmatrix_trans(r0);
-          pb1[nt] = movmatrix_trans(r1);
-        }
-        // V^T: token rows tok0 + 2t, +1, +8, +9; the 16-byte chunk g (dims 16g ..).
-        uint4 vw[4];
+          // Row tok0 is valid, so the column maxima (and mA, mB) are finite here.
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const int r = tok0 + 2 * t + (i & 1) + 8 * (i >> 1);
-          vw[i] = *reinterpret_cast<const uint4*>(smem + (size_t)s * kSlotBytes + kRowsBytes +
-                                                  r * 128 + ((g ^ (r & 7)) << 4));
+          for (int u = 0; u < SUB; ++u) {
+            const float pA0 = ex2(sA0[u] - mA[nt]), pB0 = ex2(sB0[u] - mB[nt]);
+            const float pA1 = ex2(sA1[u] - mA[nt]), pB1 = ex2(sB1[u] - mB[nt]);
+            lA[nt] += pA0 + pA1;
+            lB[nt] += pB0 + pB1;
+            const uint32_t r0 = pack2<T>(pA0, pB0), r1 = pack2<T>(pA1, pB1);
+            // lr sums the same 16-bit weights that P.V multiplies, so the output is an
+            // exact convex combination of V rows under the rounded weights.
+            const float2 w0 = Elem<T>::to_f2(r0), w1 = Elem<T>::to_f2(r1);
+            lrA[nt] += w0.x + w1.x;
+            lrB[nt] += w0.y + w1.y;
+            pb0[u][nt] = movmatrix_trans(r0);
+            pb1[u][nt] = movmatrix_trans(r1);
+          }
         }
 #pragma unroll
-        for (int mi = 0; mi < KT; ++mi) {
-          const int wi = mi >> 1;
-          const uint32_t k = 2u * (mi & 1);
-          const uint32_t y0 = wi == 0 ? vw[0].x : wi == 1 ? vw[0].y : wi == 2 ? vw[0].z : vw[0].w;
-          const uint32_t y1 = wi == 0 ? vw[1].x : wi == 1 ? vw[1].y : wi == 2 ? vw[1].z : vw[1].w;
-          const uint32_t y2 = wi == 0 ? vw[2].x : wi == 1 ? vw[2].y : wi == 2 ? vw[2].z : vw[2].w;
-          const uint32_t y3 = wi == 0 ? vw[3].x : wi == 1 ? vw[3].y : wi == 2 ? vw[3].z : vw[3].w;
-          // bytes k (dim 16g + 2mi) and k + 1 (dim 16g + 2mi + 1) of two token rows,
-          // gathered as [row0 k, row1 k, row0 k+1, row1 k+1]: each widened pair holds
-          // the row of the first word in its low half, the second in its high half
-          const uint32_t sel = ((5u + k) << 12) | ((1u + k) << 8) | ((4u + k) << 4) | k;
-          uint32_t a[4], z;
-          asm("prmt.b32 %0, %1, %2, %3;" : "=r"(z) : "r"(y0), "r"(y1), "r"(sel));
-          e4m3x4_to_f16x4(z, a[0], a[1]);
-          asm("prmt.b32 %0, %1, %2, %3;" : "=r"(z) : "r"(y2), "r"(y3), "r"(sel));
-          e4m3x4_to_f16x4(z, a[2], a[3]);
+        for (int u = 0; u < SUB; ++u) {
+          const int tb = tok0 + 16 * u;
+          // V^T: token rows tb + 2t, +1, +8, +9; the 16-byte chunk g (dims 16g ..).
+          uint4 vw[4];
 #pragma unroll
-          for (int nt = 0; nt < NT; ++nt) mma16816<T>(o[nt][mi], a, pb0[nt], pb1[nt]);
+          for (int i = 0; i < 4; ++i) {
+            const int r = tb + 2 * t + (i & 1) + 8 * (i >> 1);
+            vw[i] = *reinterpret_cast<const uint4*>(vslot + r * 128 + ((g ^ (r & 7)) << 4));
+          }
+#pragma unroll
+          for (int mi = 0; mi < KT; ++mi) {
+            const int wi = mi >> 1;
+            const uint32_t k = 2u * (mi & 1);
+            const uint32_t y0 = wi == 0 ? vw[0].x : wi == 1 ? vw[0].y : wi == 2 ? vw[0].z : vw[0].w;
+            const uint32_t y1 = wi == 0 ? vw[1].x : wi == 1 ? vw[1].y : wi == 2 ? vw[1].z : vw[1].w;
+            const uint32_t y2 = wi == 0 ? vw[2].x : wi == 1 ? vw[2].y : wi == 2 ? vw[2].z : vw[2].w;
+            const uint32_t y3 = wi == 0 ? vw[3].x : wi == 1 ? vw[3].y : wi == 2 ? vw[3].z : vw[3].w;
+            // bytes k (dim 16g + 2mi) and k + 1 (dim 16g + 2mi + 1) of two token rows,
+            // gathered as [row0 k, row1 k, row0 k+1, row1 k+1]: each widened pair holds
+            // the row of the first word in its low half, the second in its high half
+            const uint32_t sel = ((5u + k) << 12) | ((1u + k) << 8) | ((4u + k) << 4) | k;
+            uint32_t a[4], z;
+            asm("prmt.b32 %0, %1, %2, %3;" : "=r"(z) : "r"(y0), "r"(y1), "r"(sel));
+            e4m3x4_to_f16x4(z, a[0], a[1]);
+            asm("prmt.b32 %0, %1, %2, %3;" : "=r"(z) : "r"(y2), "r"(y3), "r"(sel));
+            e4m3x4_to_f16x4(z, a[2], a[3]);
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) mma16816<T>(o[nt][mi], a, pb0[u][nt], pb1[u][nt]);
+          }
         }
       }
       __syncwarp();
