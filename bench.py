@@ -55,6 +55,8 @@ def parse_args(argv=None):
     ap.add_argument("--impl", choices=["fd", "reference"], default="fd")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--W", type=int, default=DEFAULT_W, help="segments for the batch64 W-sweep workload")
+    ap.add_argument("--B", type=int, default=64,
+                    help="sequences of the batch64 workload (fewer: a smaller case of the same kernel)")
     ap.add_argument("--chunks", type=int, default=0, help="chunks per segment (0 = planner)")
     ap.add_argument("--two-launch", action="store_true", help="split + combine as two kernels")
     ap.add_argument("--ffma", action="store_true", help="CUDA-core consumers even when G >= 4")
@@ -89,7 +91,7 @@ def parse_args(argv=None):
 def make_problem(args):
     import workloads
     if args.workload.startswith("batch64"):
-        prob = workloads.batch64_gqa4_d128_L8k_bf16(W=args.W)
+        prob = workloads.batch64_gqa4_d128_L8k_bf16(W=args.W, B=getattr(args, "B", 64))
     elif args.workload in workloads.EXTRA:
         prob = workloads.EXTRA[args.workload]()
     else:
@@ -316,7 +318,7 @@ def cpu_baseline_only(args):
 def run_cpu_baseline_subprocess(args):
     env = dict(os.environ, **_ONE_THREAD)
     cmd = [sys.executable, os.path.abspath(__file__), "--cpu-baseline-only", "--workload",
-           args.workload, "--W", str(args.W), "--cpu-seconds", str(args.cpu_seconds),
+           args.workload, "--W", str(args.W), "--B", str(args.B), "--cpu-seconds", str(args.cpu_seconds),
            "--kv", args.kv]
     res = subprocess.run(cmd, env=env, capture_output=True, text=True, timeout=900)
     if res.returncode != 0:

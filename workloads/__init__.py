@@ -273,14 +273,15 @@ def ragged16_gqa4_d128(seed: int = 1003) -> DecodeProblem:
     return make_problem("ragged16_gqa4_d128", 16, 32, 8, 128, lens, W, F16, seed)
 
 
-def batch64_gqa4_d128_L8k_bf16(W: int = 1, seed: int = 1004) -> DecodeProblem:
+def batch64_gqa4_d128_L8k_bf16(W: int = 1, seed: int = 1004, B: int = 64) -> DecodeProblem:
     """B=64, Hq=32 / Hkv=8, d=128, L=8192 each, bf16 N(0,1); W in {1,2,4,8,16}, exactly W segments.
 
     The inputs do not depend on W (same seed), so a W sweep runs on identical data.
+    ``B`` < 64 gives the first B sequences of the same draw (a smaller case of the
+    same kernel, e.g. for a profiler capture); it is not one of the five cases.
     """
-    p = make_problem(f"batch64_gqa4_d128_L8k_bf16_W{W}", 64, 32, 8, 128, [8192] * 64, W,
-                     BF16, seed, literal_w=True)
-    return p
+    name = f"batch{B}_gqa4_d128_L8k_bf16_W{W}"
+    return make_problem(name, B, 32, 8, 128, [8192] * B, W, BF16, seed, literal_w=True)
 
 
 def gqa16_d128_L32k_W8(seed: int = 1005) -> DecodeProblem:
