@@ -368,7 +368,8 @@ def run_reference(args):
 # ---------------------------------------------------------------------------
 
 KERNEL_SOURCES = ("split_kv_flash_decode_gb300/csrc/fd_kernel.cuh",
-                  "split_kv_flash_decode_gb300/csrc/fd_common.h")
+                  "split_kv_flash_decode_gb300/csrc/fd_common.h",
+                  "split_kv_flash_decode_gb300/csrc/fd_tcgen05.cuh")
 
 
 def kernel_source_hash() -> str:

@@ -22,8 +22,9 @@ LIBDIR = os.path.join(PKG, "_lib")
 LIB = os.path.join(LIBDIR, "libfd_gb300.so")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-SOURCES = ["fd_api.cpp", "fd_kernel_f16.cu", "fd_kernel_bf16.cu", "fd_kernel_umma_f16.cu",
-           "fd_kernel_umma_bf16.cu", "fd_noalloc.cu"]
+SOURCES = ["fd_api.cpp", "fd_kernel_f16.cu", "fd_kernel_bf16.cu", "fd_kernel_f16_ffma.cu",
+           "fd_kernel_bf16_ffma.cu", "fd_kernel_umma_f16.cu", "fd_kernel_umma_bf16.cu",
+           "fd_noalloc.cu"]
 
 
 def _nvcc() -> str:

@@ -163,17 +163,21 @@ FD_HD void chunk_range(int L, int W, int C, int slot, int align, int* t0, int* t
   *t1 = (int)(sb + e);
 }
 
-// Launchers defined in the per-dtype kernel translation units.
+// Launchers defined in the kernel translation units (one per dtype and consumer family).
 // mode 0: fused split + last-arriver combine; 1: split only (partials); 2: combine only;
 // 3: fused split + fine-grained waits (slot 0 combines partials as their flags arrive;
 //    cooperative launch); 6: fused, every partial of a (sequence, KV head) pair in one
 //    thread-block cluster, combined through distributed shared memory.
 // pdl: launch with programmatic stream serialization (the kernel waits on its
 // predecessors with griddepcontrol.wait before touching global memory).
-cudaError_t launch_f16(const Params& p, int d, int G, int path, int mode, bool pdl, int grid,
-                       cudaStream_t s);
-cudaError_t launch_bf16(const Params& p, int d, int G, int path, int mode, bool pdl, int grid,
-                        cudaStream_t s);
+cudaError_t launch_f16_mma(const Params& p, int d, int G, int path, int mode, bool pdl, int grid,
+                           cudaStream_t s);
+cudaError_t launch_bf16_mma(const Params& p, int d, int G, int path, int mode, bool pdl, int grid,
+                            cudaStream_t s);
+cudaError_t launch_f16_ffma(const Params& p, int d, int G, int mode, bool pdl, int grid,
+                            cudaStream_t s);
+cudaError_t launch_bf16_ffma(const Params& p, int d, int G, int mode, bool pdl, int grid,
+                             cudaStream_t s);
 cudaError_t launch_umma_f16(const Params& p, int d, int G, int mode, bool pdl, int grid,
                             cudaStream_t s);
 cudaError_t launch_umma_bf16(const Params& p, int d, int G, int mode, bool pdl, int grid,

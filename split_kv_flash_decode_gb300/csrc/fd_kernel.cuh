@@ -2037,14 +2037,24 @@ cudaError_t launch_dgp(const Params& p, int mode, bool pdl, int grid, cudaStream
   return cudaLaunchKernelExC(&cfg, fn, args);
 }
 
+// Launchers per consumer family, each instantiated in its own translation unit
+// (parallel builds): CUDA-core consumers, and mma.sync consumers (16-bit and E4M3).
 template <typename T>
-cudaError_t launch_typed(const Params& p, int d, int G, int path, int mode, bool pdl, int grid,
-                         cudaStream_t s) {
+cudaError_t launch_typed_ffma(const Params& p, int d, int G, int mode, bool pdl, int grid,
+                              cudaStream_t s) {
+#define FD_CASE(DD, GG) \
+  if (d == DD && G == GG) return launch_dgp<T, DD, GG, kPathFfma>(p, mode, pdl, grid, s);
+  FD_CASE(64, 1) FD_CASE(64, 2) FD_CASE(64, 4) FD_CASE(64, 8)
+  FD_CASE(128, 1) FD_CASE(128, 2) FD_CASE(128, 4) FD_CASE(128, 8)
+#undef FD_CASE
+  return cudaErrorInvalidValue;
+}
+
+template <typename T>
+cudaError_t launch_typed_mma(const Params& p, int d, int G, int path, int mode, bool pdl, int grid,
+                             cudaStream_t s) {
 #define FD_CASE(DD, GG, PP) \
   if (d == DD && G == GG && path == PP) return launch_dgp<T, DD, GG, PP>(p, mode, pdl, grid, s);
-  FD_CASE(64, 1, kPathFfma) FD_CASE(64, 2, kPathFfma) FD_CASE(64, 4, kPathFfma)
-  FD_CASE(64, 8, kPathFfma) FD_CASE(128, 1, kPathFfma) FD_CASE(128, 2, kPathFfma)
-  FD_CASE(128, 4, kPathFfma) FD_CASE(128, 8, kPathFfma)
   FD_CASE(64, 4, kPathMma) FD_CASE(64, 8, kPathMma) FD_CASE(64, 16, kPathMma)
   FD_CASE(128, 4, kPathMma) FD_CASE(128, 8, kPathMma) FD_CASE(128, 16, kPathMma)
   if constexpr (std::is_same<T, __half>::value) {

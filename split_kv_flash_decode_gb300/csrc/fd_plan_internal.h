@@ -40,14 +40,18 @@ inline int launch_status(cudaError_t err) {
              ? FD_ERR_UNSUPPORTED
              : FD_ERR_CUDA;
 }
-// One kernel launch of the plan's consumer path and dtype (mode as for launch_f16).
+// One kernel launch of the plan's consumer path and dtype (mode as listed above the
+// launcher declarations).
 inline cudaError_t launch_plan(const fd_plan_s* pl, const Params& p, int mode, int grid,
                                cudaStream_t s) {
   const bool pdl = !(pl->flags & FD_PLAN_NO_PDL);
   if (pl->path == kPathUmma)
     return pl->dtype == FD_BF16 ? launch_umma_bf16(p, pl->d, pl->G, mode, pdl, grid, s)
                                 : launch_umma_f16(p, pl->d, pl->G, mode, pdl, grid, s);
-  return pl->dtype == FD_BF16 ? launch_bf16(p, pl->d, pl->G, pl->path, mode, pdl, grid, s)
-                              : launch_f16(p, pl->d, pl->G, pl->path, mode, pdl, grid, s);
+  if (pl->path == kPathFfma)
+    return pl->dtype == FD_BF16 ? launch_bf16_ffma(p, pl->d, pl->G, mode, pdl, grid, s)
+                                : launch_f16_ffma(p, pl->d, pl->G, mode, pdl, grid, s);
+  return pl->dtype == FD_BF16 ? launch_bf16_mma(p, pl->d, pl->G, pl->path, mode, pdl, grid, s)
+                              : launch_f16_mma(p, pl->d, pl->G, pl->path, mode, pdl, grid, s);
 }
 }  // namespace fd
