@@ -65,6 +65,8 @@ def parse_args(argv=None):
                     help="mma.sync tensor cores where tcgen05 is the default (G = 16)")
     ap.add_argument("--cluster-combine", action="store_true",
                     help="combine each (sequence, KV head) pair inside one thread-block cluster")
+    ap.add_argument("--combiners", type=int, choices=[1, 2, 4, 8, 16], default=0,
+                    help="cap on the CTAs that share one pair's combine (0 = planner)")
     ap.add_argument("--no-pdl", action="store_true", help="launch without programmatic dependent launch")
     ap.add_argument("--no-cluster", action="store_true",
                     help="one partial record per chunk (no in-cluster segment merge)")
@@ -421,7 +423,8 @@ def plan_flags(fd, args, prob):
         fd.FD_PLAN_NO_CLUSTER if args.no_cluster else 0) | (fd.FD_PLAN_CLUSTER if args.cluster else 0) | (
         fd.FD_PLAN_TCGEN05 if args.tcgen05 else 0) | (
         fd.FD_PLAN_CLUSTER_COMBINE if args.cluster_combine else 0) | (
-        fd.FD_PLAN_MMA_SYNC if args.mma_sync else 0)
+        fd.FD_PLAN_MMA_SYNC if args.mma_sync else 0) | (
+        fd.FD_PLAN_COMBINERS[args.combiners] if args.combiners else 0)
 
 
 class CaseRun:
@@ -672,6 +675,7 @@ def run_fd(args):
                 "workload": prob.name, **prob.describe(), "accumulate": "f32",
                 "chunks_per_segment": info["chunks"], "ctas": info["ctas"],
                 "records_per_segment": info["records_per_segment"],
+                "combiners": info["combiners"],
                 "partials_per_sequence_max": info["max_partials"],
                 "kv_bytes_per_step": kv_bytes, "two_launch": bool(args.two_launch),
                 "kv_storage": prob.kv_type,
@@ -683,7 +687,9 @@ def run_fd(args):
                                  else (f"in a cluster of {info['combine_cluster']} CTAs per (sequence,"
                                        " KV head), distributed shared memory"
                                        if info["combine_cluster"] else
-                                       "last arriver (atomic counter)")),
+                                       ("last arriver (atomic counter)" if info["combiners"] == 1 else
+                                        f"the last {info['combiners']} arrivers (atomic counter),"
+                                        " split by query heads"))),
                 "consumer": {0: "FFMA (CUDA cores)", 1: "mma.sync m16n8k16 (tensor cores)",
                              2: "mma.sync m16n8k16 over E4M3 K/V widened in registers",
                              3: "tcgen05.mma (accumulators in tensor memory)"}[info["path"]],

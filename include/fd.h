@@ -12,7 +12,9 @@
  * TMA/mbarrier shared-memory ring, computes its partial, publishes it, and the
  * CTA that arrives last for a (sequence, KV head) combines all partials of
  * that pair (the pages' "fully fused" variant, with a release/acquire arrival
- * counter in place of the pages' remote inbox flags).
+ * counter in place of the pages' remote inbox flags).  When the whole grid is
+ * resident at once, the last few CTAs to arrive share that combine, each taking
+ * a slice of the pair's query heads (fd_plan_info.combiners).
  *
  * Result, for sequence b, query head h, KV head g = h / (Hq / Hkv):
  *   s_j = <q[b,h,:], K[cu_b + j, g, :]> / sqrt(d),  j = 0 .. L_b - 1
@@ -118,6 +120,26 @@ enum fd_status {
 /* The mma.sync tensor-core consumers even where tcgen05 is the default (G = 16 at
  * d = 128).  Not with FD_PLAN_TCGEN05 or FD_PLAN_FFMA. */
 #define FD_PLAN_MMA_SYNC 0x1000u
+/* Cap on the CTAs that share the combine of one (sequence, KV head) pair, in bits
+ * 16..18 of the flags: FD_PLAN_COMBINERS_n allows at most n.  Without one, the
+ * planner allows 8 for G >= 8 and 1 below.  A plan whose CTAs all fit on the
+ * device at once (at most SMs x resident CTAs per SM), run as one fused launch
+ * without clusters, lets the last `combiners` arrivals of each pair share its
+ * combine: the r-th CTA before the last waits (bounded, ~4 s) until the last one
+ * has arrived, then combines query heads [r * G / combiners, (r + 1) * G /
+ * combiners).  Each head is combined by the same code either way, so the results
+ * are bit-identical.  FD_PLAN_SINGLE_COMBINER (the last arriver alone) is the
+ * ablation.  num_sms must not exceed the device's SM count for such plans: a
+ * combiner could otherwise wait for a CTA that has no SM to run on, until its
+ * bounded wait gives up (FD_ERR_TIMEOUT). */
+#define FD_PLAN_COMBINERS_SHIFT 16
+#define FD_PLAN_COMBINERS_MASK (7u << FD_PLAN_COMBINERS_SHIFT)
+#define FD_PLAN_COMBINERS_1 (1u << FD_PLAN_COMBINERS_SHIFT)
+#define FD_PLAN_COMBINERS_2 (2u << FD_PLAN_COMBINERS_SHIFT)
+#define FD_PLAN_COMBINERS_4 (3u << FD_PLAN_COMBINERS_SHIFT)
+#define FD_PLAN_COMBINERS_8 (4u << FD_PLAN_COMBINERS_SHIFT)
+#define FD_PLAN_COMBINERS_16 (5u << FD_PLAN_COMBINERS_SHIFT)
+#define FD_PLAN_SINGLE_COMBINER FD_PLAN_COMBINERS_1
 
 /* Compiled limits. */
 #define FD_MAX_BATCH 256       /* sequences per plan */
@@ -295,6 +317,9 @@ typedef struct fd_plan_info {
                                   cluster) or chunks */
   int32_t combine_cluster; /* CTAs per cluster that combine a pair's partials in shared
                               memory (FD_PLAN_CLUSTER_COMBINE: W * chunks), else 0 */
+  int32_t combiners;       /* CTAs that share the combine of one pair: a power of two
+                              dividing G (fewer for a sequence with fewer partials),
+                              1 = the last arriver alone */
 } fd_plan_info;
 
 int fd_plan_get_info(fd_plan_t plan, fd_plan_info* info);

@@ -34,6 +34,9 @@ from ._binding import (  # noqa: F401
     FD_PLAN_TCGEN05,
     FD_PLAN_CLUSTER_COMBINE,
     FD_PLAN_MMA_SYNC,
+    FD_PLAN_SINGLE_COMBINER,
+    FD_PLAN_COMBINERS,
+    FD_PLAN_COMBINERS_MASK,
     FD_PLAN_WAITS,
     FD_PLAN_TWO_LAUNCH,
     FdError,

@@ -38,6 +38,11 @@ FD_PLAN_TEST_SKIP_TILE = 0x200
 FD_PLAN_TCGEN05 = 0x400
 FD_PLAN_CLUSTER_COMBINE = 0x800
 FD_PLAN_MMA_SYNC = 0x1000
+FD_PLAN_COMBINERS_SHIFT = 16
+FD_PLAN_COMBINERS_MASK = 7 << FD_PLAN_COMBINERS_SHIFT
+# FD_PLAN_COMBINERS[n]: at most n CTAs share the combine of one (sequence, KV head) pair.
+FD_PLAN_COMBINERS = {n: (k + 1) << FD_PLAN_COMBINERS_SHIFT for k, n in enumerate((1, 2, 4, 8, 16))}
+FD_PLAN_SINGLE_COMBINER = FD_PLAN_COMBINERS[1]
 FD_MAX_BATCH = 256
 FD_MAX_PARTIALS = 1024
 
@@ -67,7 +72,7 @@ class PlanInfo(ctypes.Structure):
         ("total_tokens", ctypes.c_int64), ("total_partials", ctypes.c_int64),
         ("workspace_bytes", ctypes.c_uint64), ("kv_bytes", ctypes.c_uint64),
         ("path", ctypes.c_int32), ("records_per_segment", ctypes.c_int32),
-        ("combine_cluster", ctypes.c_int32),
+        ("combine_cluster", ctypes.c_int32), ("combiners", ctypes.c_int32),
     ]
 
 

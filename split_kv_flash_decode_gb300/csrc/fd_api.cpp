@@ -22,6 +22,13 @@ constexpr size_t kAlign = 256;
 // 256-token chunks: the CUDA-core consumers of a CTA walk its tokens serially.
 constexpr int kMinChunkTokens = 128;
 constexpr int kMaxCluster = 8;        // portable thread-block cluster size
+// CTAs that share one pair's combine unless the flags cap them: 8 for GQA groups of
+// 8 or more (measured: the 128K-token G = 8 decode 79.4 against 80.0 us per step,
+// 85.1 against 89.1 us alone; G = 16 at 32K 25.0 against 25.5 us, over an FP8 cache
+// 18.9 against 20.9 us), the last arriver alone below (G = 4 at 32K: 22.7 against
+// 22.6 us, 14.4 against 14.2 us over FP8).
+constexpr int kDefaultCombiners = 8;
+constexpr int kMinGroupForCombiners = 8;
 
 size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 
@@ -114,8 +121,10 @@ int plan_impl(int B, int Hq, int Hkv, int d, const int32_t* seqlens, const int32
   if (flags & ~(FD_PLAN_LITERAL_W | FD_PLAN_DEBUG | FD_PLAN_TWO_LAUNCH | FD_PLAN_FFMA |
                 FD_PLAN_NO_PDL | FD_PLAN_WAITS | FD_PLAN_TEST_DROP_FLAG |
                 FD_PLAN_NO_CLUSTER | FD_PLAN_CLUSTER | FD_PLAN_TEST_SKIP_TILE | FD_PLAN_TCGEN05 |
-                FD_PLAN_CLUSTER_COMBINE | FD_PLAN_MMA_SYNC))
+                FD_PLAN_CLUSTER_COMBINE | FD_PLAN_MMA_SYNC | FD_PLAN_COMBINERS_MASK))
     return FD_ERR_INVALID;
+  const uint32_t combiners_code = (flags & FD_PLAN_COMBINERS_MASK) >> FD_PLAN_COMBINERS_SHIFT;
+  if (combiners_code > 5) return FD_ERR_INVALID;
   if ((flags & FD_PLAN_CLUSTER) && (flags & (FD_PLAN_NO_CLUSTER | FD_PLAN_WAITS)))
     return FD_ERR_INVALID;
   if ((flags & FD_PLAN_WAITS) && (flags & FD_PLAN_TWO_LAUNCH)) return FD_ERR_INVALID;
@@ -228,16 +237,30 @@ int plan_impl(int B, int Hq, int Hkv, int d, const int32_t* seqlens, const int32
   // Only the first wave can start before the previous kernel ends; later CTAs
   // would only queue prefetches ahead of their own loads.
   p.prefetch_ctas = (int32_t)std::min<int64_t>(ctas, (int64_t)num_sms * fd::ctas_per_sm_for(path));
-  // When the chunk records of one (sequence, KV head) would need several passes
-  // through the combine's shared memory (at least 2; 3 over an FP8 cache, whose
-  // shorter CTAs gain less than the cluster barriers cost), segments cut into 2..8
-  // chunks merge them inside a cluster (one record per segment).  Not in the
-  // fine-grained-waits variant, which combines chunk records as they arrive.
-  const int64_t rec_bytes = (int64_t)G * max_w * C * fd::record_floats(d) * 4;
+  // The last arrivals of a pair share its combine by query heads only when every CTA
+  // is resident at once (the CTAs they wait for then always run), in the fused
+  // one-launch mode; never more combiners than partials.
+  int nc = std::min(G, combiners_code            ? 1 << (combiners_code - 1)
+                      : G >= kMinGroupForCombiners ? kDefaultCombiners
+                                                   : 1);
+  {
+    const int64_t slots = (int64_t)num_sms * fd::ctas_per_sm_for(path);
+    if ((flags & (FD_PLAN_TWO_LAUNCH | FD_PLAN_WAITS)) || pair || ctas > slots) nc = 1;
+    while (nc > 1 && nc > max_w * C) nc >>= 1;
+  }
+  // When the chunk records one combiner reads would need several passes through the
+  // combine's shared memory (at least 2; 3 over an FP8 cache, whose shorter CTAs
+  // gain less than the cluster barriers cost), segments cut into 2..8 chunks merge
+  // them inside a cluster (one record per segment); the last arriver then combines
+  // alone.  Not in the fine-grained-waits variant, which combines chunk records as
+  // they arrive.
+  const int64_t rec_bytes = (int64_t)G / nc * max_w * C * fd::record_floats(d) * 4;
   const int64_t ring = (int64_t)fd::ring_bytes_for(pl->path, d);
   const bool multi_pass = rec_bytes > (pl->path == fd::kPathMmaKv8 ? 2 : 1) * ring;
   p.rps = ((multi_pass || (flags & FD_PLAN_CLUSTER)) && C > 1 && C <= kMaxCluster &&
            !(flags & (FD_PLAN_WAITS | FD_PLAN_NO_CLUSTER | FD_PLAN_CLUSTER_COMBINE))) ? 1 : C;
+  if (p.rps != C) nc = 1;
+  p.combiners = nc;
   p.pair_cluster = pair ? W[0] * C : 0;
   // Paged caches: boundaries on whole tiles, so that every TMA box stays in one page.
   p.align = page_size ? fd::tile_for(pl->path) : 1;
@@ -304,6 +327,7 @@ int fd_plan_get_info(fd_plan_t pl, fd_plan_info* info) {
   info->path = pl->path;
   info->records_per_segment = pl->params.rps;
   info->combine_cluster = pl->params.pair_cluster;
+  info->combiners = pl->params.combiners;
   return FD_OK;
 }
 

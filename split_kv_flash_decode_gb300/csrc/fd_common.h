@@ -135,6 +135,9 @@ struct Params {
   // CTAs per cluster when every partial of a (sequence, KV head) pair forms one
   // cluster and combines there (kernel mode 6): W * C, equal for every sequence.
   int32_t pair_cluster;
+  // CTAs that share the combine of one (sequence, KV head) pair: the last
+  // `combiners` arrivals (a power of two dividing G; 1 = the last arriver alone).
+  int32_t combiners;
   float scale_log2;    // log2(e) / sqrt(d)
   int32_t B, Hq, Hkv, C;
   int32_t cu[FD_MAX_BATCH + 1];         // token prefix sums

@@ -171,6 +171,23 @@ __device__ __forceinline__ void st_release_gpu(uint32_t* addr, uint32_t v) {
   asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(addr), "r"(v) : "memory");
 }
 
+// Poll `addr` with acquiring loads until it holds at least `target`; false after
+// kCombinerWaitNs (longer than any pipeline wait, so that a CTA whose own waits ran
+// out still arrives first).
+constexpr uint64_t kCombinerWaitNs = 4 * kWaitLimitNs;
+__device__ __forceinline__ bool wait_count_reaches(const uint32_t* addr, uint32_t target) {
+  if (ld_acquire_gpu(addr) >= target) return true;
+  const uint64_t start = global_timer_ns();
+  for (;;) {
+#pragma unroll 1
+    for (int i = 0; i < 16; ++i)
+      if (ld_acquire_gpu(addr) >= target) return true;
+    if (global_timer_ns() - start > kCombinerWaitNs) return false;
+  }
+}
+// finish_cta's role for a CTA that does not take part in the combine.
+constexpr int kNotCombiner = -1;
+
 __device__ __forceinline__ float ex2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
@@ -553,15 +570,16 @@ __device__ __forceinline__ void combine_from_smem(const Params& p, int b, int kv
 }
 
 // Same combine reading the records straight from L2 (for partial counts whose
-// records do not fit in shared memory); `coef` holds G * wtot + 3 * G floats.
+// records do not fit in shared memory), for query heads [ga, gb) of the pair;
+// `coef` holds G * wtot + 3 * G floats (indexed by the head within the pair).
 template <typename T, int D, int G>
 __device__ __forceinline__ void combine_from_global(const Params& p, int b, int kvh, int wtot,
-                                                    int64_t pbase, float* coef) {
+                                                    int64_t pbase, int ga, int gb, float* coef) {
   constexpr int RS = record_floats(D);
   float* ML = coef + G * wtot;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   constexpr int kWarps = kThreads / 32;
-  for (int g = warp; g < G; g += kWarps) {
+  for (int g = ga + warp; g < gb; g += kWarps) {
     const float* row = p.part + (pbase + (int64_t)(kvh * G + g) * wtot) * RS + D;
     float M = -INFINITY, lam = 0.f, lamr = 0.f;
     for (int w = lane; w < wtot; w += 32) {
@@ -586,7 +604,7 @@ __device__ __forceinline__ void combine_from_global(const Params& p, int b, int 
   }
   __syncthreads();
   T* out = reinterpret_cast<T*>(p.out);
-  for (int v = tid; v < G * (D / 4); v += kThreads) {
+  for (int v = ga * (D / 4) + tid; v < gb * (D / 4); v += kThreads) {
     const int g = v / (D / 4), c4 = v - (v / (D / 4)) * (D / 4);
     const float4* r =
         reinterpret_cast<const float4*>(p.part + (pbase + (int64_t)(kvh * G + g) * wtot) * RS) + c4;
@@ -616,31 +634,33 @@ __device__ __forceinline__ void combine_from_global(const Params& p, int b, int 
     }
     store_out4<T>(out + ((int64_t)b * p.Hq + kvh * G + g) * D + 4 * c4, a, ML[3 * g + 2]);
   }
-  if (tid < G && p.lse != nullptr) {
-    const float M = ML[3 * tid], lam = ML[3 * tid + 1];
-    p.lse[(int64_t)b * p.Hq + kvh * G + tid] = lam != 0.f ? (M + log2f(lam)) * kLn2 : -INFINITY;
+  if (ga + tid < gb && p.lse != nullptr) {
+    const int g = ga + tid;
+    const float M = ML[3 * g], lam = ML[3 * g + 1];
+    p.lse[(int64_t)b * p.Hq + kvh * G + g] = lam != 0.f ? (M + log2f(lam)) * kLn2 : -INFINITY;
   }
 }
 
-// Combine all partials of (b, kvh).  The records of as many heads as fit are
-// pulled into shared memory (`smem`, `smem_bytes`) with one bulk copy per pass,
-// completing on mbarrier `bar` (whose next phase parity is `phase`).
+// Combine all partials of (b, kvh) for query heads [ga, gb) of the pair.  The
+// records of as many heads as fit are pulled into shared memory (`smem`,
+// `smem_bytes`) with one bulk copy per pass, completing on mbarrier `bar` (whose
+// next phase parity is `phase`).
 template <typename T, int D, int G>
 __device__ __forceinline__ void combine_partials(const Params& p, int b, int kvh, int wtot,
-                                                 int64_t pbase, uint8_t* smem, uint32_t smem_bytes,
-                                                 uint32_t bar, uint32_t& phase) {
+                                                 int64_t pbase, int ga, int gb, uint8_t* smem,
+                                                 uint32_t smem_bytes, uint32_t bar, uint32_t& phase) {
   constexpr int RS = record_floats(D);
   // Per head: its records, plus its coefficients and two Lambdas (phase 1 scratch).
   const uint32_t head_bytes = (uint32_t)wtot * RS * 4;
   const uint32_t head_need = head_bytes + (uint32_t)(wtot + 2) * 4;
   const int hpp = head_bytes > 0 ? (int)min((uint32_t)G, smem_bytes / head_need) : 0;
   if (hpp == 0) {
-    combine_from_global<T, D, G>(p, b, kvh, wtot, pbase, reinterpret_cast<float*>(smem));
+    combine_from_global<T, D, G>(p, b, kvh, wtot, pbase, ga, gb, reinterpret_cast<float*>(smem));
     return;
   }
   float* rec = reinterpret_cast<float*>(smem);
-  for (int g0 = 0; g0 < G; g0 += hpp) {
-    const int ng = min(hpp, G - g0);
+  for (int g0 = ga; g0 < gb; g0 += hpp) {
+    const int ng = min(hpp, gb - g0);
     if (threadIdx.x == 0) {
       fence_proxy_async_global();
       const uint32_t bytes = (uint32_t)ng * head_bytes;
@@ -1014,20 +1034,38 @@ __device__ __forceinline__ void finish_cta(const Params& p, const Work& wk, floa
   // Arrival: the CTA's stores are ordered before thread 0's release by the barrier
   // (release is cumulative); the acquiring RMW makes every earlier CTA's record
   // visible to the last arriver, whose threads are ordered after it by the barrier.
+  // The last `nc` arrivals share the combine: arrival r before the last (r = 0 is
+  // the last) combines query heads [r G / nc, (r + 1) G / nc) once an acquiring load
+  // of the counter reads Wtot (the release sequence of the arrivals' RMWs makes
+  // every record visible to it).  Only a plan whose whole grid is resident at once
+  // has nc > 1, so the arrivals it waits for always run.
   __syncthreads();
   uint32_t* cnt = p.counters + (int64_t)wk.b * p.Hkv + wk.kvh;
+  int nc = p.combiners;
+  while (nc > wk.wtot) nc >>= 1;  // a power of two dividing G
   if (tid == 0) {
     const uint32_t old = atom_add_acq_rel_gpu(cnt, 1u);
     if (old >= (uint32_t)wk.wtot) atomicOr(p.status, kStatusCounter);
-    sm_last = (old == (uint32_t)(wk.wtot - 1));
+    const int r = wk.wtot - 1 - (int)min(old, (uint32_t)wk.wtot);
+    int role = (r >= 0 && r < nc) ? r : kNotCombiner;
+    if (role > 0 && !wait_count_reaches(cnt, (uint32_t)wk.wtot)) {
+      atomicOr(p.status, kStatusTimeout);
+      role = kNotCombiner;  // the workspace needs fd_workspace_init after this
+    }
+    sm_last = role;
   }
   __syncthreads();
-  if (sm_last) {
+  const int role = sm_last;
+  if (role >= 0) {
     // The records end before `crec`, which other CTAs of the cluster may still read.
     uint32_t phase = 0;
-    combine_partials<T, D, G>(p, wk.b, wk.kvh, wk.nrec, wk.pbase, combine_smem,
-                              combine_bytes - crec_bytes, combine_bar, phase);
-    if (tid == 0) *cnt = 0u;
+    const int hpc = G / nc;
+    combine_partials<T, D, G>(p, wk.b, wk.kvh, wk.nrec, wk.pbase, role * hpc, (role + 1) * hpc,
+                              combine_smem, combine_bytes - crec_bytes, combine_bar, phase);
+    if (tid == 0) {
+      // The counter returns to zero once every combiner has read Wtot from it.
+      if (nc == 1 || atomicAdd(cnt, 1u) == (uint32_t)(wk.wtot + nc - 1)) *cnt = 0u;
+    }
   }
   if (merge_seg) cluster_wait();
 }
@@ -1963,7 +2001,7 @@ __global__ void __launch_bounds__(kThreads, 2) fd_combine_kernel(const __grid_co
   __syncthreads();
   const int b = blockIdx.x / p.Hkv, kvh = blockIdx.x - (blockIdx.x / p.Hkv) * p.Hkv;
   uint32_t phase = 0;
-  combine_partials<T, D, G>(p, b, kvh, p.wseg[b] * p.rps, rec_base(p, b), smem, kBytes,
+  combine_partials<T, D, G>(p, b, kvh, p.wseg[b] * p.rps, rec_base(p, b), 0, G, smem, kBytes,
                             smem_addr(bar), phase);
 }
 

@@ -85,7 +85,8 @@ def test_plan_validation(args, code):
 def test_plan_bad_dtype_flags_chunks():
     assert _raw_plan(1, 8, 8, 128, [10], [1], dtype=3) == fd.FD_ERR_INVALID
     assert _raw_plan(1, 8, 8, 128, [10], [1], dtype=2) == fd.FD_ERR_UNSUPPORTED  # FP8 K/V: G >= 4
-    assert _raw_plan(1, 8, 8, 128, [10], [1], flags=0x10000) == fd.FD_ERR_INVALID
+    assert _raw_plan(1, 8, 8, 128, [10], [1], flags=0x80000) == fd.FD_ERR_INVALID
+    assert _raw_plan(1, 8, 8, 128, [10], [1], flags=6 << 16) == fd.FD_ERR_INVALID  # cap code 6
     assert _raw_plan(1, 8, 8, 128, [10], [1], flags=fd.FD_PLAN_CLUSTER | fd.FD_PLAN_NO_CLUSTER) == fd.FD_ERR_INVALID
     assert _raw_plan(1, 8, 8, 128, [10], [1], flags=fd.FD_PLAN_CLUSTER | fd.FD_PLAN_WAITS) == fd.FD_ERR_INVALID
     assert _raw_plan(1, 8, 8, 128, [10], [1], chunks=-1) == fd.FD_ERR_INVALID
@@ -168,29 +169,46 @@ def test_literal_w_and_auto_chunks():
 
 def test_records_per_segment():
     ring = {128: 96 * 1024, 64: 96 * 1024}   # K/V rings (bytes)
-    # Auto: chunk records merge per segment (in a cluster of 2..8 CTAs) exactly when one
-    # (sequence, KV head)'s records, G * W * C * (d + 4) * 4 bytes, exceed the ring
-    # (twice the ring over an FP8 cache).
+
+    def combiners(G, ctas, slots, partials):
+        nc = min(G, 8) if ctas <= slots and G >= 8 else 1
+        while nc > 1 and nc > partials:
+            nc //= 2
+        return nc
+    # Auto: chunk records merge per segment (in a cluster of 2..8 CTAs) exactly when the
+    # records one combiner reads, G / combiners * W * C * (d + 4) * 4 bytes, exceed the
+    # ring (twice the ring over an FP8 cache).
     for Hq, W, chunks in ((32, 8, 2), (32, 8, 5), (32, 8, 8), (64, 8, 4), (128, 8, 4),
                           (128, 8, 9), (32, 8, 1), (64, 8, 16)):
         p = fd.fd_plan(1, Hq, 8, 128, [32768], W, "f16", chunks=chunks, num_sms=152)
         G = Hq // 8
-        multi = G * W * chunks * 132 * 4 > ring[128]
+        slots = 152 if G == 16 else 304                     # tcgen05: one CTA per SM
+        nc = combiners(G, 8 * W * chunks, slots, W * chunks)
+        multi = G // nc * W * chunks * 132 * 4 > ring[128]
         want = 1 if (multi and 2 <= chunks <= 8) else chunks
         assert p.info["chunks"] == chunks and p.info["records_per_segment"] == want, (Hq, chunks)
-    # the default 32K GQA-4 plan fits one pass; GQA-8 at 128K does not
+        assert p.info["combiners"] == (1 if want != chunks else nc), (Hq, chunks)
+    # The default 32K GQA-4 and 128K GQA-8 plans fit one pass per combiner.
     assert fd.fd_plan(1, 32, 8, 128, [32768], 8, "f16", num_sms=152).info["records_per_segment"] == 4
-    assert fd.fd_plan(1, 64, 8, 128, [131072], 8, "f16", num_sms=152).info["records_per_segment"] == 1
-    fp8 = lambda Hq: fd.fd_plan(1, Hq, 8, 128, [131072], 8, "f16_e4m3kv", num_sms=152)  # noqa: E731
-    assert fp8(64).info["records_per_segment"] == 4 and fp8(128).info["records_per_segment"] == 1
+    assert fd.fd_plan(1, 64, 8, 128, [131072], 8, "f16", num_sms=152).info["records_per_segment"] == 4
+    fp8 = lambda Hq, f=0: fd.fd_plan(1, Hq, 8, 128, [131072], 8, "f16_e4m3kv", flags=f,  # noqa: E731
+                                     num_sms=152)
+    assert fp8(64).info["records_per_segment"] == 4 and fp8(128).info["records_per_segment"] == 4
+    # One combiner: G * W * C * 528 bytes = 270 KB for G = 16 (> 2 rings), 135 KB for G = 8.
+    assert fp8(64, fd.FD_PLAN_SINGLE_COMBINER).info["records_per_segment"] == 4
+    assert fp8(128, fd.FD_PLAN_SINGLE_COMBINER).info["records_per_segment"] == 1
     p = fd.fd_plan(1, 32, 8, 128, [32768], 8, "f16", flags=fd.FD_PLAN_CLUSTER, num_sms=152)
     assert p.info["chunks"] == 4 and p.info["records_per_segment"] == 1
     for flags in (fd.FD_PLAN_NO_CLUSTER, fd.FD_PLAN_WAITS):
-        p = fd.fd_plan(1, 64, 8, 128, [131072], 8, "f16", flags=flags, num_sms=152)
+        p = fd.fd_plan(1, 64, 8, 128, [131072], 8, "f16", flags=flags | fd.FD_PLAN_SINGLE_COMBINER,
+                       num_sms=152)
         assert p.info["chunks"] == 4 and p.info["records_per_segment"] == 4
     # paged plans follow the same rule; one chunk per segment never forms a cluster
-    p = fd.fd_plan_paged(1, 64, 8, 128, [131072], 8, 64, "f16", num_sms=152)
+    p = fd.fd_plan_paged(1, 64, 8, 128, [131072], 8, 64, "f16", num_sms=152,
+                         flags=fd.FD_PLAN_SINGLE_COMBINER)
     assert p.info["chunks"] == 4 and p.info["records_per_segment"] == 1
+    p = fd.fd_plan_paged(1, 64, 8, 128, [131072], 8, 64, "f16", num_sms=152)
+    assert p.info["records_per_segment"] == 4 and p.info["combiners"] == 8
     p = fd.fd_plan(1, 32, 8, 128, [32768], 8, "f16", flags=fd.FD_PLAN_CLUSTER | fd.FD_PLAN_LITERAL_W,
                    num_sms=152)
     assert p.info["chunks"] == 1 and p.info["records_per_segment"] == 1
@@ -320,3 +338,40 @@ def test_paged_plan_validation_and_alignment():
         assert L.fd_decode_paged(p.handle, 16, 16, 16, 100, 16, need - 1, 16, 0, 16, None) == fd.FD_ERR_INVALID
     c = fd.fd_plan(1, 8, 8, 64, [100], 1, "f16", num_sms=152)
     assert L.fd_decode_paged(c.handle, 16, 16, 16, 10, 16, 10, 16, 0, 16, None) == fd.FD_ERR_INVALID
+
+
+def test_shared_combine_plan_rules():
+    """The last arrivals of a pair share its combine by query heads only when the
+    whole grid is resident at once, in the fused launch without clusters; the count
+    is a power of two that divides G, at most the partials of the longest sequence."""
+    def info(*a, flags=0, **k):
+        return fd.fd_plan(*a, flags=flags, num_sms=152, **k).info
+    # 32K-token decodes: one wave on 152 SMs.  By default only groups of 8 or more
+    # share; a cap in the flags opens it to smaller groups.
+    assert info(1, 32, 8, 128, [32768], 8, "f16")["combiners"] == 1            # G = 4
+    assert info(1, 32, 8, 128, [32768], 8, "f16", flags=fd.FD_PLAN_COMBINERS[8])["combiners"] == 4
+    assert info(1, 64, 8, 128, [131072], 8, "f16", chunks=4,
+                flags=fd.FD_PLAN_NO_CLUSTER)["combiners"] == 8                  # G = 8
+    g16 = info(1, 128, 8, 128, [32768], 8, "f16")
+    assert g16["path"] == 3 and g16["ctas"] <= 152 and g16["combiners"] == 8   # G = 16, tcgen05
+    assert info(1, 8, 8, 64, [4096], 32, "f16", flags=fd.FD_PLAN_COMBINERS[16])["combiners"] == 1
+    # The flags cap it; FD_PLAN_SINGLE_COMBINER is the ablation.
+    for n in (1, 2, 4, 8, 16):
+        want = min(n, 16)
+        assert info(1, 128, 8, 128, [32768], 8, "f16", flags=fd.FD_PLAN_COMBINERS[n])["combiners"] == want
+    assert info(1, 64, 8, 128, [32768], 8, "f16",
+                flags=fd.FD_PLAN_SINGLE_COMBINER)["combiners"] == 1
+    # Never more combiners than partials: W = 2 literal partials, G = 16.
+    assert info(1, 128, 8, 128, [4096], 2, "bf16", flags=fd.FD_PLAN_LITERAL_W)["combiners"] == 2
+    # Several waves (B = 64 x 16 segments = 8192 CTAs), the other launch modes and
+    # clusters: the last arriver combines alone.
+    assert info(64, 32, 8, 128, [8192] * 64, 16, "bf16", flags=fd.FD_PLAN_LITERAL_W)["combiners"] == 1
+    for flags in (fd.FD_PLAN_TWO_LAUNCH, fd.FD_PLAN_WAITS, fd.FD_PLAN_CLUSTER,
+                  fd.FD_PLAN_CLUSTER_COMBINE):
+        assert info(1, 64, 8, 128, [32768], 8, "f16", flags=flags)["combiners"] == 1, hex(flags)
+    # 128K tokens, G = 8: the 8 combiners read one head's 32 records each, which fit in
+    # one pass, so the chunks need no cluster merge; with one combiner they do.
+    c3 = info(1, 64, 8, 128, [131072], 8, "f16")
+    assert c3["records_per_segment"] == 4 and c3["combiners"] == 8
+    c3 = info(1, 64, 8, 128, [131072], 8, "f16", flags=fd.FD_PLAN_SINGLE_COMBINER)
+    assert c3["records_per_segment"] == 1 and c3["combiners"] == 1

@@ -464,7 +464,7 @@ def test_fine_grained_waits_timeout_is_reported(fd):
 
 @pytest.mark.parametrize("G,flags", [(4, 0), (4, "two_launch"), (8, "cluster"), (1, 0),
                                      (8, "tcgen05"), (16, "tcgen05_cluster"),
-                                     (4, "cluster_combine")])
+                                     (4, "cluster_combine"), (4, "single_combiner")])
 def test_pipeline_wait_timeout_leaves_workspace_clean(fd, G, flags):
     """A tile that is never loaded (test hook): the consumers' bounded wait gives up,
     the status word says so, the CTA still publishes an (empty) partial and arrives, so
@@ -474,7 +474,8 @@ def test_pipeline_wait_timeout_leaves_workspace_clean(fd, G, flags):
     flag = {0: 0, "two_launch": fd.FD_PLAN_TWO_LAUNCH, "cluster": fd.FD_PLAN_CLUSTER,
             "tcgen05": fd.FD_PLAN_TCGEN05,
             "tcgen05_cluster": fd.FD_PLAN_TCGEN05 | fd.FD_PLAN_CLUSTER,
-            "cluster_combine": fd.FD_PLAN_CLUSTER_COMBINE}[flags]
+            "cluster_combine": fd.FD_PLAN_CLUSTER_COMBINE,
+            "single_combiner": fd.FD_PLAN_SINGLE_COMBINER}[flags]
     W = 4 if flags == "cluster_combine" else [4, 2]      # one W for every sequence there
     p = workloads.make_problem("skip", 2, 4 * G, 4, 128, [5000, 700], W, "f16", seed=42 + G)
     ref_out, ref_lse = oracle.decode_reference(p.q, p.k, p.v, p.seqlens, p.dtype)
@@ -502,6 +503,51 @@ def test_pipeline_wait_timeout_leaves_workspace_clean(fd, G, flags):
     fd.fd_decode(clean, q, k, v, out2, lse2, dec.workspace)
     assert fd.fd_workspace_status(clean, dec.workspace) == fd.FD_OK
     check(out_to_f64(out2), lse2.cpu().numpy().astype(np.float64), ref_out, ref_lse, dtype=p.dtype)
+
+
+# Shapes for the shared combine: (dtype, G, d, B, Hkv, seqlens, W, kind, combiners
+# wanted); groups below 8 share only under a cap in the flags (kind "cap").  Ragged partial counts give some sequences fewer combiners than others
+# (or none, W = 1 literal); Hkv = 1 with 300 literal partials sends each combiner's
+# head to the combine that reads the records from L2; 8 heads of 32 records per
+# combiner need two passes through the 96 KB ring.
+SHARED_COMBINE_CASES = {
+    "gqa4_f16": ("f16", 4, 128, 3, 8, [9000, 17, 4096], [4, 2, 8], "cap", 4),
+    "gqa8_bf16_literal": ("bf16", 8, 128, 3, 8, [9000, 300, 4096], [4, 1, 3], "literal", 4),
+    "gqa16_tcgen05": ("f16", 16, 128, 2, 4, [20000, 3000], [8, 3], "", 8),
+    "gqa16_two_passes": ("bf16", 16, 128, 1, 2, [40000], [8], "two_passes", 2),
+    "gqa4_from_l2": ("f16", 4, 128, 1, 1, [300 * 64], [300], "literal_cap", 4),
+    "gqa2_d64_ffma": ("bf16", 2, 64, 2, 8, [5000, 100], [4, 4], "cap", 2),
+    "gqa8_e4m3": ("e4m3", 8, 128, 3, 8, [7000, 0, 2049], [4, 2, 3], "", 8),
+}
+
+
+@pytest.mark.parametrize("case", list(SHARED_COMBINE_CASES))
+def test_shared_combine_matches_single_combiner(fd, case):
+    """The last arrivals of a pair share its combine by query heads: bit-identical to
+    the last arriver combining alone over the same records, and both agree with the
+    oracle.  (No cluster merge: a single combiner's plan could otherwise merge chunks
+    per segment, which changes the order of the sums.)"""
+    dtype, G, d, B, Hkv, seqlens, W, kind, want = SHARED_COMBINE_CASES[case]
+    base = workloads.make_problem("shared_combine", B, G * Hkv, Hkv, d, seqlens, W,
+                                  "f16" if dtype == "e4m3" else dtype, seed=130 + len(case))
+    p = workloads.with_e4m3_kv(base) if dtype == "e4m3" else base
+    flags, chunks = fd.FD_PLAN_NO_CLUSTER, 0
+    if kind.startswith("literal"):
+        flags |= fd.FD_PLAN_LITERAL_W
+    if kind.endswith("cap"):
+        flags |= fd.FD_PLAN_COMBINERS[16]
+    elif kind == "two_passes":
+        flags, chunks = flags | fd.FD_PLAN_MMA_SYNC | fd.FD_PLAN_COMBINERS[2], 4
+    ref_out, ref_lse = reference(p)
+    (o1, l1), dec = run_gpu(fd, p, flags=flags, chunks=chunks)
+    assert dec.info["combiners"] == want
+    check(o1, l1, ref_out, ref_lse, dtype=p.dtype)
+    single = (flags & ~fd.FD_PLAN_COMBINERS_MASK) | fd.FD_PLAN_SINGLE_COMBINER
+    (o2, l2), dec2 = run_gpu(fd, p, flags=single, chunks=chunks)
+    assert dec2.info["combiners"] == 1
+    assert dec2.info["records_per_segment"] == dec.info["records_per_segment"]
+    check(o2, l2, ref_out, ref_lse, dtype=p.dtype)
+    assert np.array_equal(o1, o2) and np.array_equal(l1, l2)
 
 
 def test_fine_grained_waits_needs_coresidency(fd):
