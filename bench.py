@@ -85,6 +85,8 @@ def parse_args(argv=None):
     ap.add_argument("--ref-budget-s", type=float, default=120.0)
     ap.add_argument("--no-graph", action="store_true", help="launch each step from Python")
     ap.add_argument("--no-extra", action="store_true", help="skip the 32K / 128K extra cases")
+    ap.add_argument("--no-read-floor", action="store_true",
+                    help="skip timing a plain read of the same bytes")
     ap.add_argument("--extra-steps", type=int, default=500)
     ap.add_argument("--cpu-baseline-only", action="store_true", help=argparse.SUPPRESS)
     return ap.parse_args(argv)
@@ -540,6 +542,81 @@ class CaseRun:
         return [x.elapsed_time(y) * 1e3 for x, y in evs]
 
 
+class ReadFloor:
+    """A plain read of the same number of bytes by a library kernel (torch's sum over
+    float32 words), timed like the decode: back to back, one event pair around each
+    launch, and alone after the same 2 x L2 flush.  It puts the single-decode figures
+    next to what any kernel reading those bytes achieves under the same events."""
+
+    def __init__(self, nbytes, l2, device, stream, steps):
+        import torch
+        self.stream, self.K = stream, steps
+        words = max(1, nbytes // 4)
+        copies = max(1, math.ceil(4 * l2 / max(nbytes, 1)))
+        copies = min(copies, max(1, int(20e9 // max(nbytes, 1))))
+        self.bufs = [torch.ones(words, dtype=torch.float32, device=device) for _ in range(copies)]
+        self.flush = torch.ones(2 * l2 // 4, dtype=torch.float32, device=device)
+        self.res = torch.empty((), dtype=torch.float32, device=device)
+        ev = lambda: torch.cuda.Event(enable_timing=True, external=True)  # noqa: E731
+        self.ev_all = (ev(), ev())
+        self.ev_b = [(ev(), ev()) for _ in range(steps)]
+        self.ev_c = [(ev(), ev()) for _ in range(steps)]
+        with torch.cuda.stream(stream):
+            for i in range(3):
+                torch.sum(self.bufs[i % len(self.bufs)], dim=0, out=self.res)
+        stream.synchronize()
+        self.graphs = {}
+        for name in ("a", "b", "c"):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                self._record(name)
+            self.graphs[name] = g
+        stream.synchronize()
+
+    def _record(self, name):
+        import torch
+        if name == "a":
+            self.ev_all[0].record(self.stream)
+        for i in range(self.K):
+            if name == "c":
+                self.flush_sum = self.flush.sum()
+            if name != "a":
+                (self.ev_b if name == "b" else self.ev_c)[i][0].record(self.stream)
+            torch.sum(self.bufs[i % len(self.bufs)], dim=0, out=self.res)
+            if name != "a":
+                (self.ev_b if name == "b" else self.ev_c)[i][1].record(self.stream)
+        if name == "a":
+            self.ev_all[1].record(self.stream)
+
+    def measure(self):
+        import torch
+        out = {}
+        with torch.cuda.stream(self.stream):
+            for name in ("a", "a", "b", "c"):
+                self.graphs[name].replay()
+                self.stream.synchronize()
+        out["step_us"] = self.ev_all[0].elapsed_time(self.ev_all[1]) * 1e3 / self.K
+        out["latency_us"] = statistics.median(x.elapsed_time(y) * 1e3 for x, y in self.ev_b)
+        out["isolated_us"] = statistics.median(x.elapsed_time(y) * 1e3 for x, y in self.ev_c)
+        out["what"] = ("torch.sum over the same number of bytes (float32), same three "
+                       "graphs and events as the decode; medians")
+        return out
+
+
+def read_floor(nbytes, l2, device, stream, steps):
+    """ReadFloor figures, or None where CUDA-graph timing events are unavailable."""
+    import torch
+    try:
+        torch.cuda.Event(enable_timing=True, external=True)
+    except TypeError:
+        return None
+    rf = ReadFloor(nbytes, l2, device, stream, steps)
+    out = rf.measure()
+    del rf
+    torch.cuda.empty_cache()
+    return out
+
+
 def stats_us(xs):
     qs = sorted(xs)
 
@@ -571,6 +648,7 @@ def extra_case(fd, args, name, device, stream, peak):
     if run.dec.status() != fd.FD_OK:
         raise RuntimeError(f"device status word reported an error on {name}")
     kv = prob.kv_bytes
+    l2 = run.l2
     out = {"workload": prob.name, "kv_bytes_per_step": kv, "steps": run.K,
            "ctas": run.dec.info["ctas"], "chunks_per_segment": run.dec.info["chunks"],
            "step_us": step_us, "step_gbs": kv / (step_us * 1e-6) / 1e9,
@@ -583,6 +661,8 @@ def extra_case(fd, args, name, device, stream, peak):
     del run
     import torch
     torch.cuda.empty_cache()
+    if not args.no_read_floor:
+        out["plain_read"] = read_floor(kv, l2, device, stream, min(max(1, args.extra_steps), 200))
     return out
 
 
@@ -651,6 +731,7 @@ def run_fd(args):
     info = dec.info
     del run
     torch.cuda.empty_cache()
+    floor = None if args.no_read_floor else read_floor(kv_bytes, l2, device, stream, min(K, 200))
 
     extras = {}
     if not args.no_extra and world == 1 and not args.paged:
@@ -706,6 +787,7 @@ def run_fd(args):
                                           "unrelated kernel) before each, events around the "
                                           "decode only (third replay)"},
             "step_us": step_us,
+            "plain_read": floor,
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak,
                          "traffic": load_traffic(prob.name, kernel_label),
