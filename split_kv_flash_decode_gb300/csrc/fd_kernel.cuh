@@ -453,119 +453,75 @@ __device__ __forceinline__ float warp_sum(float x) {
   return x;
 }
 
-// Maximum over the warp (floating-point redux; NaN inputs are ignored, like fmaxf).
-__device__ __forceinline__ float warp_max_redux(float x) {
-  float r;
-  asm volatile("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(x));
-  return r;
-}
 
 // OnlineSoftmaxCombine of the Wtot partials of (b, kvh) for query heads
 // [g0, g0 + ng), from their records in shared memory, head-major
-// [ng][wtot][D + 4].  Two phases over all threads.
-//   (1) Per head: M = max of the partial maxima, coef_w = exp2(m_w - M) into
-//       `coef` ([ng][wtot]), Lambda = sum_w coef_w l_w and Lambda~ = sum_w coef_w l~_w
-//       in a fixed shuffle tree, lse = M + log Lambda.  With at most 16 partials a
-//       warp takes several heads at once (lanes = head x partial, segmented
-//       reductions); otherwise one warp per head.
-//   (2) Every thread owns one (head, 4 output dimensions) slice and sums
-//       coef_w O_w over the partials in index order, its loads independent of each
-//       other; out = that sum times 1 / Lambda~ (the weights P.V multiplied).
-// The order of every sum is fixed, so the result does not depend on the order in
-// which the partials arrived.  (Measured: the chain of dependent shuffles of phase
-// 1 costs ~900 cycles per round of heads, so packing 16 heads of 8 partials into one
-// round instead of four, and one reciprocal instead of four divisions per slice,
-// shorten the last arriver's combine.)
+// [ng][wtot][D + 4].  Every thread owns one (head, 4 output dimensions) slice and
+// works alone, with no barrier and no shuffle: it reads the partial maxima of its
+// head (broadcast loads within the warp) for M, then walks the partials in index
+// order, computing coef_w = exp2(m_w - M) and summing coef_w O_w, Lambda =
+// sum_w coef_w l_w and Lambda~ = sum_w coef_w l~_w; out = the O sum times 1 /
+// Lambda~ (the weights P.V multiplied), lse = M + log Lambda.  Every thread of a
+// head computes the same M and Lambdas in the same order, and every sum runs in
+// index order, so the result does not depend on the order in which the partials
+// arrived.  (Measured on 4 heads x 32 partials: a two-phase form, coefficients by
+// one warp per head with shuffle reductions, a barrier, then the weighted sums,
+// took ~2200 cycles, most of it in chains of dependent shuffles; this form keeps
+// every load of a thread independent.)
 template <typename T, int D, int G>
 __device__ __forceinline__ void combine_from_smem(const Params& p, int b, int kvh, int wtot,
-                                                  int g0, int ng, const float* rec, float* coef) {
+                                                  int g0, int ng, const float* rec) {
   constexpr int RS = record_floats(D);
-  constexpr int Q = D / 4;   // float4 columns per head
-  constexpr int U = 8;       // partials in flight per thread
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  constexpr int kWarps = kThreads / 32;
-  float* lams = coef + (size_t)ng * wtot;  // [ng][2]: Lambda, 1 / Lambda~
-  auto finish_head = [&](int g, float M, float lam, float lamr) {
-    lams[2 * g] = lam;
-    lams[2 * g + 1] = lamr != 0.f ? 1.f / lamr : 0.f;  // no token: out = 0 (NaN stays NaN)
-    if (p.lse != nullptr)
-      p.lse[(int64_t)b * p.Hq + kvh * G + g0 + g] = lam != 0.f ? (M + log2f(lam)) * kLn2 : -INFINITY;
-  };
-  if (wtot <= 16) {
-    // S lanes per head (a power of two >= wtot), 32 / S heads per warp.
-    const int S = wtot <= 2 ? 2 : wtot <= 4 ? 4 : wtot <= 8 ? 8 : 16;
-    const int hpw = 32 / S;
-    const int w = lane & (S - 1);
-    for (int gb = warp * hpw; gb < ng; gb += kWarps * hpw) {
-      const int g = gb + lane / S;
-      const bool valid = g < ng && w < wtot;
-      float4 ml = make_float4(-INFINITY, 0.f, 0.f, 0.f);
-      if (valid) ml = *reinterpret_cast<const float4*>(rec + ((size_t)g * wtot + w) * RS + D);
-      float M = ml.x;
-      for (int off = 1; off < S; off <<= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
-      const float c = (valid && M != -INFINITY) ? ex2(ml.x - M) : 0.f;
-      if (valid) coef[(size_t)g * wtot + w] = c;
-      float lam = c * ml.y, lamr = c * ml.z;
-      for (int off = 1; off < S; off <<= 1) {
-        lam += __shfl_xor_sync(0xffffffffu, lam, off);
-        lamr += __shfl_xor_sync(0xffffffffu, lamr, off);
-      }
-      if (w == 0 && g < ng) finish_head(g, M, lam, lamr);
-    }
-  } else {
-    for (int g = warp; g < ng; g += kWarps) {
-      const float* rg = rec + (size_t)g * wtot * RS + D;
-      float M = -INFINITY;
-      for (int w = lane; w < wtot; w += 32) M = fmaxf(M, rg[(size_t)w * RS]);
-      M = warp_max_redux(M);
-      float lam = 0.f, lamr = 0.f;
-      for (int w = lane; w < wtot; w += 32) {
-        const float4 ml = *reinterpret_cast<const float4*>(rg + (size_t)w * RS);
-        const float c = M == -INFINITY ? 0.f : ex2(ml.x - M);  // exp2(-inf) = 0: empty partial
-        coef[(size_t)g * wtot + w] = c;
-        lam = fmaf(c, ml.y, lam);
-        lamr = fmaf(c, ml.z, lamr);
-      }
-      lam = warp_sum(lam);
-      lamr = warp_sum(lamr);
-      if (lane == 0) finish_head(g, M, lam, lamr);
-    }
-  }
-  __syncthreads();
+  constexpr int Q = D / 4;  // float4 columns per head
+  constexpr int U = 8;      // partials in flight per thread
   T* out = reinterpret_cast<T*>(p.out);
-  for (int i = tid; i < ng * Q; i += kThreads) {
+  for (int i = threadIdx.x; i < ng * Q; i += kThreads) {
     const int g = i / Q, c4 = i - (i / Q) * Q;
-    const float* base = rec + (size_t)g * wtot * RS + 4 * c4;
-    const float* cg = coef + (size_t)g * wtot;
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    const float* rg = rec + (size_t)g * wtot * RS;
+    // M: the largest partial maximum (fmaxf skips NaN maxima; an empty partial has
+    // m = -inf).  Four independent running maxima keep the loads in flight.
+    float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
     int w = 0;
-    for (; w + U <= wtot; w += U) {
-      float4 x[U];
+    for (; w + 4 <= wtot; w += 4) {
 #pragma unroll
-      for (int u = 0; u < U; ++u) x[u] = *reinterpret_cast<const float4*>(base + (size_t)(w + u) * RS);
-#pragma unroll
-      for (int u = 0; u < U; ++u) {
-        const float c = cg[w + u];
-        acc.x = fmaf(c, x[u].x, acc.x);
-        acc.y = fmaf(c, x[u].y, acc.y);
-        acc.z = fmaf(c, x[u].z, acc.z);
-        acc.w = fmaf(c, x[u].w, acc.w);
-      }
+      for (int u = 0; u < 4; ++u) m4[u] = fmaxf(m4[u], rg[(size_t)(w + u) * RS + D]);
     }
-    for (; w < wtot; ++w) {
-      const float4 x = *reinterpret_cast<const float4*>(base + (size_t)w * RS);
-      const float c = cg[w];
+    for (; w < wtot; ++w) m4[0] = fmaxf(m4[0], rg[(size_t)w * RS + D]);
+    const float M = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+    const bool none = M == -INFINITY;  // no token in any partial: coefficients 0
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    float lam = 0.f, lamr = 0.f;
+    auto add = [&](const float4& ml, const float4& x) {
+      const float c = none ? 0.f : ex2(ml.x - M);
       acc.x = fmaf(c, x.x, acc.x);
       acc.y = fmaf(c, x.y, acc.y);
       acc.z = fmaf(c, x.z, acc.z);
       acc.w = fmaf(c, x.w, acc.w);
+      lam = fmaf(c, ml.y, lam);
+      lamr = fmaf(c, ml.z, lamr);
+    };
+    w = 0;
+    for (; w + U <= wtot; w += U) {
+      float4 ml[U], x[U];
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const float* r = rg + (size_t)(w + u) * RS;
+        ml[u] = *reinterpret_cast<const float4*>(r + D);
+        x[u] = *reinterpret_cast<const float4*>(r + 4 * c4);
+      }
+#pragma unroll
+      for (int u = 0; u < U; ++u) add(ml[u], x[u]);
     }
-    const float inv = lams[2 * g + 1];
+    for (; w < wtot; ++w) {
+      const float* r = rg + (size_t)w * RS;
+      add(*reinterpret_cast<const float4*>(r + D), *reinterpret_cast<const float4*>(r + 4 * c4));
+    }
+    const float inv = lamr != 0.f ? 1.f / lamr : 0.f;  // no token: out = 0 (NaN stays NaN)
     T* dst = out + ((int64_t)b * p.Hq + kvh * G + g0 + g) * D + 4 * c4;
-    dst[0] = Elem<T>::from_f(acc.x * inv);
-    dst[1] = Elem<T>::from_f(acc.y * inv);
-    dst[2] = Elem<T>::from_f(acc.z * inv);
-    dst[3] = Elem<T>::from_f(acc.w * inv);
+    *reinterpret_cast<uint2*>(dst) =
+        make_uint2(pack2<T>(acc.x * inv, acc.y * inv), pack2<T>(acc.z * inv, acc.w * inv));
+    if (c4 == 0 && p.lse != nullptr)
+      p.lse[(int64_t)b * p.Hq + kvh * G + g0 + g] = lam != 0.f ? (M + log2f(lam)) * kLn2 : -INFINITY;
   }
 }
 
@@ -650,10 +606,9 @@ __device__ __forceinline__ void combine_partials(const Params& p, int b, int kvh
                                                  int64_t pbase, int ga, int gb, uint8_t* smem,
                                                  uint32_t smem_bytes, uint32_t bar, uint32_t& phase) {
   constexpr int RS = record_floats(D);
-  // Per head: its records, plus its coefficients and two Lambdas (phase 1 scratch).
+  // Heads per pass: as many heads' records as fit in the shared memory.
   const uint32_t head_bytes = (uint32_t)wtot * RS * 4;
-  const uint32_t head_need = head_bytes + (uint32_t)(wtot + 2) * 4;
-  const int hpp = head_bytes > 0 ? (int)min((uint32_t)G, smem_bytes / head_need) : 0;
+  const int hpp = head_bytes > 0 ? (int)min((uint32_t)G, smem_bytes / head_bytes) : 0;
   if (hpp == 0) {
     combine_from_global<T, D, G>(p, b, kvh, wtot, pbase, ga, gb, reinterpret_cast<float*>(smem));
     return;
@@ -673,8 +628,7 @@ __device__ __forceinline__ void combine_partials(const Params& p, int b, int kvh
     }
     if (!mbar_wait(bar, phase)) atomicOr(p.status, kStatusTimeout);
     phase ^= 1u;
-    combine_from_smem<T, D, G>(p, b, kvh, wtot, g0, ng, rec,
-                               rec + (size_t)ng * wtot * RS);
+    combine_from_smem<T, D, G>(p, b, kvh, wtot, g0, ng, rec);
     __syncthreads();  // the next pass overwrites the records
   }
 }
