@@ -101,12 +101,13 @@ enum fd_status {
 #define FD_PLAN_TEST_SKIP_TILE 0x200u
 /* Fifth-generation tensor cores (tcgen05.mma with accumulators in tensor memory)
  * for the scores and P.V: 128-token tiles, d = 128, G in {4, 8, 16}, fp16 or bf16
- * (FD_ERR_UNSUPPORTED otherwise).  The default for G = 16 at d = 128; this flag
- * selects it for G = 4 and 8 too.  A kernel with tcgen05 instructions is resident
- * one CTA per SM, so these plans size their grid for one CTA per SM and give it a
- * 192 KB K/V ring.  S^T = K Q^T runs with the tokens on M and the
- * heads, padded to 16, on N, straight from the TMA-swizzled K tile; P^T is staged
- * in shared memory; O^T = V^T P^T accumulates in tensor memory. */
+ * (FD_ERR_UNSUPPORTED otherwise).  Not the default: mma.sync measured faster on
+ * every decode case measured once the combine is shared (G = 16 at 32K tokens: 24.9 against
+ * 24.2 us).  A kernel with tcgen05 instructions is resident one CTA per SM, so these
+ * plans size their grid for one CTA per SM and give it a 192 KB K/V ring.
+ * S^T = K Q^T runs with the tokens on M and the heads, padded to 16, on N, straight
+ * from the TMA-swizzled K tile; P^T is staged in shared memory; O^T = V^T P^T
+ * accumulates in tensor memory. */
 #define FD_PLAN_TCGEN05 0x400u
 /* Combine in a thread-block cluster: the W * C partial CTAs of each (sequence, KV
  * head) pair run as one cluster (at most 16 CTAs), keep their partials in shared
@@ -117,8 +118,8 @@ enum fd_status {
  * FD_PLAN_WAITS, FD_PLAN_TWO_LAUNCH, FD_PLAN_CLUSTER or FD_PLAN_NO_CLUSTER.  A
  * device that cannot place the clusters makes fd_decode return FD_ERR_UNSUPPORTED. */
 #define FD_PLAN_CLUSTER_COMBINE 0x800u
-/* The mma.sync tensor-core consumers even where tcgen05 is the default (G = 16 at
- * d = 128).  Not with FD_PLAN_TCGEN05 or FD_PLAN_FFMA. */
+/* The mma.sync tensor-core consumers (the default for G >= 4; the flag pins that
+ * choice).  Not with FD_PLAN_TCGEN05 or FD_PLAN_FFMA. */
 #define FD_PLAN_MMA_SYNC 0x1000u
 /* Cap on the CTAs that share the combine of one (sequence, KV head) pair, in bits
  * 16..18 of the flags: FD_PLAN_COMBINERS_n allows at most n.  Without one, the

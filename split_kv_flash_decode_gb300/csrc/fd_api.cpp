@@ -146,12 +146,12 @@ int plan_impl(int B, int Hq, int Hkv, int d, const int32_t* seqlens, const int32
       (dtype == FD_F16_E4M3KV || d != 128 || G < 4 || (flags & (FD_PLAN_FFMA | FD_PLAN_MMA_SYNC))))
     return FD_ERR_UNSUPPORTED;
   if ((flags & FD_PLAN_MMA_SYNC) && (flags & FD_PLAN_FFMA)) return FD_ERR_INVALID;
-  // Tensor cores whenever the GQA group covers at least half of the mma N = 8 tile.
-  // tcgen05 by default where it was measured faster: G = 16 at d = 128 (a 32K decode
-  // in 26.5 us against 27.5 us for two mma.sync N tiles).
-  const bool umma = (flags & FD_PLAN_TCGEN05) ||
-                    (G == 16 && d == 128 && dtype != FD_F16_E4M3KV &&
-                     !(flags & (FD_PLAN_MMA_SYNC | FD_PLAN_FFMA)));
+  // Tensor cores whenever the GQA group covers at least half of the mma N = 8 tile:
+  // mma.sync by default, tcgen05 when asked for.  tcgen05 was the default for G = 16
+  // until the combine was shared among the last arrivals: then two mma.sync N tiles
+  // (256 CTAs, two per SM) decode 32K tokens in 24.2 us against 24.9 us on tcgen05
+  // (128 CTAs, one per SM), the same box, three runs each.
+  const bool umma = (flags & FD_PLAN_TCGEN05) != 0;
   const int path = dtype == FD_F16_E4M3KV                 ? fd::kPathMmaKv8
                    : umma                                 ? fd::kPathUmma
                    : (G >= 4 && !(flags & FD_PLAN_FFMA)) ? fd::kPathMma

@@ -75,9 +75,10 @@ FD_HD constexpr int ring_slots_for(int path, int d) { return ring_target_bytes(p
 FD_HD constexpr size_t ring_bytes_for(int path, int d) {
   return (size_t)ring_slots_for(path, d) * slot_bytes_for(path, d);
 }
-// Bytes after the ring: 2 mbarriers per slot, the combine's mbarrier, two flags,
-// the tcgen05 path's two mbarriers and tensor-memory address, and up to 1 KB of
-// slack for aligning the ring to 1024 bytes.
+// Bytes after the ring: 2 mbarriers per slot, an unused word, two flags, the
+// tcgen05 path's two mbarriers and tensor-memory address, the combine's 16
+// mbarriers (one per head of a pass), and up to 1 KB of slack for aligning the ring
+// to 1024 bytes.
 constexpr int kRingMetaBytes = 2048;
 // The tcgen05 path's operands outside the ring: Q (16 x 128, 4 KB), P^T (128 x 16,
 // 4 KB) and 1 KB of reduction scratch.

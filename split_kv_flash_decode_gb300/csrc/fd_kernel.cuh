@@ -54,6 +54,7 @@ namespace dev {
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale when the max grows by > 2^8
 constexpr float kLn2 = 0.693147180559945309417f;
 constexpr uint64_t kWaitLimitNs = 1000000000ull;  // bounded waits give up after ~1 s
+constexpr int kCombineBars = 16;  // mbarriers of the combine's copies (one per head of a pass)
 constexpr uint32_t kTmemCols = 64;   // tensor-memory columns per CTA (tcgen05 path)
 constexpr uint32_t kColS = 0;        // S^T [128 tokens][16 heads]
 constexpr uint32_t kColO = 32;       // O^T [128 dims][16 heads]
@@ -470,13 +471,17 @@ __device__ __forceinline__ float warp_sum(float x) {
 // every load of a thread independent.)
 template <typename T, int D, int G>
 __device__ __forceinline__ void combine_from_smem(const Params& p, int b, int kvh, int wtot,
-                                                  int g0, int ng, const float* rec) {
+                                                  int g0, int ng, const float* rec, uint32_t bars,
+                                                  uint32_t phase) {
   constexpr int RS = record_floats(D);
   constexpr int Q = D / 4;  // float4 columns per head
   constexpr int U = 8;      // partials in flight per thread
   T* out = reinterpret_cast<T*>(p.out);
   for (int i = threadIdx.x; i < ng * Q; i += kThreads) {
     const int g = i / Q, c4 = i - (i / Q) * Q;
+    // This head's records have landed (the copy of each head completes on its own
+    // barrier, so the first heads are combined while the later ones still arrive).
+    if (!mbar_wait(bars + 8u * (uint32_t)g, phase)) atomicOr(p.status, kStatusTimeout);
     const float* rg = rec + (size_t)g * wtot * RS;
     // M: the largest partial maximum (fmaxf skips NaN maxima; an empty partial has
     // m = -inf).  Four independent running maxima keep the loads in flight.
@@ -599,16 +604,17 @@ __device__ __forceinline__ void combine_from_global(const Params& p, int b, int 
 
 // Combine all partials of (b, kvh) for query heads [ga, gb) of the pair.  The
 // records of as many heads as fit are pulled into shared memory (`smem`,
-// `smem_bytes`) with one bulk copy per pass, completing on mbarrier `bar` (whose
-// next phase parity is `phase`).
+// `smem_bytes`) in each pass, head j of the pass by bulk copies that complete on
+// mbarrier `bars` + 8 j (kCombineBars of them, all at the next phase parity
+// `phase`).
 template <typename T, int D, int G>
 __device__ __forceinline__ void combine_partials(const Params& p, int b, int kvh, int wtot,
                                                  int64_t pbase, int ga, int gb, uint8_t* smem,
-                                                 uint32_t smem_bytes, uint32_t bar, uint32_t& phase) {
+                                                 uint32_t smem_bytes, uint32_t bars, uint32_t& phase) {
   constexpr int RS = record_floats(D);
   // Heads per pass: as many heads' records as fit in the shared memory.
   const uint32_t head_bytes = (uint32_t)wtot * RS * 4;
-  const int hpp = head_bytes > 0 ? (int)min((uint32_t)G, smem_bytes / head_bytes) : 0;
+  const int hpp = head_bytes > 0 ? (int)min((uint32_t)min(G, kCombineBars), smem_bytes / head_bytes) : 0;
   if (hpp == 0) {
     combine_from_global<T, D, G>(p, b, kvh, wtot, pbase, ga, gb, reinterpret_cast<float*>(smem));
     return;
@@ -618,17 +624,18 @@ __device__ __forceinline__ void combine_partials(const Params& p, int b, int kvh
     const int ng = min(hpp, gb - g0);
     if (threadIdx.x == 0) {
       fence_proxy_async_global();
-      const uint32_t bytes = (uint32_t)ng * head_bytes;
-      mbar_arrive_expect_tx(bar, bytes);
       const uint8_t* src = reinterpret_cast<const uint8_t*>(
           p.part + (pbase + (int64_t)(kvh * G + g0) * wtot) * RS);
       const uint32_t dst = smem_addr(smem);
-      for (uint32_t off = 0; off < bytes; off += 32768u)
-        bulk_load(dst + off, src + off, min(32768u, bytes - off), bar);
+      for (int j = 0; j < ng; ++j) {
+        const uint32_t bar = bars + 8u * (uint32_t)j, h0 = (uint32_t)j * head_bytes;
+        mbar_arrive_expect_tx(bar, head_bytes);
+        for (uint32_t off = 0; off < head_bytes; off += 32768u)
+          bulk_load(dst + h0 + off, src + h0 + off, min(32768u, head_bytes - off), bar);
+      }
     }
-    if (!mbar_wait(bar, phase)) atomicOr(p.status, kStatusTimeout);
+    combine_from_smem<T, D, G>(p, b, kvh, wtot, g0, ng, rec, bars, phase);
     phase ^= 1u;
-    combine_from_smem<T, D, G>(p, b, kvh, wtot, g0, ng, rec);
     __syncthreads();  // the next pass overwrites the records
   }
 }
@@ -885,7 +892,7 @@ __device__ __forceinline__ void combine_in_cluster(const Params& p, const Work& 
 template <typename T, int D, int G, int NGRP, int MODE, bool SEG, bool PAIR>
 __device__ __forceinline__ void finish_cta(const Params& p, const Work& wk, float* sm_acc,
                                            int& sm_last, bool aborted, uint8_t* combine_smem,
-                                           uint32_t combine_bytes, uint32_t combine_bar) {
+                                           uint32_t combine_bytes, uint32_t combine_bars) {
   float* sm_m = sm_acc + NGRP * G * D;  // [NGRP][G]
   float* sm_l = sm_m + NGRP * G;        // [NGRP][G]
   float* sm_lr = sm_l + NGRP * G;       // [NGRP][G]
@@ -1006,6 +1013,10 @@ __device__ __forceinline__ void finish_cta(const Params& p, const Work& wk, floa
       atomicOr(p.status, kStatusTimeout);
       role = kNotCombiner;  // the workspace needs fd_workspace_init after this
     }
+    if (role >= 0) {  // only a combining CTA pays for its copy barriers
+      for (int j = 0; j < kCombineBars; ++j) mbar_init(combine_bars + 8u * j, 1);
+      fence_mbar_init();
+    }
     sm_last = role;
   }
   __syncthreads();
@@ -1015,7 +1026,7 @@ __device__ __forceinline__ void finish_cta(const Params& p, const Work& wk, floa
     uint32_t phase = 0;
     const int hpc = G / nc;
     combine_partials<T, D, G>(p, wk.b, wk.kvh, wk.nrec, wk.pbase, role * hpc, (role + 1) * hpc,
-                              combine_smem, combine_bytes - crec_bytes, combine_bar, phase);
+                              combine_smem, combine_bytes - crec_bytes, combine_bars, phase);
     if (tid == 0) {
       // The counter returns to zero once every combiner has read Wtot from it.
       if (nc == 1 || atomicAdd(cnt, 1u) == (uint32_t)(wk.wtot + nc - 1)) *cnt = 0u;
@@ -1045,7 +1056,7 @@ __global__ void __launch_bounds__(kThreads, 2) fd_split_kernel(const __grid_cons
   constexpr uint32_t kRing = NSLOT * kSlotBytes;
   constexpr uint32_t kExtra = extra_bytes_for(PATH);
   static_assert(NSLOT >= 2 && kRowsBytes % 1024 == 0, "slots hold whole swizzle atoms");
-  static_assert((2 * NSLOT + 5) * 8 + 1024 <= kRingMetaBytes, "ring metadata must fit");
+  static_assert((2 * NSLOT + 5 + kCombineBars) * 8 + 1024 <= kRingMetaBytes, "ring metadata must fit");
   static_assert(kRing == ring_bytes_for(PATH, D), "ring layout");
   constexpr int NGRP_FFMA = kConsumerWarps * (32 / ((G * D > 512) ? 16 : 8));
   constexpr int NGRP = PATH == kPathUmma ? 1 : is_mma(PATH) ? kConsumerWarps : NGRP_FFMA;
@@ -1065,6 +1076,7 @@ __global__ void __launch_bounds__(kThreads, 2) fd_split_kernel(const __grid_cons
   const uint32_t bar_s = smem_addr(bars + 2 * NSLOT + 2);
   const uint32_t bar_o = smem_addr(bars + 2 * NSLOT + 3);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * NSLOT + 4);
+  const uint32_t combine_bars = smem_addr(bars + 2 * NSLOT + 5);  // kCombineBars of them
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   pdl_launch_dependents();
@@ -1077,7 +1089,6 @@ __global__ void __launch_bounds__(kThreads, 2) fd_split_kernel(const __grid_cons
       // Released by every consumer warp, or by one tcgen05 commit.
       mbar_init(empty_bar(s), PATH == kPathUmma ? 1 : kConsumerWarps);
     }
-    mbar_init(smem_addr(bars + 2 * NSLOT), 1);  // combine copies
     if (PATH == kPathUmma) {
       mbar_init(bar_s, 1);
       mbar_init(bar_o, 1);
@@ -1935,7 +1946,7 @@ __global__ void __launch_bounds__(kThreads, 2) fd_split_kernel(const __grid_cons
   // empty partial: its (sequence, KV head) counter must complete and return to zero,
   // and a CTA of a cluster must still reach the cluster barriers.
   finish_cta<T, D, G, NGRP, kMode, kSeg, kPair>(p, wk, sm_acc, sm_last, sm_abort != 0, smem, kRing,
-                                         smem_addr(bars + 2 * NSLOT));
+                                         combine_bars);
 }
 
 // Two-launch ablation, second kernel: one CTA per (sequence, KV head) combines
@@ -1945,10 +1956,11 @@ __global__ void __launch_bounds__(kThreads, 2) fd_combine_kernel(const __grid_co
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw;  // bulk copies need 16-byte alignment only
   constexpr uint32_t kBytes = (uint32_t)ring_bytes_for(PATH, D);
-  uint64_t* bar = reinterpret_cast<uint64_t*>(smem + kBytes);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kBytes);  // kCombineBars of them
+  static_assert(kCombineBars * 8 <= kRingMetaBytes, "combine barriers fit after the ring");
   pdl_launch_dependents();
   if (threadIdx.x == 0) {
-    mbar_init(smem_addr(bar), 1);
+    for (int j = 0; j < kCombineBars; ++j) mbar_init(smem_addr(bars + j), 1);
     fence_mbar_init();
   }
   pdl_wait();
@@ -1956,7 +1968,7 @@ __global__ void __launch_bounds__(kThreads, 2) fd_combine_kernel(const __grid_co
   const int b = blockIdx.x / p.Hkv, kvh = blockIdx.x - (blockIdx.x / p.Hkv) * p.Hkv;
   uint32_t phase = 0;
   combine_partials<T, D, G>(p, b, kvh, p.wseg[b] * p.rps, rec_base(p, b), 0, G, smem, kBytes,
-                            smem_addr(bar), phase);
+                            smem_addr(bars), phase);
 }
 
 }  // namespace dev

@@ -182,7 +182,7 @@ def test_records_per_segment():
                           (128, 8, 9), (32, 8, 1), (64, 8, 16)):
         p = fd.fd_plan(1, Hq, 8, 128, [32768], W, "f16", chunks=chunks, num_sms=152)
         G = Hq // 8
-        slots = 152 if G == 16 else 304                     # tcgen05: one CTA per SM
+        slots = 304                                         # mma.sync: two CTAs per SM
         nc = combiners(G, 8 * W * chunks, slots, W * chunks)
         multi = G // nc * W * chunks * 132 * 4 > ring[128]
         want = 1 if (multi and 2 <= chunks <= 8) else chunks
@@ -225,8 +225,10 @@ def test_consumer_path_choice():
         assert p.info["path"] == path, G
     p = fd.fd_plan(1, 64, 8, 128, [1000], 2, "bf16", flags=fd.FD_PLAN_FFMA, num_sms=152)
     assert p.info["path"] == 0
-    # G = 16: tcgen05 at d = 128 unless mma.sync is asked for; mma.sync at d = 64
-    assert fd.fd_plan(1, 128, 8, 128, [1000], 2, "f16", num_sms=152).info["path"] == 3
+    # G = 16: mma.sync (two N tiles) unless tcgen05 is asked for
+    assert fd.fd_plan(1, 128, 8, 128, [1000], 2, "f16", num_sms=152).info["path"] == 1
+    assert fd.fd_plan(1, 128, 8, 128, [1000], 2, "f16", flags=fd.FD_PLAN_TCGEN05,
+                      num_sms=152).info["path"] == 3
     assert fd.fd_plan(1, 128, 8, 128, [1000], 2, "bf16", flags=fd.FD_PLAN_MMA_SYNC,
                       num_sms=152).info["path"] == 1
     assert fd.fd_plan(1, 128, 8, 64, [1000], 2, "f16", num_sms=152).info["path"] == 1
@@ -353,12 +355,19 @@ def test_shared_combine_plan_rules():
     assert info(1, 64, 8, 128, [131072], 8, "f16", chunks=4,
                 flags=fd.FD_PLAN_NO_CLUSTER)["combiners"] == 8                  # G = 8
     g16 = info(1, 128, 8, 128, [32768], 8, "f16")
-    assert g16["path"] == 3 and g16["ctas"] <= 152 and g16["combiners"] == 8   # G = 16, tcgen05
+    assert g16["path"] == 1 and g16["ctas"] == 256 and g16["combiners"] == 8   # G = 16
+    g16 = info(1, 128, 8, 128, [32768], 8, "f16", flags=fd.FD_PLAN_TCGEN05)
+    assert g16["path"] == 3 and g16["ctas"] <= 152 and g16["combiners"] == 8   # tcgen05
     assert info(1, 8, 8, 64, [4096], 32, "f16", flags=fd.FD_PLAN_COMBINERS[16])["combiners"] == 1
     # The flags cap it; FD_PLAN_SINGLE_COMBINER is the ablation.
     for n in (1, 2, 4, 8, 16):
         want = min(n, 16)
-        assert info(1, 128, 8, 128, [32768], 8, "f16", flags=fd.FD_PLAN_COMBINERS[n])["combiners"] == want
+        assert info(1, 128, 8, 128, [32768], 8, "f16",
+                    flags=fd.FD_PLAN_TCGEN05 | fd.FD_PLAN_COMBINERS[n])["combiners"] == want
+    # With fewer combiners each one's records outgrow the 96 KB mma.sync ring, and the
+    # chunks of a segment merge in clusters first: then the last arriver combines alone.
+    g16 = info(1, 128, 8, 128, [32768], 8, "f16", flags=fd.FD_PLAN_COMBINERS[2])
+    assert g16["records_per_segment"] == 1 and g16["combiners"] == 1
     assert info(1, 64, 8, 128, [32768], 8, "f16",
                 flags=fd.FD_PLAN_SINGLE_COMBINER)["combiners"] == 1
     # Never more combiners than partials: W = 2 literal partials, G = 16.

@@ -176,15 +176,15 @@ def test_forced_ffma_path(fd, G):
 
 @pytest.mark.parametrize("dtype,d", [("f16", 128), ("bf16", 64), ("bf16", 128)])
 def test_gqa16_tensor_core_path(fd, dtype, d):
-    """G = 16 query heads per KV head: tcgen05 by default at d = 128, two mma.sync N
-    tiles per KV tile at d = 64 or with FD_PLAN_MMA_SYNC."""
+    """G = 16 query heads per KV head: two mma.sync N tiles per KV tile by default,
+    tcgen05 at d = 128 with FD_PLAN_TCGEN05."""
     p = workloads.make_problem("gqa16", 3, 128, 8, d, [9000, 1, 2049], [4, 1, 3], dtype,
                                seed=60 + d)
     ref_out, ref_lse = oracle.decode_reference(p.q, p.k, p.v, p.seqlens, p.dtype)
-    for sync in ((False, True) if d == 128 else (False,)):
+    for tc in ((False, True) if d == 128 else (False,)):
         for flags in (0, fd.FD_PLAN_TWO_LAUNCH, fd.FD_PLAN_WAITS):
-            (out, lse), dec = run_gpu(fd, p, flags=flags | (fd.FD_PLAN_MMA_SYNC if sync else 0))
-            assert dec.info["path"] == (3 if d == 128 and not sync else 1) and dec.info["G"] == 16
+            (out, lse), dec = run_gpu(fd, p, flags=flags | (fd.FD_PLAN_TCGEN05 if tc else 0))
+            assert dec.info["path"] == (3 if tc else 1) and dec.info["G"] == 16
             check(out, lse, ref_out, ref_lse, dtype=p.dtype)
 
 
@@ -513,7 +513,8 @@ def test_pipeline_wait_timeout_leaves_workspace_clean(fd, G, flags):
 SHARED_COMBINE_CASES = {
     "gqa4_f16": ("f16", 4, 128, 3, 8, [9000, 17, 4096], [4, 2, 8], "cap", 4),
     "gqa8_bf16_literal": ("bf16", 8, 128, 3, 8, [9000, 300, 4096], [4, 1, 3], "literal", 4),
-    "gqa16_tcgen05": ("f16", 16, 128, 2, 4, [20000, 3000], [8, 3], "", 8),
+    "gqa16_mma": ("f16", 16, 128, 2, 4, [20000, 3000], [8, 3], "", 8),
+    "gqa16_tcgen05": ("f16", 16, 128, 2, 4, [20000, 3000], [8, 3], "tcgen05", 8),
     "gqa16_two_passes": ("bf16", 16, 128, 1, 2, [40000], [8], "two_passes", 2),
     "gqa4_from_l2": ("f16", 4, 128, 1, 1, [300 * 64], [300], "literal_cap", 4),
     "gqa2_d64_ffma": ("bf16", 2, 64, 2, 8, [5000, 100], [4, 4], "cap", 2),
@@ -538,6 +539,8 @@ def test_shared_combine_matches_single_combiner(fd, case):
         flags |= fd.FD_PLAN_COMBINERS[16]
     elif kind == "two_passes":
         flags, chunks = flags | fd.FD_PLAN_MMA_SYNC | fd.FD_PLAN_COMBINERS[2], 4
+    elif kind == "tcgen05":
+        flags |= fd.FD_PLAN_TCGEN05
     ref_out, ref_lse = reference(p)
     (o1, l1), dec = run_gpu(fd, p, flags=flags, chunks=chunks)
     assert dec.info["combiners"] == want
