@@ -99,6 +99,15 @@ enum fd_status {
  * nothing is skipped.  Not with
  * FD_PLAN_TEST_DROP_FLAG. */
 #define FD_PLAN_TEST_SKIP_TILE 0x200u
+/* Test hook for the shared combine's bounded wait: partial slot 1 of (sequence 0, KV
+ * head 0) publishes its partial but never arrives.  The combiners of that pair wait
+ * for the last arrival, give up after ~4 s and report FD_ERR_TIMEOUT in the status
+ * word; the pair's out/lse are not written, and its counter is left short, so the
+ * workspace needs fd_workspace_init before the next decode.  Only meaningful for a
+ * plan with fd_plan_info.combiners > 1 (with a single combiner nothing waits and the
+ * pair is simply never combined).  Not with FD_PLAN_WAITS, FD_PLAN_TWO_LAUNCH,
+ * FD_PLAN_CLUSTER_COMBINE or the other test hooks. */
+#define FD_PLAN_TEST_DROP_ARRIVAL 0x2000u
 /* Fifth-generation tensor cores (tcgen05.mma with accumulators in tensor memory)
  * for the scores and P.V: 128-token tiles, d = 128, G in {4, 8, 16}, fp16 or bf16
  * (FD_ERR_UNSUPPORTED otherwise).  Not the default: mma.sync measured faster on

@@ -38,6 +38,7 @@ FD_PLAN_TEST_SKIP_TILE = 0x200
 FD_PLAN_TCGEN05 = 0x400
 FD_PLAN_CLUSTER_COMBINE = 0x800
 FD_PLAN_MMA_SYNC = 0x1000
+FD_PLAN_TEST_DROP_ARRIVAL = 0x2000
 FD_PLAN_COMBINERS_SHIFT = 16
 FD_PLAN_COMBINERS_MASK = 7 << FD_PLAN_COMBINERS_SHIFT
 # FD_PLAN_COMBINERS[n]: at most n CTAs share the combine of one (sequence, KV head) pair.

@@ -121,7 +121,8 @@ int plan_impl(int B, int Hq, int Hkv, int d, const int32_t* seqlens, const int32
   if (flags & ~(FD_PLAN_LITERAL_W | FD_PLAN_DEBUG | FD_PLAN_TWO_LAUNCH | FD_PLAN_FFMA |
                 FD_PLAN_NO_PDL | FD_PLAN_WAITS | FD_PLAN_TEST_DROP_FLAG |
                 FD_PLAN_NO_CLUSTER | FD_PLAN_CLUSTER | FD_PLAN_TEST_SKIP_TILE | FD_PLAN_TCGEN05 |
-                FD_PLAN_CLUSTER_COMBINE | FD_PLAN_MMA_SYNC | FD_PLAN_COMBINERS_MASK))
+                FD_PLAN_CLUSTER_COMBINE | FD_PLAN_MMA_SYNC | FD_PLAN_COMBINERS_MASK |
+                FD_PLAN_TEST_DROP_ARRIVAL))
     return FD_ERR_INVALID;
   const uint32_t combiners_code = (flags & FD_PLAN_COMBINERS_MASK) >> FD_PLAN_COMBINERS_SHIFT;
   if (combiners_code > 5) return FD_ERR_INVALID;
@@ -133,6 +134,10 @@ int plan_impl(int B, int Hq, int Hkv, int d, const int32_t* seqlens, const int32
     return FD_ERR_INVALID;
   if ((flags & FD_PLAN_TEST_DROP_FLAG) && !(flags & FD_PLAN_WAITS)) return FD_ERR_INVALID;
   if ((flags & FD_PLAN_TEST_DROP_FLAG) && (flags & FD_PLAN_TEST_SKIP_TILE)) return FD_ERR_INVALID;
+  if ((flags & FD_PLAN_TEST_DROP_ARRIVAL) &&
+      (flags & (FD_PLAN_WAITS | FD_PLAN_TWO_LAUNCH | FD_PLAN_CLUSTER_COMBINE | FD_PLAN_TEST_DROP_FLAG |
+                FD_PLAN_TEST_SKIP_TILE)))
+    return FD_ERR_INVALID;
   const int G = Hq / Hkv;
   if (page_size != 0 && (page_size < 16 || page_size > 256 || (page_size & (page_size - 1))))
     return FD_ERR_UNSUPPORTED;
@@ -230,9 +235,10 @@ int plan_impl(int B, int Hq, int Hkv, int d, const int32_t* seqlens, const int32
   fd::Params& p = pl->params;
   std::memset(&p, 0, sizeof(p));
   p.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)d));
-  p.test_hook = (flags & FD_PLAN_TEST_DROP_FLAG)   ? fd::kHookDropFlag
-                : (flags & FD_PLAN_TEST_SKIP_TILE) ? fd::kHookSkipTile
-                                                   : fd::kHookNone;
+  p.test_hook = (flags & FD_PLAN_TEST_DROP_FLAG)      ? fd::kHookDropFlag
+                : (flags & FD_PLAN_TEST_SKIP_TILE)    ? fd::kHookSkipTile
+                : (flags & FD_PLAN_TEST_DROP_ARRIVAL) ? fd::kHookDropArrival
+                                                      : fd::kHookNone;
   p.B = B; p.Hq = Hq; p.Hkv = Hkv; p.C = C;
   // Only the first wave can start before the previous kernel ends; later CTAs
   // would only queue prefetches ahead of their own loads.

@@ -105,10 +105,12 @@ constexpr uint32_t kStatusCounter = 2u;
 // kHookDropFlag: partial slot 1 of (sequence 0, KV head 0) never sets its ready flag
 // (fine-grained-waits variant).  kHookSkipTile: the producer of partial slot 0 of
 // (sequence 0, KV head 0) never issues the loads of its second tile, so that CTA's
-// consumers give up waiting for it.
+// consumers give up waiting for it.  kHookDropArrival: partial slot 1 of (sequence 0,
+// KV head 0) never arrives, so the pair's combiners give up waiting for the last one.
 constexpr int32_t kHookNone = 0;
 constexpr int32_t kHookDropFlag = 1;
 constexpr int32_t kHookSkipTile = 2;
+constexpr int32_t kHookDropArrival = 3;
 
 // Kernel parameters (passed by value as a __grid_constant__ struct; < 4 KB).
 struct Params {

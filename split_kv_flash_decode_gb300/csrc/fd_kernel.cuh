@@ -1004,7 +1004,10 @@ __device__ __forceinline__ void finish_cta(const Params& p, const Work& wk, floa
   uint32_t* cnt = p.counters + (int64_t)wk.b * p.Hkv + wk.kvh;
   int nc = p.combiners;
   while (nc > wk.wtot) nc >>= 1;  // a power of two dividing G
-  if (tid == 0) {
+  const bool drop_arrival =
+      p.test_hook == kHookDropArrival && wk.b == 0 && wk.kvh == 0 && wk.slot == 1;
+  if (tid == 0 && drop_arrival) sm_last = kNotCombiner;
+  if (tid == 0 && !drop_arrival) {
     const uint32_t old = atom_add_acq_rel_gpu(cnt, 1u);
     if (old >= (uint32_t)wk.wtot) atomicOr(p.status, kStatusCounter);
     const int r = wk.wtot - 1 - (int)min(old, (uint32_t)wk.wtot);

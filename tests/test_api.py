@@ -384,3 +384,14 @@ def test_shared_combine_plan_rules():
     assert c3["records_per_segment"] == 4 and c3["combiners"] == 8
     c3 = info(1, 64, 8, 128, [131072], 8, "f16", flags=fd.FD_PLAN_SINGLE_COMBINER)
     assert c3["records_per_segment"] == 1 and c3["combiners"] == 1
+
+
+def test_drop_arrival_hook_rules():
+    """FD_PLAN_TEST_DROP_ARRIVAL: a fused one-launch plan only, not with the other hooks."""
+    ok = fd.fd_plan(1, 64, 8, 128, [32768], 8, "f16", flags=fd.FD_PLAN_TEST_DROP_ARRIVAL,
+                    num_sms=152)
+    assert ok.info["combiners"] == 8
+    for other in (fd.FD_PLAN_WAITS, fd.FD_PLAN_TWO_LAUNCH, fd.FD_PLAN_CLUSTER_COMBINE,
+                  fd.FD_PLAN_TEST_SKIP_TILE, fd.FD_PLAN_WAITS | fd.FD_PLAN_TEST_DROP_FLAG):
+        assert _raw_plan(1, 64, 8, 128, [32768], [8],
+                         flags=fd.FD_PLAN_TEST_DROP_ARRIVAL | other) == fd.FD_ERR_INVALID, hex(other)

@@ -553,6 +553,37 @@ def test_shared_combine_matches_single_combiner(fd, case):
     assert np.array_equal(o1, o2) and np.array_equal(l1, l2)
 
 
+def test_shared_combine_wait_runs_out(fd):
+    """A partial that never arrives (test hook): the pair's combiners wait for the last
+    arrival, give up after their bound (~4 s) and report FD_ERR_TIMEOUT; that pair's
+    out/lse stay untouched, every other pair is correct, and after fd_workspace_init
+    the next decode on the same workspace is correct."""
+    import torch
+    p = workloads.make_problem("drop_arrival", 2, 32, 4, 128, [5000, 700], [4, 2], "f16", seed=77)
+    ref_out, ref_lse = oracle.decode_reference(p.q, p.k, p.v, p.seqlens, p.dtype)
+    dec = fd.Decoder(p.Hq, p.Hkv, p.d, p.seqlens, p.W, p.dtype, flags=fd.FD_PLAN_TEST_DROP_ARRIVAL)
+    assert dec.info["combiners"] > 1 and dec.plan.range(0, 1)[1] > dec.plan.range(0, 1)[0]
+    q, k, v = (to_torch(x, p.dtype) for x in (p.q, p.k, p.v))
+    out = torch.full_like(q, float("nan"))
+    lse = torch.full((p.B, p.Hq), float("nan"), dtype=torch.float32, device="cuda")
+    dec(q, k, v, out, lse)
+    assert dec.status() == fd.FD_ERR_TIMEOUT
+    o, l = out_to_f64(out), lse.cpu().numpy().astype(np.float64)
+    G = p.Hq // p.Hkv
+    assert np.isnan(o[0, :G]).all() and np.isnan(l[0, :G]).all()   # the pair nobody combined
+    keep = np.ones((p.B, p.Hq), dtype=bool)
+    keep[0, :G] = False
+    assert np.abs(o[keep] - ref_out[keep]).max() <= OUT_TOL
+    assert np.abs(l[keep] - ref_lse[keep]).max() <= LSE_TOL
+    clean = fd.fd_plan(p.B, p.Hq, p.Hkv, p.d, p.seqlens, p.W, p.dtype)
+    assert clean.workspace_bytes == dec.plan.workspace_bytes
+    fd.fd_workspace_init(clean, dec.workspace)
+    out2, lse2 = torch.empty_like(q), torch.empty_like(lse)
+    fd.fd_decode(clean, q, k, v, out2, lse2, dec.workspace)
+    assert fd.fd_workspace_status(clean, dec.workspace) == fd.FD_OK
+    check(out_to_f64(out2), lse2.cpu().numpy().astype(np.float64), ref_out, ref_lse, dtype=p.dtype)
+
+
 def test_fine_grained_waits_needs_coresidency(fd):
     p = workloads.make_problem("big", 64, 32, 8, 128, [512] * 64, 16, "bf16", seed=41)
     dec = fd.Decoder(p.Hq, p.Hkv, p.d, p.seqlens, p.W, p.dtype,
