@@ -67,6 +67,8 @@ def parse_args(argv=None):
                     help="combine each (sequence, KV head) pair inside one thread-block cluster")
     ap.add_argument("--combiners", type=int, choices=[1, 2, 4, 8, 16], default=0,
                     help="cap on the CTAs that share one pair's combine (0 = planner)")
+    ap.add_argument("--deep-ring", action="store_true",
+                    help="two CTAs per SM with 96 KB rings even for many short CTAs")
     ap.add_argument("--no-pdl", action="store_true", help="launch without programmatic dependent launch")
     ap.add_argument("--no-cluster", action="store_true",
                     help="one partial record per chunk (no in-cluster segment merge)")
@@ -426,7 +428,8 @@ def plan_flags(fd, args, prob):
         fd.FD_PLAN_TCGEN05 if args.tcgen05 else 0) | (
         fd.FD_PLAN_CLUSTER_COMBINE if args.cluster_combine else 0) | (
         fd.FD_PLAN_MMA_SYNC if args.mma_sync else 0) | (
-        fd.FD_PLAN_COMBINERS[args.combiners] if args.combiners else 0)
+        fd.FD_PLAN_COMBINERS[args.combiners] if args.combiners else 0) | (
+        fd.FD_PLAN_DEEP_RING if args.deep_ring else 0)
 
 
 class CaseRun:
@@ -756,7 +759,7 @@ def run_fd(args):
                 "workload": prob.name, **prob.describe(), "accumulate": "f32",
                 "chunks_per_segment": info["chunks"], "ctas": info["ctas"],
                 "records_per_segment": info["records_per_segment"],
-                "combiners": info["combiners"],
+                "combiners": info["combiners"], "ctas_per_sm": info["ctas_per_sm"],
                 "partials_per_sequence_max": info["max_partials"],
                 "kv_bytes_per_step": kv_bytes, "two_launch": bool(args.two_launch),
                 "kv_storage": prob.kv_type,

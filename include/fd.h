@@ -108,6 +108,12 @@ enum fd_status {
  * pair is simply never combined).  Not with FD_PLAN_WAITS, FD_PLAN_TWO_LAUNCH,
  * FD_PLAN_CLUSTER_COMBINE or the other test hooks. */
 #define FD_PLAN_TEST_DROP_ARRIVAL 0x2000u
+/* Keep two CTAs per SM with 96 KB K/V rings (ablation).  Without it, a plan on the
+ * mma.sync path (G = 4 or 8, 16-bit K/V) whose CTAs do not all fit two per SM and read
+ * at most 512 KB of K/V each on average, run as one fused launch without clusters,
+ * runs three CTAs per SM with 64 KB rings: one CTA's ramp and tail then leave two
+ * others streaming (fd_plan_info.ctas_per_sm). */
+#define FD_PLAN_DEEP_RING 0x4000u
 /* Fifth-generation tensor cores (tcgen05.mma with accumulators in tensor memory)
  * for the scores and P.V: 128-token tiles, d = 128, G in {4, 8, 16}, fp16 or bf16
  * (FD_ERR_UNSUPPORTED otherwise).  Not the default: mma.sync measured faster on
@@ -330,6 +336,8 @@ typedef struct fd_plan_info {
   int32_t combiners;       /* CTAs that share the combine of one pair: a power of two
                               dividing G (fewer for a sequence with fewer partials),
                               1 = the last arriver alone */
+  int32_t ctas_per_sm;     /* resident CTAs per SM the split kernel is launched for:
+                              2 (96 KB rings), 3 (64 KB rings) or 1 (tcgen05) */
 } fd_plan_info;
 
 int fd_plan_get_info(fd_plan_t plan, fd_plan_info* info);

@@ -32,6 +32,7 @@ from ._binding import (  # noqa: F401
     FD_PLAN_TEST_DROP_FLAG,
     FD_PLAN_TEST_SKIP_TILE,
     FD_PLAN_TEST_DROP_ARRIVAL,
+    FD_PLAN_DEEP_RING,
     FD_PLAN_TCGEN05,
     FD_PLAN_CLUSTER_COMBINE,
     FD_PLAN_MMA_SYNC,

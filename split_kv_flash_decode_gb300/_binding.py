@@ -39,6 +39,7 @@ FD_PLAN_TCGEN05 = 0x400
 FD_PLAN_CLUSTER_COMBINE = 0x800
 FD_PLAN_MMA_SYNC = 0x1000
 FD_PLAN_TEST_DROP_ARRIVAL = 0x2000
+FD_PLAN_DEEP_RING = 0x4000
 FD_PLAN_COMBINERS_SHIFT = 16
 FD_PLAN_COMBINERS_MASK = 7 << FD_PLAN_COMBINERS_SHIFT
 # FD_PLAN_COMBINERS[n]: at most n CTAs share the combine of one (sequence, KV head) pair.
@@ -74,6 +75,7 @@ class PlanInfo(ctypes.Structure):
         ("workspace_bytes", ctypes.c_uint64), ("kv_bytes", ctypes.c_uint64),
         ("path", ctypes.c_int32), ("records_per_segment", ctypes.c_int32),
         ("combine_cluster", ctypes.c_int32), ("combiners", ctypes.c_int32),
+        ("ctas_per_sm", ctypes.c_int32),
     ]
 
 

@@ -29,6 +29,9 @@ constexpr int kMaxCluster = 8;        // portable thread-block cluster size
 // 22.6 us, 14.4 against 14.2 us over FP8).
 constexpr int kDefaultCombiners = 8;
 constexpr int kMinGroupForCombiners = 8;
+// Plans whose CTAs read at most this many K/V bytes on average, and that have more
+// CTAs than fit two per SM, run three CTAs per SM with 64 KB rings (fd_common.h).
+constexpr int64_t kShallowMaxCtaBytes = 512 * 1024;
 
 size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 
@@ -122,7 +125,7 @@ int plan_impl(int B, int Hq, int Hkv, int d, const int32_t* seqlens, const int32
                 FD_PLAN_NO_PDL | FD_PLAN_WAITS | FD_PLAN_TEST_DROP_FLAG |
                 FD_PLAN_NO_CLUSTER | FD_PLAN_CLUSTER | FD_PLAN_TEST_SKIP_TILE | FD_PLAN_TCGEN05 |
                 FD_PLAN_CLUSTER_COMBINE | FD_PLAN_MMA_SYNC | FD_PLAN_COMBINERS_MASK |
-                FD_PLAN_TEST_DROP_ARRIVAL))
+                FD_PLAN_TEST_DROP_ARRIVAL | FD_PLAN_DEEP_RING))
     return FD_ERR_INVALID;
   const uint32_t combiners_code = (flags & FD_PLAN_COMBINERS_MASK) >> FD_PLAN_COMBINERS_SHIFT;
   if (combiners_code > 5) return FD_ERR_INVALID;
@@ -212,7 +215,7 @@ int plan_impl(int B, int Hq, int Hkv, int d, const int32_t* seqlens, const int32
     int64_t need = (G * wt + 3 * G) * 4 + 16;                       // coefficients
     if (flags & FD_PLAN_WAITS)                                      // running state + lists
       need = std::max<int64_t>(need, (int64_t)(G * d + 4 * G + G * wt) * 4 + (2 * wt + 2) * 4);
-    if (need > (int64_t)fd::ring_bytes_for(path, d)) return FD_ERR_UNSUPPORTED;
+    if (need > (int64_t)fd::ring_bytes_for(path, d, fd::ctas_per_sm_for(path))) return FD_ERR_UNSUPPORTED;
   }
   const int64_t ctas = (int64_t)Hkv * sum_w * C;
   if (ctas >= (int64_t)1 << 31) return FD_ERR_UNSUPPORTED;
@@ -240,9 +243,6 @@ int plan_impl(int B, int Hq, int Hkv, int d, const int32_t* seqlens, const int32
                 : (flags & FD_PLAN_TEST_DROP_ARRIVAL) ? fd::kHookDropArrival
                                                       : fd::kHookNone;
   p.B = B; p.Hq = Hq; p.Hkv = Hkv; p.C = C;
-  // Only the first wave can start before the previous kernel ends; later CTAs
-  // would only queue prefetches ahead of their own loads.
-  p.prefetch_ctas = (int32_t)std::min<int64_t>(ctas, (int64_t)num_sms * fd::ctas_per_sm_for(path));
   // The last arrivals of a pair share its combine by query heads only when every CTA
   // is resident at once (the CTAs they wait for then always run), in the fused
   // one-launch mode; never more combiners than partials.
@@ -261,12 +261,28 @@ int plan_impl(int B, int Hq, int Hkv, int d, const int32_t* seqlens, const int32
   // alone.  Not in the fine-grained-waits variant, which combines chunk records as
   // they arrive.
   const int64_t rec_bytes = (int64_t)G / nc * max_w * C * fd::record_floats(d) * 4;
-  const int64_t ring = (int64_t)fd::ring_bytes_for(pl->path, d);
+  const int64_t ring = (int64_t)fd::ring_bytes_for(pl->path, d, fd::ctas_per_sm_for(path));
   const bool multi_pass = rec_bytes > (pl->path == fd::kPathMmaKv8 ? 2 : 1) * ring;
   p.rps = ((multi_pass || (flags & FD_PLAN_CLUSTER)) && C > 1 && C <= kMaxCluster &&
            !(flags & (FD_PLAN_WAITS | FD_PLAN_NO_CLUSTER | FD_PLAN_CLUSTER_COMBINE))) ? 1 : C;
   if (p.rps != C) nc = 1;
   p.combiners = nc;
+  // Many short CTAs on the fused mma.sync path, G <= 8 (more CTAs than two per SM,
+  // at most kShallowMaxCtaBytes of K/V each): three CTAs per SM with 64 KB rings.
+  {
+    const int64_t kv_bytes = n_tokens * Hkv * d * 2 * fd::kv_elem_bytes(path);
+    const int64_t slots = (int64_t)num_sms * fd::ctas_per_sm_for(path);
+    const int64_t wt = (int64_t)max_w * C;
+    const bool shallow =
+        path == fd::kPathMma && G <= 8 && !pair && p.rps == C &&
+        !(flags & (FD_PLAN_TWO_LAUNCH | FD_PLAN_WAITS | FD_PLAN_DEEP_RING)) && ctas > slots &&
+        kv_bytes <= ctas * kShallowMaxCtaBytes &&
+        (G * wt + 3 * G) * 4 + 16 <= (int64_t)fd::ring_bytes_for(path, d, fd::kShallowCtasPerSm);
+    p.ctas_per_sm = shallow ? fd::kShallowCtasPerSm : fd::ctas_per_sm_for(path);
+  }
+  // Only the first wave can start before the previous kernel ends; later CTAs
+  // would only queue prefetches ahead of their own loads.
+  p.prefetch_ctas = (int32_t)std::min<int64_t>(ctas, (int64_t)num_sms * p.ctas_per_sm);
   p.pair_cluster = pair ? W[0] * C : 0;
   // Paged caches: boundaries on whole tiles, so that every TMA box stays in one page.
   p.align = page_size ? fd::tile_for(pl->path) : 1;
@@ -334,6 +350,7 @@ int fd_plan_get_info(fd_plan_t pl, fd_plan_info* info) {
   info->records_per_segment = pl->params.rps;
   info->combine_cluster = pl->params.pair_cluster;
   info->combiners = pl->params.combiners;
+  info->ctas_per_sm = pl->params.ctas_per_sm;
   return FD_OK;
 }
 

@@ -66,14 +66,27 @@ constexpr int kRingBytes = 96 * 1024;
 // calculator reports 1 for any such kernel, whatever its shared memory), so that
 // path gets the bytes in flight of two CTAs of the other paths: a 192 KB ring.
 FD_HD constexpr int ctas_per_sm_for(int path) { return path == kPathUmma ? 1 : 2; }
-FD_HD constexpr int ring_target_bytes(int path) { return path == kPathUmma ? 2 * kRingBytes : kRingBytes; }
+// Plans of many short CTAs on the mma.sync path run three CTAs per SM with 64 KB
+// rings instead (kShallowCtasPerSm): one CTA's ramp and tail then leave two others
+// streaming.  (Measured on 64 sequences of 8K tokens: 512-token CTAs 305.2 against
+// 314.2 us, 1024-token CTAs 299.8 against 301.2 us; 2048 tokens even; 4096 and more
+// tokens per CTA, and every one-wave plan, slower.)
+constexpr int kShallowCtasPerSm = 3;
+constexpr int kShallowRingBytes = 64 * 1024;
+FD_HD constexpr int ring_target_bytes(int path, int cps) {
+  return path == kPathUmma ? 2 * kRingBytes : cps == kShallowCtasPerSm ? kShallowRingBytes : kRingBytes;
+}
 FD_HD constexpr int slot_bytes_for(int path, int d) {
   return (2 / loads_per_tile(path)) * tile_for(path) * d * kv_elem_bytes(path);
 }
-FD_HD constexpr int ring_slots_for(int path, int d) { return ring_target_bytes(path) / slot_bytes_for(path, d); }
+// `cps`: resident CTAs per SM the kernel is built for (ctas_per_sm_for, or
+// kShallowCtasPerSm).
+FD_HD constexpr int ring_slots_for(int path, int d, int cps) {
+  return ring_target_bytes(path, cps) / slot_bytes_for(path, d);
+}
 // Bytes of the K/V ring (also the scratch the combine reuses).
-FD_HD constexpr size_t ring_bytes_for(int path, int d) {
-  return (size_t)ring_slots_for(path, d) * slot_bytes_for(path, d);
+FD_HD constexpr size_t ring_bytes_for(int path, int d, int cps) {
+  return (size_t)ring_slots_for(path, d, cps) * slot_bytes_for(path, d);
 }
 // Bytes after the ring: 2 mbarriers per slot, an unused word, two flags, the
 // tcgen05 path's two mbarriers and tensor-memory address, the combine's 16
@@ -84,8 +97,8 @@ constexpr int kRingMetaBytes = 2048;
 // 4 KB) and 1 KB of reduction scratch.
 FD_HD constexpr int extra_bytes_for(int path) { return path == kPathUmma ? 9216 : 0; }
 // Dynamic shared memory of one CTA: the ring, the extra operands and the metadata.
-FD_HD constexpr size_t smem_bytes_for(int path, int d) {
-  return ring_bytes_for(path, d) + extra_bytes_for(path) + kRingMetaBytes;
+FD_HD constexpr size_t smem_bytes_for(int path, int d, int cps) {
+  return ring_bytes_for(path, d, cps) + extra_bytes_for(path) + kRingMetaBytes;
 }
 // Floats per partial record: O[0..d), m, l, l~ and a pad word (16-byte records).
 // l sums the fp32 softmax weights (it gives lse); l~ sums the weights as rounded
@@ -141,6 +154,9 @@ struct Params {
   // CTAs that share the combine of one (sequence, KV head) pair: the last
   // `combiners` arrivals (a power of two dividing G; 1 = the last arriver alone).
   int32_t combiners;
+  // Resident CTAs per SM the split kernel is launched for: ctas_per_sm_for(path), or
+  // kShallowCtasPerSm (64 KB rings) for plans of many short CTAs on the mma.sync path.
+  int32_t ctas_per_sm;
   float scale_log2;    // log2(e) / sqrt(d)
   int32_t B, Hq, Hkv, C;
   int32_t cu[FD_MAX_BATCH + 1];         // token prefix sums

@@ -1043,14 +1043,16 @@ __device__ __forceinline__ void finish_cta(const Params& p, const Work& wk, floa
 // segment's chunk partials merged inside a thread-block cluster (rps == 1).
 // MODE 6: fused, every partial of a (sequence, KV head) in one thread-block cluster
 // that combines them through distributed shared memory.
-template <typename T, int D, int G, int PATH, int MODE>
-__global__ void __launch_bounds__(kThreads, 2) fd_split_kernel(const __grid_constant__ Params p) {
+// CPS: resident CTAs per SM the kernel is built for; 3 (kShallowCtasPerSm) gives it
+// the 64 KB ring of plans of many short CTAs (mma.sync path, fused), else 2.
+template <typename T, int D, int G, int PATH, int MODE, int CPS = 2>
+__global__ void __launch_bounds__(kThreads, CPS) fd_split_kernel(const __grid_constant__ Params p) {
   constexpr bool kSeg = MODE == 4 || MODE == 5;
   constexpr bool kPair = MODE == 6;
   constexpr int kMode = kSeg ? MODE - 4 : kPair ? 0 : MODE;
   constexpr int TILE = tile_for(PATH);
   constexpr int LPT = loads_per_tile(PATH);       // ring slots per tile (2: K and V apart)
-  constexpr int NSLOT = ring_slots_for(PATH, D);  // ring slots
+  constexpr int NSLOT = ring_slots_for(PATH, D, CPS);  // ring slots
   constexpr int BOXC = box_cols_for(PATH, D);   // columns per TMA box
   constexpr int NBOX = D / BOXC;                // boxes per tensor per stage
   constexpr int KVES = kv_elem_bytes(PATH);     // bytes per stored K/V element
@@ -1060,7 +1062,7 @@ __global__ void __launch_bounds__(kThreads, 2) fd_split_kernel(const __grid_cons
   constexpr uint32_t kExtra = extra_bytes_for(PATH);
   static_assert(NSLOT >= 2 && kRowsBytes % 1024 == 0, "slots hold whole swizzle atoms");
   static_assert((2 * NSLOT + 5 + kCombineBars) * 8 + 1024 <= kRingMetaBytes, "ring metadata must fit");
-  static_assert(kRing == ring_bytes_for(PATH, D), "ring layout");
+  static_assert(kRing == ring_bytes_for(PATH, D, CPS), "ring layout");
   constexpr int NGRP_FFMA = kConsumerWarps * (32 / ((G * D > 512) ? 16 : 8));
   constexpr int NGRP = PATH == kPathUmma ? 1 : is_mma(PATH) ? kConsumerWarps : NGRP_FFMA;
   static_assert(PATH == kPathFfma || G >= 4, "the MMA path needs G >= 4 heads on N");
@@ -1958,7 +1960,7 @@ template <typename T, int D, int G, int PATH>
 __global__ void __launch_bounds__(kThreads, 2) fd_combine_kernel(const __grid_constant__ Params p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw;  // bulk copies need 16-byte alignment only
-  constexpr uint32_t kBytes = (uint32_t)ring_bytes_for(PATH, D);
+  constexpr uint32_t kBytes = (uint32_t)ring_bytes_for(PATH, D, 2);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kBytes);  // kCombineBars of them
   static_assert(kCombineBars * 8 <= kRingMetaBytes, "combine barriers fit after the ring");
   pdl_launch_dependents();
@@ -1978,16 +1980,24 @@ __global__ void __launch_bounds__(kThreads, 2) fd_combine_kernel(const __grid_co
 
 template <typename T, int D, int G, int PATH>
 cudaError_t launch_dgp(const Params& p, int mode, bool pdl, int grid, cudaStream_t stream) {
-  const size_t smem = smem_bytes_for(PATH, D);
+  // The shallow-ring build exists for the fused mma.sync kernel with G <= 8 only (the
+  // planner asks for it nowhere else; at G = 16 it would not fit its registers).
+  constexpr bool kHasShallow = PATH == kPathMma && G <= 8;
+  const bool shallow = kHasShallow && mode == 0 && p.ctas_per_sm == kShallowCtasPerSm;
+  const size_t smem = smem_bytes_for(PATH, D, shallow ? kShallowCtasPerSm : 2);
   // The split kernels of plans that merge segments in clusters are separate
   // instantiations (kernel modes 4 and 5).
   // Mode 6 (every partial of a pair in one cluster) comes from the host; the split
   // kernels of plans that merge segments in clusters are kernel modes 4 and 5.
   const bool seg = mode <= 1 && p.rps != p.C;
-  const int kmode = seg ? mode + 4 : mode;
+  const int kmode = seg ? mode + 4 : shallow ? 7 : mode;
   const void* fn;
   switch (kmode) {
     case 0: fn = reinterpret_cast<const void*>(&dev::fd_split_kernel<T, D, G, PATH, 0>); break;
+    case 7:
+      fn = reinterpret_cast<const void*>(
+          &dev::fd_split_kernel<T, D, G, PATH, 0, kHasShallow ? kShallowCtasPerSm : 2>);
+      break;
     case 1: fn = reinterpret_cast<const void*>(&dev::fd_split_kernel<T, D, G, PATH, 1>); break;
     case 2: fn = reinterpret_cast<const void*>(&dev::fd_combine_kernel<T, D, G, PATH>); break;
     case 3: fn = reinterpret_cast<const void*>(&dev::fd_split_kernel<T, D, G, PATH, 3>); break;
@@ -2000,7 +2010,7 @@ cudaError_t launch_dgp(const Params& p, int mode, bool pdl, int grid, cudaStream
   if (err != cudaSuccess) return err;
   // The opt-in shared-memory size (and, for clusters of more than 8 CTAs, the
   // non-portable cluster size) are per-device function attributes.
-  static uint64_t done_mask[7] = {0, 0, 0, 0, 0, 0, 0};
+  static uint64_t done_mask[8] = {0, 0, 0, 0, 0, 0, 0, 0};
   const uint64_t bit = 1ull << (dev_id & 63);
   if (!(__atomic_load_n(&done_mask[kmode], __ATOMIC_ACQUIRE) & bit)) {
     err = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);

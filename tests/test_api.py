@@ -395,3 +395,25 @@ def test_drop_arrival_hook_rules():
                   fd.FD_PLAN_TEST_SKIP_TILE, fd.FD_PLAN_WAITS | fd.FD_PLAN_TEST_DROP_FLAG):
         assert _raw_plan(1, 64, 8, 128, [32768], [8],
                          flags=fd.FD_PLAN_TEST_DROP_ARRIVAL | other) == fd.FD_ERR_INVALID, hex(other)
+
+
+def test_shallow_ring_plan_rule():
+    """Three CTAs per SM with 64 KB rings for many short CTAs on the fused mma.sync path
+    (G = 4 or 8, more CTAs than two per SM, <= 512 KB of K/V per CTA); two otherwise."""
+    def cps(*a, flags=0, **k):
+        return fd.fd_plan(*a, flags=flags, num_sms=152, **k).info["ctas_per_sm"]
+    lw = fd.FD_PLAN_LITERAL_W
+    # 64 sequences of 8K tokens, bf16: W = 16 and 8 (512 / 1024-token CTAs) shallow,
+    # W <= 4 (2048 tokens and more) not.
+    for W, want in ((16, 3), (8, 3), (4, 2), (2, 2), (1, 2)):
+        assert cps(64, 32, 8, 128, [8192] * 64, W, "bf16", flags=lw) == want, W
+    assert cps(64, 64, 8, 128, [8192] * 64, 16, "bf16", flags=lw) == 3          # G = 8
+    assert cps(64, 128, 8, 128, [8192] * 64, 16, "bf16", flags=lw) == 2         # G = 16
+    assert cps(64, 16, 8, 128, [8192] * 64, 16, "bf16", flags=lw) == 2          # G = 2: CUDA cores
+    assert cps(64, 32, 8, 128, [8192] * 64, 16, "f16_e4m3kv", flags=lw) == 2    # FP8 path
+    assert cps(64, 32, 8, 128, [8192] * 64, 16, "bf16", flags=lw | fd.FD_PLAN_TCGEN05) == 1
+    for other in (fd.FD_PLAN_DEEP_RING, fd.FD_PLAN_TWO_LAUNCH, fd.FD_PLAN_CLUSTER_COMBINE):
+        assert cps(64, 32, 8, 128, [8192] * 64, 16, "bf16", flags=lw | other) in (1, 2), hex(other)
+    # One-wave plans keep two CTAs per SM.
+    assert cps(1, 32, 8, 128, [32768], 8, "f16") == 2
+    assert cps(16, 32, 8, 128, [4096] * 16, 2, "f16") == 2

@@ -146,6 +146,32 @@ def test_batch64_bf16_w_sweep_deterministic(fd):
         check(out0, lse0, ref_out, ref_lse)
 
 
+@pytest.mark.parametrize("dtype,G,d", [("bf16", 4, 128), ("f16", 8, 128), ("bf16", 4, 64)])
+def test_shallow_ring_matches_deep_ring(fd, dtype, G, d):
+    """Many short CTAs: the three-per-SM build (64 KB rings) agrees with the oracle and,
+    bit for bit, with the two-per-SM build (FD_PLAN_DEEP_RING): the ring depth changes
+    the schedule, not the arithmetic."""
+    rs = np.random.default_rng(140 + G + d)
+    lens = [int(x) for x in rs.integers(1, 3000, size=40)] + [0, 1, 64, 4096]
+    p = workloads.make_problem("shallow", len(lens), 8 * G, 8, d, lens, 8, dtype, seed=141 + G + d)
+    ref_out, ref_lse = oracle.decode_reference(p.q, p.k, p.v, p.seqlens, p.dtype)
+    (o1, l1), dec = run_gpu(fd, p)
+    assert dec.info["ctas_per_sm"] == 3 and dec.info["ctas"] > 2 * 152
+    check(o1, l1, ref_out, ref_lse, dtype=dtype)
+    (o2, l2), dec2 = run_gpu(fd, p, flags=fd.FD_PLAN_DEEP_RING)
+    assert dec2.info["ctas_per_sm"] == 2 and dec2.info["chunks"] == dec.info["chunks"]
+    assert np.array_equal(o1, o2) and np.array_equal(l1, l2)
+
+
+def test_shallow_ring_batch64_w16(fd):
+    """The default bench case on the shallow ring: bitwise equal to the deep ring."""
+    p = workloads.batch64_gqa4_d128_L8k_bf16(W=16)
+    (o1, l1), dec = run_gpu(fd, p)
+    assert dec.info["ctas_per_sm"] == 3
+    (o2, l2), _ = run_gpu(fd, p, flags=fd.FD_PLAN_DEEP_RING)
+    assert np.array_equal(o1, o2) and np.array_equal(l1, l2)
+
+
 # ---------------------------------------------------------------------------
 # Edge shapes: tile boundaries, W beyond L, every G and d, both dtypes.
 # ---------------------------------------------------------------------------
