@@ -95,9 +95,8 @@ enum fd_status {
  * still arrives, so every arrival counter returns to zero; the status word
  * reports FD_ERR_TIMEOUT and the out/lse of (sequence 0, KV head 0) lack that
  * partial.  Needs L_0 large enough for slot 0 to span two tiles (128 tokens with
- * FD_PLAN_TCGEN05, 64 on the other tensor-core paths, 32 on CUDA cores); otherwise
- * nothing is skipped.  Not with
- * FD_PLAN_TEST_DROP_FLAG. */
+ * FD_PLAN_TCGEN05 or an E4M3 cache, 64 on the other tensor-core paths, 32 on CUDA
+ * cores); otherwise nothing is skipped.  Not with FD_PLAN_TEST_DROP_FLAG. */
 #define FD_PLAN_TEST_SKIP_TILE 0x200u
 /* Test hook for the shared combine's bounded wait: partial slot 1 of (sequence 0, KV
  * head 0) publishes its partial but never arrives.  The combiners of that pair wait
@@ -117,8 +116,8 @@ enum fd_status {
 /* Fifth-generation tensor cores (tcgen05.mma with accumulators in tensor memory)
  * for the scores and P.V: 128-token tiles, d = 128, G in {4, 8, 16}, fp16 or bf16
  * (FD_ERR_UNSUPPORTED otherwise).  Not the default: mma.sync measured faster on
- * every decode case measured once the combine is shared (G = 16 at 32K tokens: 24.9 against
- * 24.2 us).  A kernel with tcgen05 instructions is resident one CTA per SM, so these
+ * every decode case measured once the combine is shared (G = 16 at 32K tokens: 24.9
+ * against 24.2 us).  A kernel with tcgen05 instructions is resident one CTA per SM, so these
  * plans size their grid for one CTA per SM and give it a 192 KB K/V ring.
  * S^T = K Q^T runs with the tokens on M and the heads, padded to 16, on N, straight
  * from the TMA-swizzled K tile; P^T is staged in shared memory; O^T = V^T P^T
