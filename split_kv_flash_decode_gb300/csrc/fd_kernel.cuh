@@ -200,6 +200,7 @@ struct Elem;
 
 template <>
 struct Elem<__half> {
+  static constexpr int kMantissaBits = 11;  // significant bits, implicit one included
   static __device__ __forceinline__ float2 to_f2(uint32_t u) {
     __half2 h;
     *reinterpret_cast<uint32_t*>(&h) = u;
@@ -210,6 +211,7 @@ struct Elem<__half> {
 
 template <>
 struct Elem<__nv_bfloat16> {
+  static constexpr int kMantissaBits = 8;
   // bf16 is the upper half of an fp32 bit pattern: widening is exact.
   static __device__ __forceinline__ float2 to_f2(uint32_t u) {
     return make_float2(__uint_as_float(u << 16), __uint_as_float(u & 0xffff0000u));
@@ -1678,6 +1680,11 @@ __global__ void __launch_bounds__(kThreads, CPS) fd_split_kernel(const __grid_co
       lA[nt] = lB[nt] = lrA[nt] = lrB[nt] = 0.f;
     }
     const float scale = p.scale_log2;
+    // bf16 weights carry 8 significant bits: a weight rounded once is off by up to
+    // 2^-9 of itself, which over a few tokens moves out by more than the tolerance.
+    // So P.V takes each bf16 weight as hi + lo (two bf16 values, 16 significant bits
+    // together) in two mma; f16 (11 bits) needs no split.
+    constexpr bool kSplitP = Elem<T>::kMantissaBits < 11;
     const int tok0 = warp * 16;
     const int krow = tok0 + (mj & 1) * 8 + mr;   // K rows this lane addresses (A = K)
     const int vrow = tok0 + (mj >> 1) * 8 + mr;  // V rows this lane addresses (A = V^T)
@@ -1715,7 +1722,7 @@ __global__ void __launch_bounds__(kThreads, CPS) fd_split_kernel(const __grid_co
 #pragma unroll
           for (int i = 0; i < 4; ++i) sc[nt][i] += sd[nt][i];
         const bool v0 = tok0 + qrow < ntok, v1 = tok0 + qrow + 8 < ntok;
-        uint32_t pb0[NT], pb1[NT];
+        uint32_t pb0[NT], pb1[NT], pc0[NT], pc1[NT];
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
           const float sA0 = v0 ? sc[nt][0] * scale : -INFINITY;
@@ -1753,8 +1760,17 @@ __global__ void __launch_bounds__(kThreads, CPS) fd_split_kernel(const __grid_co
           // lr sums the same 16-bit weights that P.V multiplies (numerator and
           // normaliser of out see one set of weights).
           const float2 w0 = Elem<T>::to_f2(r0), w1 = Elem<T>::to_f2(r1);
-          lrA[nt] += w0.x + w1.x;
-          lrB[nt] += w0.y + w1.y;
+          if constexpr (kSplitP) {
+            const uint32_t t0 = pack2<T>(pA0 - w0.x, pB0 - w0.y), t1 = pack2<T>(pA1 - w1.x, pB1 - w1.y);
+            const float2 z0 = Elem<T>::to_f2(t0), z1 = Elem<T>::to_f2(t1);
+            lrA[nt] += (w0.x + z0.x) + (w1.x + z1.x);
+            lrB[nt] += (w0.y + z0.y) + (w1.y + z1.y);
+            pc0[nt] = movmatrix_trans(t0);
+            pc1[nt] = movmatrix_trans(t1);
+          } else {
+            lrA[nt] += w0.x + w1.x;
+            lrB[nt] += w0.y + w1.y;
+          }
           // P (tokens x heads, accumulator layout) -> P^T as the B operand (k = token).
           pb0[nt] = movmatrix_trans(r0);
           pb1[nt] = movmatrix_trans(r1);
@@ -1764,7 +1780,10 @@ __global__ void __launch_bounds__(kThreads, CPS) fd_split_kernel(const __grid_co
           uint32_t a[4];
           ldmatrix_x4_trans(a, swz_addr(vbase, TILE, vrow, 2 * mi + (mj & 1)));
 #pragma unroll
-          for (int nt = 0; nt < NT; ++nt) mma16816<T>(o[nt][mi], a, pb0[nt], pb1[nt]);
+          for (int nt = 0; nt < NT; ++nt) {
+            mma16816<T>(o[nt][mi], a, pb0[nt], pb1[nt]);
+            if constexpr (kSplitP) mma16816<T>(o[nt][mi], a, pc0[nt], pc1[nt]);
+          }
         }
       }
       __syncwarp();

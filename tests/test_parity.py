@@ -163,6 +163,23 @@ def test_shallow_ring_matches_deep_ring(fd, dtype, G, d):
     assert np.array_equal(o1, o2) and np.array_equal(l1, l2)
 
 
+@pytest.mark.parametrize("page_size", [16, 64])
+def test_shallow_ring_paged(fd, page_size):
+    """Many short CTAs over a paged cache: the three-per-SM build against the oracle and,
+    bit for bit, against the two-per-SM build."""
+    rs = np.random.default_rng(150 + page_size)
+    lens = [int(x) for x in rs.integers(1, 2500, size=44)]
+    p = workloads.make_problem("shallow_paged", len(lens), 32, 8, 128, lens, 8, "bf16",
+                               seed=151 + page_size)
+    ref_out, ref_lse = oracle.decode_reference(p.q, p.k, p.v, p.seqlens, p.dtype)
+    o1, l1, dec, _ = run_paged(fd, p, page_size)
+    assert dec.info["ctas_per_sm"] == 3
+    check(o1, l1, ref_out, ref_lse, dtype=p.dtype)
+    o2, l2, dec2, _ = run_paged(fd, p, page_size, flags=fd.FD_PLAN_DEEP_RING)
+    assert dec2.info["ctas_per_sm"] == 2
+    assert np.array_equal(o1, o2) and np.array_equal(l1, l2)
+
+
 def test_shallow_ring_batch64_w16(fd):
     """The default bench case on the shallow ring: bitwise equal to the deep ring."""
     p = workloads.batch64_gqa4_d128_L8k_bf16(W=16)
