@@ -94,8 +94,8 @@ FD_HD constexpr size_t ring_bytes_for(int path, int d, int cps) {
 // to 1024 bytes.
 constexpr int kRingMetaBytes = 2048;
 // The tcgen05 path's operands outside the ring: Q (16 x 128, 4 KB), P^T (128 x 16,
-// 4 KB) and 1 KB of reduction scratch.
-FD_HD constexpr int extra_bytes_for(int path) { return path == kPathUmma ? 9216 : 0; }
+// 4 KB), 1 KB of reduction scratch, and P^T's low part for bf16 weights (4 KB).
+FD_HD constexpr int extra_bytes_for(int path) { return path == kPathUmma ? 13312 : 0; }
 // Dynamic shared memory of one CTA: the ring, the extra operands and the metadata.
 FD_HD constexpr size_t smem_bytes_for(int path, int d, int cps) {
   return ring_bytes_for(path, d, cps) + extra_bytes_for(path) + kRingMetaBytes;

@@ -1239,7 +1239,11 @@ __global__ void __launch_bounds__(kThreads, CPS) fd_split_kernel(const __grid_co
     uint8_t* qs = smem + kRing;        // Q: 16 rows x 128, two 64-column 128-byte-swizzled halves
     uint8_t* ps = qs + 4096;           // P^T: 128 token rows x 16 heads, 32-byte swizzle
     float* wmax = reinterpret_cast<float*>(qs + 8192);  // [4 warps][16] per-warp tile maxima
-    const uint32_t qs_a = smem_addr(qs), ps_a = smem_addr(ps);
+    // bf16: the residuals of the rounded weights, P^T's second part (same layout); P.V
+    // takes hi + lo, 16 significant bits (a weight rounded once to bf16 is off by up
+    // to 2^-9 of itself, enough over a few tokens to move out past the tolerance).
+    uint8_t* ps_lo = qs + 9216;
+    const uint32_t qs_a = smem_addr(qs), ps_a = smem_addr(ps), ps_lo_a = smem_addr(ps_lo);
 
     // Q into shared memory (zero rows for the padding heads).
     for (int c = tid; c < NP * (D / 8); c += 4 * 32) {
@@ -1283,6 +1287,13 @@ __global__ void __launch_bounds__(kThreads, CPS) fd_split_kernel(const __grid_co
                        tc::smem_desc(va + kk * 2048, TILE * 128, 1024, tc::kSwizzle128B),
                        tc::smem_desc(ps_a + kk * 512, 16, 256, tc::kSwizzle32B),
                        kIdO, (kt > 0 || kk > 0) ? 1u : 0u);
+      if constexpr (kBf16) {
+#pragma unroll
+        for (int kk = 0; kk < TILE / 16; ++kk)
+          tc::mma_f16_ss(tmem + kColO,
+                         tc::smem_desc(va + kk * 2048, TILE * 128, 1024, tc::kSwizzle128B),
+                         tc::smem_desc(ps_lo_a + kk * 512, 16, 256, tc::kSwizzle32B), kIdO, 1u);
+      }
       tc::commit(empty_bar(s));
       return true;
     };
@@ -1351,7 +1362,7 @@ __global__ void __launch_bounds__(kThreads, CPS) fd_split_kernel(const __grid_co
         }
       }
       // P^T row of token tid (zero for padding heads and masked tokens).
-      uint32_t pk[NP / 2];
+      uint32_t pk[NP / 2], pl[NP / 2];
 #pragma unroll
       for (int i = 0; i < NP / 2; ++i) {
         if (2 * i < G) {
@@ -1360,17 +1371,32 @@ __global__ void __launch_bounds__(kThreads, CPS) fd_split_kernel(const __grid_co
           l_ex[2 * i + 1] += pb;
           pk[i] = pack2<T>(pa, pb);
           const float2 w = Elem<T>::to_f2(pk[i]);
-          l_rd[2 * i] += w.x;
-          l_rd[2 * i + 1] += w.y;
+          if constexpr (kBf16) {
+            pl[i] = pack2<T>(pa - w.x, pb - w.y);
+            const float2 z = Elem<T>::to_f2(pl[i]);
+            l_rd[2 * i] += w.x + z.x;
+            l_rd[2 * i + 1] += w.y + z.y;
+          } else {
+            pl[i] = 0u;
+            l_rd[2 * i] += w.x;
+            l_rd[2 * i + 1] += w.y;
+          }
         } else {
           pk[i] = 0u;
+          pl[i] = 0u;
         }
       }
       {
-        uint8_t* prow = ps + (tid >> 3) * 256 + (tid & 7) * 32;
+        const uint32_t roff = (tid >> 3) * 256 + (tid & 7) * 32;
         const int sw = (tid >> 2) & 1;  // 32-byte swizzle: 16-byte halves swap in rows 4..7
+        uint8_t* prow = ps + roff;
         *reinterpret_cast<uint4*>(prow + (sw << 4)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
         *reinterpret_cast<uint4*>(prow + ((sw ^ 1) << 4)) = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+        if constexpr (kBf16) {
+          uint8_t* lrow = ps_lo + roff;
+          *reinterpret_cast<uint4*>(lrow + (sw << 4)) = make_uint4(pl[0], pl[1], pl[2], pl[3]);
+          *reinterpret_cast<uint4*>(lrow + ((sw ^ 1) << 4)) = make_uint4(pl[4], pl[5], pl[6], pl[7]);
+        }
       }
       tc::fence_proxy_async_smem();
       tc::fence_before_sync();
